@@ -1,0 +1,192 @@
+"""ctypes front end of the fp64 C oracle (``txl_oracle.c``) and the FIFO memory semantics.
+
+TEST INFRASTRUCTURE ONLY -- see the package docstring.  All arithmetic of the method lives in
+``txl_oracle.c``; this module only converts arrays to float64 and passes pointers, except for
+``ring_push``/``ring_logical``, which restate the FIFO memory of "Transformer-XL架构解析" §1.1
+(the newest segment evicts the oldest cached positions) with plain per-position loops.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "txl_oracle.c")
+_SO = os.path.join(_HERE, "_txl_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_dp = ctypes.POINTER(ctypes.c_double)
+_ip = ctypes.POINTER(ctypes.c_int)
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc into ``oracle/_txl_oracle.so`` (host-specific, git-ignored)."""
+    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
+        tmp = _SO + ".tmp%d" % os.getpid()
+        cmd = ["gcc", "-O2", "-std=c11", "-shared", "-fPIC", "-o", tmp, _SRC, "-lm", "-lpthread"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _SO)
+    return _SO
+
+
+def library():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_SO)
+            lib.txlo_sinusoid.argtypes = [ctypes.c_double, ctypes.c_int, _dp]
+            lib.txlo_sinusoid.restype = None
+            lib.txlo_rel_table.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                           _dp, ctypes.c_int64, _dp]
+            lib.txlo_rel_table.restype = None
+            lib.txlo_score_terms.argtypes = [ctypes.c_int, _dp, _dp, _dp, _dp, _dp, _dp]
+            lib.txlo_score_terms.restype = ctypes.c_double
+            lib.txlo_rel_attn.argtypes = [ctypes.c_int] * 8 + [_dp] * 6 + [
+                ctypes.c_int64, ctypes.c_double, _dp, ctypes.c_int, ctypes.c_int, _ip, ctypes.c_int64]
+            lib.txlo_rel_attn.restype = ctypes.c_int
+            lib.txlo_stream_attn.argtypes = [ctypes.c_int] * 8 + [_dp] * 6 + [
+                ctypes.c_int64, ctypes.c_double, _dp, ctypes.c_int, ctypes.c_int, _ip, ctypes.c_int64]
+            lib.txlo_stream_attn.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _f64(a) -> np.ndarray:
+    """float64, C-contiguous copy of a numpy array or a CPU torch tensor (bf16 upcast exactly)."""
+    if hasattr(a, "detach"):
+        a = a.detach().to("cpu")
+        import torch  # local: only when a tensor is passed
+        a = a.to(torch.float64).numpy()
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _p(a: np.ndarray):
+    return a.ctypes.data_as(_dp)
+
+
+def _threads(n):
+    return int(n) if n else (os.cpu_count() or 1)
+
+
+def sinusoid(delta: float, d_model: int) -> np.ndarray:
+    out = np.empty(d_model, dtype=np.float64)
+    library().txlo_sinusoid(float(delta), int(d_model), _p(out))
+    return out
+
+
+def rel_table(n_rows: int, d_model: int, H: int, D: int, W_R) -> np.ndarray:
+    """r[delta][h][d] = sum_m R_delta[m] W_R[m][h*D+d] for delta = 0..n_rows-1."""
+    W = _f64(W_R)
+    assert W.shape[0] == d_model and W.shape[1] >= H * D
+    out = np.empty((n_rows, H, D), dtype=np.float64)
+    library().txlo_rel_table(n_rows, d_model, H, D, _p(W), W.shape[1], _p(out))
+    return out
+
+
+def score_terms(q, k, r, u, v):
+    """Four-term relative score for explicit vectors; returns (sum, [a, b, c, d])."""
+    q, k, r, u, v = (_f64(x).reshape(-1) for x in (q, k, r, u, v))
+    D = q.shape[0]
+    terms = np.empty(4, dtype=np.float64)
+    s = library().txlo_score_terms(D, _p(q), _p(k), _p(r), _p(u), _p(v), _p(terms))
+    return s, terms
+
+
+def _sel(rows):
+    if rows is None:
+        return None, 0
+    sel = np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 3))
+    return sel, sel.shape[0]
+
+
+def rel_attn(q, k, v, u, vb, W_R, M: int, mem_valid: int, clamp_len: int, scale=None,
+             memo: bool = True, threads=None, rows=None) -> np.ndarray:
+    """One call over [memory ++ current].
+
+    q [B,L,H,D]; k, v [B,M+L,H,D] in logical order (memory first); u, vb [H,D];
+    W_R [d_model, >=H*D].  ``rows``: optional (b, h, i) triples; other rows come back NaN.
+    """
+    q, k, v, u, vb, W = (_f64(x) for x in (q, k, v, u, vb, W_R))
+    B, L, H, D = q.shape
+    assert k.shape == (B, M + L, H, D) and v.shape == k.shape
+    d_model = W.shape[0]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    out = np.full((B, L, H, D), np.nan, dtype=np.float64)
+    sel, n_sel = _sel(rows)
+    rc = library().txlo_rel_attn(
+        B, L, H, D, M, mem_valid, clamp_len, d_model, _p(q), _p(k), _p(v), _p(u), _p(vb), _p(W),
+        W.shape[1], float(scale), _p(out), int(bool(memo)), _threads(threads),
+        sel.ctypes.data_as(_ip) if sel is not None else None, n_sel)
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return out
+
+
+def stream_attn(q, k, v, u, vb, W_R, L: int, M: int, clamp_len: int, scale=None,
+                memo: bool = True, threads=None, rows=None) -> np.ndarray:
+    """Segment recurrence evaluated on the concatenated sequence.
+
+    q, k, v [B, S*L, H, D] hold all S segments back to back.  A query at global position t
+    (segment s = t // L) sees keys g in [max(0, s*L - M), t] with distance t - g.
+    ``rows``: optional (b, h, t) triples.
+    """
+    q, k, v, u, vb, W = (_f64(x) for x in (q, k, v, u, vb, W_R))
+    B, T, H, D = q.shape
+    assert T % L == 0
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    out = np.full((B, T, H, D), np.nan, dtype=np.float64)
+    sel, n_sel = _sel(rows)
+    rc = library().txlo_stream_attn(
+        B, H, D, L, M, T // L, clamp_len, W.shape[0], _p(q), _p(k), _p(v), _p(u), _p(vb), _p(W),
+        W.shape[1], float(scale), _p(out), int(bool(memo)), _threads(threads),
+        sel.ctypes.data_as(_ip) if sel is not None else None, n_sel)
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return out
+
+
+def ring_push(ring_k: np.ndarray, ring_v: np.ndarray, wp: int, valid: int, k_new: np.ndarray,
+              v_new: np.ndarray):
+    """FIFO memory of M positions ("Transformer-XL架构解析" §1.1: the newest segment's states
+    evict the oldest).  ring_* [B, M, ...] hold position slots; the oldest valid position is at
+    slot ``wp`` once the ring is full.  Returns (ring_k, ring_v, wp, valid) after appending the
+    L positions of k_new/v_new [B, L, ...], one position at a time, oldest first."""
+    ring_k = ring_k.copy()
+    ring_v = ring_v.copy()
+    M = ring_k.shape[1]
+    L = k_new.shape[1]
+    for t in range(L):
+        if M == 0:
+            break
+        ring_k[:, wp] = k_new[:, t]
+        ring_v[:, wp] = v_new[:, t]
+        wp = (wp + 1) % M
+        valid = min(valid + 1, M)
+    return ring_k, ring_v, wp, valid
+
+
+def ring_logical(ring: np.ndarray, wp: int, valid: int) -> np.ndarray:
+    """Logical memory [B, M, ...]: index M-1 is the newest position, M-valid the oldest valid
+    one; positions below M-valid are not valid (returned as zeros)."""
+    M = ring.shape[1]
+    out = np.zeros_like(ring)
+    for j in range(M - valid, M):
+        out[:, j] = ring[:, (wp + j) % M]
+    return out
+
+
+def attn_flops(B: int, H: int, D: int, L: int, M: int, mem_valid: int | None = None) -> int:
+    """Algorithmic flops of one call: 6*D per visible (query, key) pair (AC 2D, BD 2D, PV 2D)."""
+    if mem_valid is None:
+        mem_valid = M
+    pairs = L * mem_valid + L * (L + 1) // 2
+    return 6 * D * pairs * B * H
