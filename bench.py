@@ -1,0 +1,386 @@
+"""Benchmark of the Transformer-XL relative-attention hot path on GB300.
+
+One step = one pass of the whole path over one batch of the workload:
+    txl_rel_pos_gen  (sinusoid R on chip, r = R W_R, tcgen05)
+    txl_rel_attn_fwd (fused TMA + tcgen05 attention over [memory ++ current])
+    txl_mem_push     (FIFO update of the K/V memory with the current segment)
+on the large workload (B16 H16 D64 L384 M384, clamp 1000, bf16).  Inputs are resident in HBM;
+four input sets (252 MB > 129 MB L2) rotate so no step reads L2-warm inputs.  Steps are replayed
+from a CUDA graph of four consecutive steps (no host launch overhead in the timed region).
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the fp64 oracle on the host cores on
+bounded samples of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "large"        # B16 H16 D64 L384 M384 clamp 1000 bf16
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return d["bf16_tflops"], d.get("bf16_tflops_sustained"), d["hbm_gbs"], "measured"
+    except Exception:
+        return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+def _flops(cfg):
+    import oracle
+    attn = oracle.attn_flops(cfg.B, cfg.H, cfg.D, cfg.L, cfg.M)
+    pos = 2 * cfg.n_rows * cfg.d_model * cfg.H * cfg.D
+    return attn, pos
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        sel = [p for (t, p) in self.rows if t0 <= t <= t1]
+        if not sel:
+            sel = [p for (_, p) in self.rows]
+        if not sel:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        mhz = sorted(float(p[1]) for p in sel if p[1].replace(".", "").isdigit())
+        mx = max((float(p[2]) for p in sel if p[2].replace(".", "").isdigit()), default=None)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for p in sel for k in range(4) if p[5 + k].lower() == "active"})
+        return {"sm_mhz": mhz[len(mhz) // 2] if mhz else None, "sm_max_mhz": mx,
+                "reasons": reasons, "samples": len(sel)}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def _max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _profile_traffic(kernel_src: str):
+    """DRAM bytes per launch of the fused kernel from the committed ncu summary, if it was taken
+    on the current kernel source (sha256 recorded next to it); else None."""
+    path = os.path.join(ROOT, "profiles", "rel_attn_fwd_large.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        with open(kernel_src, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()
+        if d.get("kernel_sha256") == sha:
+            return d.get("dram_bytes_per_launch")
+    except Exception:
+        pass
+    return None
+
+
+def cpu_baseline(cfg, target_s: float = 12.0, threads=None):
+    """The oracle as it stands on the host cores, on a bounded sample of the workload: whole
+    batch entries (every head and query) until about target_s seconds of work."""
+    import oracle
+    import txl_inputs
+    threads = threads or (os.cpu_count() or 1)
+    case = txl_inputs.make_case(cfg)
+    from oracle.oracle import _f64
+    q, k, v, u, vb = (_f64(case[n]) for n in ("q", "k", "v", "u", "vb"))
+    W = _f64(case["W_R"][:, : cfg.H * cfg.D])
+    done_flops, t_total, nb = 0, 0.0, 0
+    while nb < cfg.B and t_total < target_s:
+        rows = [(nb, h, i) for h in range(cfg.H) for i in range(cfg.L)]
+        t0 = time.perf_counter()
+        oracle.rel_attn(q, k, v, u, vb, W, cfg.M, cfg.M, cfg.clamp_len, threads=threads, rows=rows)
+        t_total += time.perf_counter() - t0
+        done_flops += oracle.attn_flops(1, cfg.H, cfg.D, cfg.L, cfg.M)
+        nb += 1
+    return {"value": done_flops / t_total / 1e12, "unit": "TFLOP/s", "cores": threads,
+            "kind": "oracle",
+            "sample": "%d of %d batch entries (all %d heads x %d queries), fp64, %.1f s" % (
+                nb, cfg.B, cfg.H, cfg.L, t_total)}
+
+
+def run_reference(args):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    import txl_inputs
+    cfg = txl_inputs.CONFIGS[WORKLOAD]
+    for _ in range(args.warmup):
+        cpu_baseline(cfg, target_s=0.5)
+    vals, t0 = [], time.perf_counter()
+    for _ in range(args.steps):
+        vals.append(cpu_baseline(cfg, target_s=max(1.0, 60.0 / max(args.steps, 1))))
+    dt = time.perf_counter() - t0
+    value = sum(v["value"] for v in vals) / len(vals)
+    attn, _ = _flops(cfg)
+    line = {
+        "impl": "reference", "metric": "rel-attn TFLOP/s (L384 M384 H16 D64)", "value": value,
+        "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * dt / max(args.steps, 1), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "large: B16 H16 D64 d_model1024 L384 M384 clamp1000",
+                   "sample": vals[-1]["sample"]},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": vals[-1]["cores"],
+                         "kind": "oracle", "sample": vals[-1]["sample"]},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_txl(args):
+    import torch
+
+    world, rank, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", torch.cuda.current_device())
+    import transformer_xl_relative_gb300 as txl
+    import txl_inputs
+
+    cfg = txl_inputs.CONFIGS[WORKLOAD]
+    B, H, D, L, M, C = cfg.B, cfg.H, cfg.D, cfg.L, cfg.M, cfg.clamp_len
+    dt = cfg.torch_dtype
+    n_rows = cfg.n_rows
+    NSETS = 4
+    g = torch.Generator(device=device).manual_seed(cfg.seed + 7919 * rank)
+    sets = []
+    for _ in range(NSETS):
+        q = torch.randn(B, L, H, D, generator=g, device=device).to(dt)
+        k = torch.randn(B, M + L, H, D, generator=g, device=device).to(dt)
+        v = torch.randn(B, M + L, H, D, generator=g, device=device).to(dt)
+        sets.append((q, k, v))
+    u = (0.02 * torch.randn(H, D, generator=g, device=device)).float()
+    vb = (0.02 * torch.randn(H, D, generator=g, device=device)).float()
+    W = (torch.randn(cfg.d_model, H * D, generator=g, device=device) * cfg.d_model ** -0.5).to(dt)
+    r = torch.empty(n_rows, H, D, dtype=dt, device=device)
+    outs = [torch.empty(B, L, H, D, dtype=dt, device=device) for _ in range(NSETS)]
+    ring = txl.Memory.empty(B, M, H, D, dtype=dt, device=device)
+    mems = [txl.Memory.full(k[:, :M], v[:, :M]) for (_, k, v) in sets]
+
+    def step(s):
+        q, k, v = sets[s]
+        txl.rel_pos_gen(W, r, n_rows, cfg.d_model, H, D)
+        txl.rel_attn_fwd(q, mems[s], k[:, M:], v[:, M:], u, vb, r, n_rows, C, outs[s])
+        txl.mem_push(ring, k[:, M:], v[:, M:])
+
+    assert txl.rel_attn_path(sets[0][0], mems[0], sets[0][1][:, M:], sets[0][2][:, M:], r, outs[0]) == 1
+    stream = torch.cuda.Stream(device=device)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for s in range(NSETS):           # warm-up outside capture (first-call attribute setup)
+            step(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for s in range(NSETS):
+            step(s)
+    attn_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(attn_graph, stream=stream):
+        for s in range(NSETS):
+            q, k, v = sets[s]
+            txl.rel_attn_fwd(q, mems[s], k[:, M:], v[:, M:], u, vb, r, n_rows, C, outs[s])
+
+    reps = max(1, math.ceil(args.steps / NSETS))
+    steps = reps * NSETS
+    warm_reps = max(1, math.ceil(args.warmup / NSETS))
+    sampler = ClockSampler(device.index if device.index is not None else 0)
+    sampler.start()
+    time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        for _ in range(warm_reps):
+            graph.replay()
+    torch.cuda.synchronize()
+    _barrier(world)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    _barrier(world)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    t_step_ms = ev0.elapsed_time(ev1) / steps
+    t_step_ms = _max_over_ranks(t_step_ms, world, device)
+
+    # the fused attention kernel alone, same rotation, same stream
+    with torch.cuda.stream(stream):
+        attn_graph.replay()
+    torch.cuda.synchronize()
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        a0.record(stream)
+        for _ in range(reps):
+            attn_graph.replay()
+        a1.record(stream)
+    torch.cuda.synchronize()
+    t_attn_ms = a0.elapsed_time(a1) / steps
+    sampler.stop()
+    clocks = sampler.summary(wall0, wall1)
+
+    # end to end through the public API: pinned host inputs in, output back, every step
+    hq = [s[0].cpu().pin_memory() for s in sets[:2]]
+    hk = [s[1].cpu().pin_memory() for s in sets[:2]]
+    hv = [s[2].cpu().pin_memory() for s in sets[:2]]
+    ho = torch.empty(B, L, H, D, dtype=dt).pin_memory()
+    e2e_steps = max(4, min(steps, 40))
+    dq, dk, dv = sets[0]
+    dmem = mems[0]
+    with torch.cuda.stream(stream):
+        for i in range(2):                 # warm-up
+            dq.copy_(hq[i % 2], non_blocking=True); dk.copy_(hk[i % 2], non_blocking=True)
+            dv.copy_(hv[i % 2], non_blocking=True)
+            txl.rel_pos_gen(W, r, n_rows, cfg.d_model, H, D)
+            txl.rel_attn_fwd(dq, dmem, dk[:, M:], dv[:, M:], u, vb, r, n_rows, C, outs[0])
+            txl.mem_push(ring, dk[:, M:], dv[:, M:])
+            ho.copy_(outs[0], non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(e2e_steps):
+            dq.copy_(hq[i % 2], non_blocking=True); dk.copy_(hk[i % 2], non_blocking=True)
+            dv.copy_(hv[i % 2], non_blocking=True)
+            txl.rel_pos_gen(W, r, n_rows, cfg.d_model, H, D)
+            txl.rel_attn_fwd(dq, dmem, dk[:, M:], dv[:, M:], u, vb, r, n_rows, C, outs[0])
+            txl.mem_push(ring, dk[:, M:], dv[:, M:])
+            ho.copy_(outs[0], non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    t_e2e_ms = _max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, device)
+    h2d = sum(t.numel() * t.element_size() for t in (dq, dk, dv))
+    d2h = ho.numel() * ho.element_size()
+
+    attn_flops, pos_flops = _flops(cfg)
+    step_flops = attn_flops + pos_flops
+    peak, peak_sust, _, peak_kind = _peaks()
+    value = world * step_flops / (t_step_ms * 1e-3) / 1e12
+    achieved = attn_flops / (t_attn_ms * 1e-3) / 1e12
+    kernel_src = os.path.join(ROOT, "transformer_xl_relative_gb300", "csrc", "txl_attn_tc.cu")
+    line = {
+        "metric": "rel-attn TFLOP/s (L384 M384 H16 D64 bf16), whole step: pos-gen + fused attention + memory push",
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": steps,
+        "warmup": warm_reps * NSETS,
+        "ms_per_step": t_step_ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) q/k/v, N(0,0.02^2) u/v_bias, N(0,1/d_model) W_R)",
+        "config": {"workload": "large: B16 H16 D64 d_model1024 L384 M384 clamp1000 (per GPU)",
+                   "global_batch": B * world, "seq_len": L, "mem_len": M,
+                   "l2": "4 rotating input sets, 252 MB > 129 MB L2",
+                   "parallelism": "dp%d: independent replicas, no collective on the data path" % world},
+        "tokens_per_s": world * B * L / (t_step_ms * 1e-3),
+        "attn_tflops": achieved,
+        "frac_of_bf16_peak_step": value / world / peak,
+        "clocks": clocks,
+        "e2e": {"value": world * step_flops / (t_e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": t_e2e_ms},
+        "gpu_launches": 3 * steps,
+        "roofline": {"kernel": "txl_rel_attn_fwd (attn_tc_kernel<1>)", "bound": "tensor",
+                     "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "peak_source": "%s bf16 burst (MEASURED_PEAKS.json)" % peak_kind
+                     if peak_kind == "measured" else "fallback 1.9 PFLOP/s",
+                     "traffic": _profile_traffic(kernel_src),
+                     "algorithmic_flops_per_launch": attn_flops},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=40)
+    ap.add_argument("--impl", choices=["txl", "reference"], default="txl")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_txl(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,165 @@
+/*
+ * txl.h -- C ABI of libtxl.so: Transformer-XL relative multi-head attention over
+ * [memory ++ current segment] on one NVIDIA GB300 (sm_103a).
+ *
+ * The operation (citations are page title and section):
+ *   "跨窗口的相对位置编码" §3 and "Transformer-XL 和相对位置编码" §2.3.2 (terms (a)-(d)):
+ *       A_ij = q_i.k_j + q_i.r_{i-j} + u.k_j + v.r_{i-j}
+ *   "跨窗口的相对位置编码" §2, "Transformer-XL 和相对位置编码" §2.3.2:
+ *       R_delta[2k] = sin(delta * 10000^(-2k/d_model)), R_delta[2k+1] = cos(same)
+ *       r_delta = R_delta W_R                  (W_{k,R}; "TransformerXL 相对位置编码" §3.1 r_proj)
+ *   "TransformerXL 相对位置编码" §2.4: distances beyond clamp_len count as clamp_len.
+ *   "TransformerXL 相对位置编码" §4.2/§4.3: mask the summed score; keys span memory + current.
+ *   "Transformer-XL 和相对位置编码" §2.3.1: K, V from [SG(memory) ∘ current], Q from current.
+ *   "Transformer-XL架构解析" §1.1: the memory is a FIFO of mem_len positions.
+ *
+ * Conventions for every entry point:
+ *  - Pointers named "device" are CUDA device addresses; the caller owns all memory.  The library
+ *    never allocates, frees or synchronises.  Work is enqueued on `stream` (a cudaStream_t; NULL
+ *    is the legacy default stream) on the calling thread's current device, and calls return as
+ *    soon as it is enqueued.
+ *  - Arguments are validated on the host before anything is launched; a non-TXL_OK status means
+ *    nothing was enqueued (except TXL_ERR_CUDA, which reports a failed launch).
+ *  - Element strides are in elements, not bytes.  The innermost index (d) is always contiguous.
+ *  - No exceptions, no printing, no CPU fallback.
+ */
+#ifndef TXL_H
+#define TXL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TXL_OK = 0,
+    TXL_ERR_INVALID_ARG = 1,   /* null pointer, non-positive size, inconsistent shapes       */
+    TXL_ERR_UNSUPPORTED = 2,   /* valid request this build does not implement                 */
+    TXL_ERR_ALIGNMENT = 3,     /* a base address or stride is not 16-byte aligned where needed */
+    TXL_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed                            */
+    TXL_ERR_TIMEOUT = 5,       /* written to err_flag by a kernel whose bounded wait expired   */
+    TXL_ERR_WORKSPACE = 6      /* workspace missing or smaller than txl_rel_attn_workspace_size */
+} txl_status;
+
+typedef enum { TXL_F32 = 0, TXL_BF16 = 1 } txl_dtype;
+
+/* A [B][T][H][D] tensor in device memory: element (b,t,h,d) lives at
+ * ptr + b*stride_b + t*stride_t + h*stride_h + d   (elements of the call's dtype). */
+typedef struct {
+    void* ptr;
+    int64_t stride_b;
+    int64_t stride_t;
+    int64_t stride_h;
+} txl_view;
+
+/* K/V memory of M positions per batch entry ("Transformer-XL架构解析" §1.1: FIFO cache).
+ * k and v are device [B][M][H][D] slot arrays with the strides below (shared by k and v).
+ * Logical memory key j (0 <= j < M, j = M-1 newest) lives in physical slot (wp + j) mod M and
+ * is valid iff j >= M - valid.  A freshly zeroed ring has wp = 0, valid = 0.  A plain
+ * contiguous memory (oldest first) is described by wp = 0, valid = M.  M = 0 means no memory
+ * (k, v may then be NULL). */
+typedef struct {
+    void* k;
+    void* v;
+    int64_t stride_b;
+    int64_t stride_t;
+    int64_t stride_h;
+    int B, M, H, D;
+    txl_dtype dtype;
+    int wp;      /* next slot to write == slot of the oldest position once the ring is full */
+    int valid;   /* number of valid positions, 0..M */
+} txl_mem;
+
+/* Human-readable name of a status code (static string). */
+const char* txl_status_str(txl_status status);
+
+/* Library ABI version (major*10000 + minor*100 + patch). */
+int txl_version(void);
+
+/*
+ * txl_rel_pos_gen -- position key vectors of every distance the attention can see.
+ *   r[delta][h][d] = sum_m R_delta[m] * W_R[m][h*d_head + d],  delta = 0 .. n_rows-1,
+ * with R_delta the interleaved sinusoid above (fp32 angles, on chip; never stored).
+ * Row index == distance.  For one attention call, n_rows = min(M+L, clamp_len+1).
+ *   W_R : device [d_model][ld_w], dtype; columns 0 .. n_head*d_head-1 are used; no bias.
+ *   r   : device [n_rows][n_head][ld_r], dtype; only d < d_head is written.
+ * Limits: d_model even, 2 <= d_model <= 4096; ld_w >= n_head*d_head; ld_r >= d_head.
+ * bf16: tensor-core path (fp32 accumulate, R rounded to bf16 before the product, output rounded
+ *       to bf16 once); needs W_R 16-byte aligned and ld_w a multiple of 8.
+ * f32 : fp32 SIMT path with R rounded once from double precision.
+ */
+txl_status txl_rel_pos_gen(int n_rows, int d_model, int n_head, int d_head,
+                           const void* W_R, int64_t ld_w,
+                           void* r, int64_t ld_r,
+                           txl_dtype dtype, void* stream);
+
+/*
+ * txl_rel_attn_fwd -- one forward call of relative multi-head attention.
+ * For every batch b, head h and query i (0 <= i < L, absolute position M+i) over keys
+ * j in [memory(0..M-1) ++ current(M..M+L-1)]:
+ *   delta = M + i - j,  delta_c = min(delta, clamp_len)
+ *   visible(i, j) <=> (M - valid) <= j <= M + i
+ *   s_ij  = scale * ( q_i.k_j + q_i.r[delta_c] + u_h.k_j + v_h.r[delta_c] )
+ *   out_i = sum_j softmax_j(s_ij over visible j) * v_j          (masked keys weigh exactly 0)
+ * Arguments:
+ *   q      : view of [B][L][H][D] queries of the current segment (device).
+ *   mem    : the memory (see txl_mem); may be NULL when there is no memory (M = 0).
+ *   k_cur, v_cur : views of [B][L][H][D] keys/values of the current segment (device).
+ *   u, v_bias : device fp32 [H][D] global content / position biases.
+ *   r      : device [n_rows][H][ld_r] from txl_rel_pos_gen; n_rows >= min(M+L, clamp_len+1).
+ *   scale  : logit scale; <= 0 selects 1/sqrt(D).
+ *   out    : view of [B][L][H][D] outputs (device), dtype.
+ *   workspace : device scratch of workspace_bytes (txl_rel_attn_workspace_size); may be NULL
+ *            when that size is 0.
+ *   err_flag : optional device int; a kernel whose bounded wait expires writes TXL_ERR_TIMEOUT
+ *            there (and its outputs are then undefined).  Never cleared by the library.
+ * Paths:
+ *   bf16, D <= 128, every base and stride 16-byte aligned, and a ring whose wp and M are
+ *   multiples of 128 (or wp == 0): the fused TMA + tcgen05 kernel (TMEM accumulators; the
+ *   relative shift is an index remap; the score matrix never reaches HBM).
+ *   otherwise (f32, other layouts, other rings): a warp-per-query SIMT kernel on the GPU.
+ */
+txl_status txl_rel_attn_fwd(int B, int L, int H, int D, int clamp_len,
+                            const txl_view* q, const txl_mem* mem,
+                            const txl_view* k_cur, const txl_view* v_cur,
+                            const float* u, const float* v_bias,
+                            const void* r, int64_t ld_r, int n_rows,
+                            float scale, const txl_view* out, txl_dtype dtype,
+                            void* workspace, size_t workspace_bytes,
+                            int* err_flag, void* stream);
+
+/* Bytes of device workspace txl_rel_attn_fwd needs for this shape (0 for every path of this
+ * version; kept so callers can size it once). */
+size_t txl_rel_attn_workspace_size(int B, int L, int H, int D, const txl_mem* mem,
+                                   txl_dtype dtype);
+
+/* Which kernel txl_rel_attn_fwd would run for these arguments: 1 = fused tcgen05 kernel,
+ * 2 = SIMT kernel, or a negative txl_status if the arguments are rejected. */
+int txl_rel_attn_path(int B, int L, int H, int D, const txl_view* q, const txl_mem* mem,
+                      const txl_view* k_cur, const txl_view* v_cur, const void* r,
+                      int64_t ld_r, const txl_view* out, txl_dtype dtype);
+
+/*
+ * txl_mem_push -- append L positions to the FIFO memory ("Transformer-XL架构解析" §1.1;
+ * "Transformer-XL 和相对位置编码" §2.3.1: the cached states of the previous segment).
+ * Copies k_new/v_new [B][L][H][D] (device views) into slots (wp + t) mod M for
+ * t = max(0, L-M) .. L-1 (a segment longer than the memory keeps its last M positions), then
+ * updates mem->wp = (wp + L) mod M and mem->valid = min(valid + L, M) on the host at enqueue
+ * time.  The copy is ordered on `stream`; the attention for this segment must be enqueued
+ * before the push if it should see the previous memory.  Bit-exact copy.
+ */
+txl_status txl_mem_push(txl_mem* mem, const txl_view* k_new, const txl_view* v_new, int L,
+                        void* stream);
+
+/* Self-test of the bounded waits used by every kernel: launches one CTA that waits on an
+ * mbarrier nothing will signal, gives up after timeout_us microseconds (1 .. 10^7), writes
+ * TXL_ERR_TIMEOUT to the device int err_flag and returns.  The context stays usable. */
+txl_status txl_selftest_wait_timeout(int* err_flag, unsigned timeout_us, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TXL_H */

@@ -1,0 +1,135 @@
+"""CPU tests of the C ABI: the library builds, loads, exports every function include/txl.h
+declares, and its host-side validation and kernel selection behave as documented.  Nothing here
+launches a kernel (every call is rejected, or decides a path, before any CUDA work)."""
+import ctypes
+import importlib.util
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def native():
+    spec = importlib.util.spec_from_file_location(
+        "txl_build", os.path.join(ROOT, "transformer_xl_relative_gb300", "_build.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    mod.build()
+    from transformer_xl_relative_gb300 import native as n
+    n.load()
+    return n
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "txl.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(txl_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_lists_the_boundary():
+    names = declared_functions()
+    for fn in ("txl_rel_pos_gen", "txl_rel_attn_fwd", "txl_mem_push"):
+        assert fn in names
+
+
+def test_every_declared_function_is_exported(native):
+    lib = native.load()
+    for fn in declared_functions():
+        assert hasattr(lib, fn), fn
+    assert set(declared_functions()) == set(native.EXPORTS)
+
+
+def test_status_strings_and_version(native):
+    lib = native.load()
+    assert lib.txl_status_str(0) == b"ok"
+    assert lib.txl_status_str(5) == b"device wait timed out"
+    assert lib.txl_version() >= 10000
+
+
+def _view(ptr, sb, st, sh):
+    return native_mod().TxlView(ptr, sb, st, sh)
+
+
+def native_mod():
+    from transformer_xl_relative_gb300 import native as n
+    return n
+
+
+FAKE = 1 << 40          # an aligned address that is never dereferenced (host-side checks only)
+
+
+def _path(native, B=2, L=200, H=4, D=64, M=128, wp=0, valid=128, dtype=1, sh=None, misalign=0,
+          ld_r=64):
+    sh = sh or D
+    V = native.TxlView
+    q = V(FAKE + misalign, L * H * sh, H * sh, sh)
+    kc = V(FAKE, (M + L) * H * sh, H * sh, sh)
+    out = V(FAKE, L * H * sh, H * sh, sh)
+    mem = native.TxlMem(FAKE, FAKE, (M + L) * H * sh, H * sh, sh, B, M, H, D, dtype, wp, valid)
+    return native.load().txl_rel_attn_path(B, L, H, D, ctypes.byref(q), ctypes.byref(mem),
+                                           ctypes.byref(kc), ctypes.byref(kc), FAKE, ld_r,
+                                           ctypes.byref(out), dtype)
+
+
+def test_path_selection(native):
+    assert _path(native) == 1                                 # bf16, aligned: fused tcgen05
+    assert _path(native, dtype=0) == 2                        # fp32: SIMT
+    assert _path(native, D=41, sh=41, ld_r=48) == 2           # 82-byte rows: no TMA
+    assert _path(native, D=41, sh=48, ld_r=48) == 1           # padded head stride: TMA
+    assert _path(native, misalign=2) == 2                     # misaligned base
+    assert _path(native, M=256, wp=128, valid=256) == 1       # ring aligned to 128
+    assert _path(native, M=256, wp=64, valid=256) == 2        # ring not aligned
+    assert _path(native, M=300, wp=128, valid=300) == 2       # ring length not a multiple
+    assert _path(native, D=128, ld_r=128) == 1
+    assert _path(native, D=130, ld_r=136) == -native.TXL_ERR_UNSUPPORTED
+    assert _path(native, wp=128, valid=128) == -native.TXL_ERR_INVALID_ARG   # wp >= M
+
+
+def test_rejections_before_any_launch(native):
+    lib = native.load()
+    V = native.TxlView
+    q = V(FAKE, 1, 1, 1)
+    nullv = V(None, 1, 1, 1)
+    # null query view
+    assert lib.txl_rel_attn_fwd(1, 8, 1, 8, 16, ctypes.byref(nullv), None, ctypes.byref(q),
+                                ctypes.byref(q), FAKE, FAKE, FAKE, 8, 16, 0.0, ctypes.byref(q), 1,
+                                None, 0, None, None) == native.TXL_ERR_INVALID_ARG
+    # too few rows in r: min(M+L, clamp+1) = 8 > 4
+    assert lib.txl_rel_attn_fwd(1, 8, 1, 8, 16, ctypes.byref(q), None, ctypes.byref(q),
+                                ctypes.byref(q), FAKE, FAKE, FAKE, 8, 4, 0.0, ctypes.byref(q), 1,
+                                None, 0, None, None) == native.TXL_ERR_INVALID_ARG
+    # negative clamp
+    assert lib.txl_rel_attn_fwd(1, 8, 1, 8, -1, ctypes.byref(q), None, ctypes.byref(q),
+                                ctypes.byref(q), FAKE, FAKE, FAKE, 8, 16, 0.0, ctypes.byref(q), 1,
+                                None, 0, None, None) == native.TXL_ERR_INVALID_ARG
+    # d_head above 128
+    assert lib.txl_rel_attn_fwd(1, 8, 1, 256, 16, ctypes.byref(q), None, ctypes.byref(q),
+                                ctypes.byref(q), FAKE, FAKE, FAKE, 256, 16, 0.0, ctypes.byref(q), 1,
+                                None, 0, None, None) == native.TXL_ERR_UNSUPPORTED
+    # position table: odd d_model, misaligned bf16 W_R, d_model above the limit
+    assert lib.txl_rel_pos_gen(8, 15, 2, 8, FAKE, 16, FAKE, 8, 1, None) == native.TXL_ERR_INVALID_ARG
+    assert lib.txl_rel_pos_gen(8, 16, 2, 8, FAKE + 2, 16, FAKE, 8, 1, None) == native.TXL_ERR_ALIGNMENT
+    assert lib.txl_rel_pos_gen(8, 16, 2, 8, FAKE, 20, FAKE, 8, 1, None) == native.TXL_ERR_ALIGNMENT
+    assert lib.txl_rel_pos_gen(8, 8192, 2, 8, FAKE, 16, FAKE, 8, 1, None) == native.TXL_ERR_INVALID_ARG
+    # memory push: write pointer outside the ring, and an empty segment (no work, no change)
+    mem = native.TxlMem(FAKE, FAKE, 64, 8, 8, 1, 8, 1, 8, 1, 9, 0)
+    assert lib.txl_mem_push(ctypes.byref(mem), ctypes.byref(q), ctypes.byref(q), 4, None) == \
+        native.TXL_ERR_INVALID_ARG
+    mem = native.TxlMem(FAKE, FAKE, 64, 8, 8, 1, 8, 1, 8, 1, 3, 5)
+    assert lib.txl_mem_push(ctypes.byref(mem), ctypes.byref(q), ctypes.byref(q), 0, None) == native.TXL_OK
+    assert (mem.wp, mem.valid) == (3, 5)
+    # self-test limits
+    assert lib.txl_selftest_wait_timeout(FAKE, 0, None) == native.TXL_ERR_INVALID_ARG
+    assert lib.txl_selftest_wait_timeout(None, 10, None) == native.TXL_ERR_INVALID_ARG
+
+
+def test_empty_batch_is_a_no_op(native):
+    lib = native.load()
+    q = native.TxlView(FAKE, 1, 1, 1)
+    assert lib.txl_rel_attn_fwd(0, 8, 1, 8, 16, ctypes.byref(q), None, ctypes.byref(q),
+                                ctypes.byref(q), FAKE, FAKE, FAKE, 8, 16, 0.0, ctypes.byref(q), 1,
+                                None, 0, None, None) == native.TXL_OK
+    assert lib.txl_rel_pos_gen(0, 16, 2, 8, FAKE, 16, FAKE, 8, 1, None) == native.TXL_OK

@@ -1,0 +1,19 @@
+"""Transformer-XL relative multi-head attention over [memory ++ current segment] for GB300.
+
+The computation lives in libtxl.so (CUDA, sm_103a; C ABI in include/txl.h).  This package is its
+Python binding: torch supplies device memory and streams, the library supplies every kernel.
+Importing the package loads the library and fails loudly if it has not been built.
+"""
+from . import native
+from .api import (  # noqa: F401
+    Memory,
+    mem_push,
+    rel_attn_fwd,
+    rel_attn_path,
+    rel_pos_gen,
+    selftest_wait_timeout,
+    version,
+)
+from .native import TxlError  # noqa: F401
+
+native.load()

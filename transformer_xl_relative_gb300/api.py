@@ -1,0 +1,160 @@
+"""Python binding of libtxl.so over torch CUDA tensors.
+
+Argument marshalling only: every function converts tensors to pointers and element strides and
+calls the C ABI of the same name; all computation happens in the library's CUDA kernels.  Torch
+provides device memory and streams.  Tensors are [B, T, H, D] views whose last dimension is
+contiguous; r is [n_rows, H, ld_r].
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import native
+from .native import TxlMem, TxlView, check
+
+_DTYPES = {torch.float32: native.TXL_F32, torch.bfloat16: native.TXL_BF16}
+
+
+def _lib():
+    return native.load()
+
+
+def dtype_code(t: torch.Tensor) -> int:
+    try:
+        return _DTYPES[t.dtype]
+    except KeyError:
+        raise TypeError("libtxl computes in float32 or bfloat16, got %s" % t.dtype) from None
+
+
+def view(t: torch.Tensor) -> TxlView:
+    """[B, T, H, D] tensor with contiguous D -> txl_view."""
+    if t.dim() != 4:
+        raise ValueError("expected a [B, T, H, D] tensor, got shape %s" % (tuple(t.shape),))
+    if t.shape[-1] > 1 and t.stride(-1) != 1:
+        raise ValueError("the last (d) dimension must be contiguous")
+    if not t.is_cuda:
+        raise ValueError("tensors must live on a CUDA device")
+    return TxlView(t.data_ptr(), t.stride(0), t.stride(1), t.stride(2))
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+class Memory:
+    """K/V memory of M positions per batch entry (FIFO ring, or a plain contiguous memory).
+
+    ``k`` and ``v`` are [B, M, H, D] tensors (same strides).  ``wp``/``valid`` follow txl_mem:
+    logical memory key j lives in slot (wp + j) mod M and is valid iff j >= M - valid.
+    """
+
+    def __init__(self, k: torch.Tensor, v: torch.Tensor, wp: int = 0, valid: int = 0):
+        if k.shape != v.shape or k.stride() != v.stride() or k.dtype != v.dtype:
+            raise ValueError("k and v must share shape, strides and dtype")
+        self.k, self.v = k, v
+        B, M, H, D = k.shape
+        self._c = TxlMem(k.data_ptr() if M else None, v.data_ptr() if M else None,
+                         k.stride(0), k.stride(1), k.stride(2), B, M, H, D, dtype_code(k), wp, valid)
+
+    @classmethod
+    def empty(cls, B, M, H, D, dtype=torch.bfloat16, device="cuda", head_stride=None):
+        hs = head_stride or D
+        store = torch.zeros(B, M, H, hs, dtype=dtype, device=device)
+        store2 = torch.zeros(B, M, H, hs, dtype=dtype, device=device)
+        return cls(store[..., :D], store2[..., :D], 0, 0)
+
+    @classmethod
+    def full(cls, k: torch.Tensor, v: torch.Tensor):
+        """A contiguous memory, oldest position first, every slot valid."""
+        return cls(k, v, 0, k.shape[1])
+
+    @property
+    def M(self) -> int:
+        return self._c.M
+
+    @property
+    def wp(self) -> int:
+        return self._c.wp
+
+    @property
+    def valid(self) -> int:
+        return self._c.valid
+
+    def state(self):
+        """Host ring state (wp, valid): with the buffers, everything needed to resume."""
+        return self._c.wp, self._c.valid
+
+    def restore(self, wp: int, valid: int) -> None:
+        self._c.wp, self._c.valid = int(wp), int(valid)
+
+    @property
+    def c_struct(self) -> TxlMem:
+        return self._c
+
+
+def rel_pos_gen(W_R: torch.Tensor, r: torch.Tensor, n_rows: int, d_model: int, n_head: int,
+                d_head: int, stream=None) -> torch.Tensor:
+    """r[delta, h, d] = sum_m R_delta[m] W_R[m, h*d_head + d] for delta < n_rows (txl_rel_pos_gen)."""
+    if W_R.dim() != 2 or W_R.stride(1) != 1 or r.dim() != 3 or r.stride(2) != 1:
+        raise ValueError("W_R must be [d_model, ld_w] and r [n_rows, H, ld_r] with unit last stride")
+    if r.stride(1) * n_head != r.stride(0) and r.shape[0] > 1:
+        raise ValueError("r rows must be n_head * ld_r elements apart")
+    st = _lib().txl_rel_pos_gen(n_rows, d_model, n_head, d_head, W_R.data_ptr(), W_R.stride(0),
+                                r.data_ptr(), r.stride(1), dtype_code(W_R), _stream(stream))
+    check(st, "txl_rel_pos_gen")
+    return r
+
+
+def _attn_args(q, mem, k_cur, v_cur, r, out):
+    B, L, H, D = q.shape
+    memc = ctypes.byref(mem.c_struct) if mem is not None else None
+    return (B, L, H, D), memc, view(q), view(k_cur), view(v_cur), view(out)
+
+
+def rel_attn_fwd(q: torch.Tensor, mem: Memory | None, k_cur: torch.Tensor, v_cur: torch.Tensor,
+                 u: torch.Tensor, v_bias: torch.Tensor, r: torch.Tensor, n_rows: int,
+                 clamp_len: int, out: torch.Tensor, scale: float = 0.0,
+                 err_flag: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """One relative-attention call over [memory ++ current] (txl_rel_attn_fwd)."""
+    (B, L, H, D), memc, vq, vk, vv, vo = _attn_args(q, mem, k_cur, v_cur, r, out)
+    if u.dtype != torch.float32 or v_bias.dtype != torch.float32:
+        raise TypeError("u and v_bias are fp32 [H, D]")
+    if not (u.is_contiguous() and v_bias.is_contiguous()):
+        raise ValueError("u and v_bias must be contiguous [H, D]")
+    st = _lib().txl_rel_attn_fwd(
+        B, L, H, D, int(clamp_len), ctypes.byref(vq), memc, ctypes.byref(vk), ctypes.byref(vv),
+        u.data_ptr(), v_bias.data_ptr(), r.data_ptr(), r.stride(1), int(n_rows), float(scale),
+        ctypes.byref(vo), dtype_code(q), None, 0,
+        err_flag.data_ptr() if err_flag is not None else None, _stream(stream))
+    check(st, "txl_rel_attn_fwd")
+    return out
+
+
+def rel_attn_path(q, mem, k_cur, v_cur, r, out) -> int:
+    """1 = fused tcgen05 kernel, 2 = SIMT kernel (txl_rel_attn_path)."""
+    (B, L, H, D), memc, vq, vk, vv, vo = _attn_args(q, mem, k_cur, v_cur, r, out)
+    return _lib().txl_rel_attn_path(B, L, H, D, ctypes.byref(vq), memc, ctypes.byref(vk),
+                                    ctypes.byref(vv), r.data_ptr(), r.stride(1), ctypes.byref(vo),
+                                    dtype_code(q))
+
+
+def mem_push(mem: Memory, k_new: torch.Tensor, v_new: torch.Tensor, stream=None) -> Memory:
+    """Append k_new/v_new [B, L, H, D] to the FIFO memory (txl_mem_push)."""
+    vk, vv = view(k_new), view(v_new)
+    st = _lib().txl_mem_push(ctypes.byref(mem.c_struct), ctypes.byref(vk), ctypes.byref(vv),
+                             k_new.shape[1], _stream(stream))
+    check(st, "txl_mem_push")
+    return mem
+
+
+def selftest_wait_timeout(err_flag: torch.Tensor, timeout_us: int, stream=None) -> None:
+    st = _lib().txl_selftest_wait_timeout(err_flag.data_ptr(), int(timeout_us), _stream(stream))
+    check(st, "txl_selftest_wait_timeout")
+
+
+def version() -> int:
+    return _lib().txl_version()

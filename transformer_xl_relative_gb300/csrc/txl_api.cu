@@ -1,0 +1,302 @@
+// txl_api.cu -- the C ABI of libtxl.so (declared in include/txl.h): argument validation, TMA
+// descriptor encoding and kernel selection.  Host code only; it never allocates, frees or
+// synchronises, and it never prints.
+#include <cmath>
+#include <cstring>
+#include <algorithm>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "txl_internal.h"
+
+using namespace txl;
+
+namespace {
+
+constexpr int kVersion = 10000;   // 1.0.0
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool encoder_ready()
+{
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode != nullptr;
+}
+
+inline bool a16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool s16(int64_t stride_elems, int elem) { return ((stride_elems * elem) & 15) == 0; }
+
+// [B][T][H][D] view -> TMA dims (d, h, t, b), box (64, 1, 128, 1), 128-byte swizzle, bf16.
+bool encode_view4(CUtensorMap* map, const void* ptr, int D, int H, int T, int B, int64_t sh,
+                  int64_t st, int64_t sb)
+{
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
+                                static_cast<cuuint64_t>(T > 0 ? T : 1), static_cast<cuuint64_t>(B)};
+    // extent-1 dimensions never move the coordinate; give them a harmless aligned stride
+    const int64_t biggest = std::max(std::max(sh, st), sb) * 2;
+    const cuuint64_t strides[3] = {
+        static_cast<cuuint64_t>(H > 1 ? sh * 2 : biggest),
+        static_cast<cuuint64_t>(T > 1 ? st * 2 : biggest),
+        static_cast<cuuint64_t>(B > 1 ? sb * 2 : biggest)};
+    const cuuint32_t box[4] = {64, 1, 128, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_rtab(CUtensorMap* map, const void* r, int D, int H, int n_rows, int64_t ld_r)
+{
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
+                                static_cast<cuuint64_t>(n_rows)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld_r * 2),
+                                   static_cast<cuuint64_t>(static_cast<int64_t>(H) * ld_r * 2)};
+    const cuuint32_t box[3] = {64, 1, 128};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(r), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool view_ok(const txl_view* v) { return v && v->ptr; }
+
+bool view_tma_ok(const txl_view* v, int T, int H, int B)
+{
+    return a16(v->ptr) && (H <= 1 || s16(v->stride_h, 2)) && (T <= 1 || s16(v->stride_t, 2)) &&
+           (B <= 1 || s16(v->stride_b, 2)) && v->stride_h > 0 && v->stride_t > 0 && v->stride_b > 0;
+}
+
+// Shared argument checks of txl_rel_attn_fwd / txl_rel_attn_path.  Returns TXL_OK or an error.
+txl_status check_attn(int B, int L, int H, int D, const txl_view* q, const txl_mem* mem,
+                      const txl_view* k_cur, const txl_view* v_cur, const void* r, int64_t ld_r,
+                      const txl_view* out, txl_dtype dtype)
+{
+    if (B < 0 || L < 0 || H <= 0 || D <= 0 || D > 128) return D > 128 ? TXL_ERR_UNSUPPORTED : TXL_ERR_INVALID_ARG;
+    if (dtype != TXL_F32 && dtype != TXL_BF16) return TXL_ERR_INVALID_ARG;
+    if (!view_ok(q) || !view_ok(k_cur) || !view_ok(v_cur) || !view_ok(out) || !r) return TXL_ERR_INVALID_ARG;
+    if (ld_r < D) return TXL_ERR_INVALID_ARG;
+    if (mem && mem->M > 0) {
+        if (!mem->k || !mem->v || mem->B != B || mem->H != H || mem->D != D || mem->dtype != dtype)
+            return TXL_ERR_INVALID_ARG;
+        if (mem->wp < 0 || mem->wp >= mem->M || mem->valid < 0 || mem->valid > mem->M) return TXL_ERR_INVALID_ARG;
+    } else if (mem && (mem->M < 0 || mem->valid != 0)) {
+        return TXL_ERR_INVALID_ARG;
+    }
+    return TXL_OK;
+}
+
+bool attn_tc_eligible(int B, int L, int H, int D, const txl_view* q, const txl_mem* mem,
+                      const txl_view* k_cur, const txl_view* v_cur, const void* r, int64_t ld_r,
+                      txl_dtype dtype)
+{
+    if (dtype != TXL_BF16 || D > 128) return false;
+    if (!view_tma_ok(q, L, H, B) || !view_tma_ok(k_cur, L, H, B) || !view_tma_ok(v_cur, L, H, B)) return false;
+    if (!a16(r) || !s16(ld_r, 2)) return false;
+    const int M = mem ? mem->M : 0;
+    if (M > 0) {
+        txl_view km{mem->k, mem->stride_b, mem->stride_t, mem->stride_h};
+        txl_view vm{mem->v, mem->stride_b, mem->stride_t, mem->stride_h};
+        if (!view_tma_ok(&km, M, H, B) || !view_tma_ok(&vm, M, H, B)) return false;
+        if (mem->wp != 0 && ((mem->wp % 128) != 0 || (M % 128) != 0)) return false;
+    }
+    return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* txl_status_str(txl_status status)
+{
+    switch (status) {
+    case TXL_OK: return "ok";
+    case TXL_ERR_INVALID_ARG: return "invalid argument";
+    case TXL_ERR_UNSUPPORTED: return "unsupported";
+    case TXL_ERR_ALIGNMENT: return "misaligned address or stride";
+    case TXL_ERR_CUDA: return "CUDA error";
+    case TXL_ERR_TIMEOUT: return "device wait timed out";
+    case TXL_ERR_WORKSPACE: return "workspace missing or too small";
+    }
+    return "unknown status";
+}
+
+int txl_version(void) { return kVersion; }
+
+txl_status txl_rel_pos_gen(int n_rows, int d_model, int n_head, int d_head, const void* W_R, int64_t ld_w,
+                           void* r, int64_t ld_r, txl_dtype dtype, void* stream)
+{
+    if (n_rows < 0 || d_model < 2 || (d_model & 1) || d_model > kMaxDModel || n_head <= 0 || d_head <= 0)
+        return TXL_ERR_INVALID_ARG;
+    if (!W_R || !r || ld_w < static_cast<int64_t>(n_head) * d_head || ld_r < d_head) return TXL_ERR_INVALID_ARG;
+    if (dtype != TXL_F32 && dtype != TXL_BF16) return TXL_ERR_INVALID_ARG;
+    if (n_rows == 0) return TXL_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (dtype == TXL_F32) {
+        PosGenF32Params p{};
+        p.W = static_cast<const float*>(W_R);
+        p.r = static_cast<float*>(r);
+        p.ld_w = ld_w;
+        p.ld_r = ld_r;
+        p.n_rows = n_rows;
+        p.d_model = d_model;
+        p.H = n_head;
+        p.D = d_head;
+        return launch_pos_gen_f32(p, s) == cudaSuccess ? TXL_OK : TXL_ERR_CUDA;
+    }
+    if (!a16(W_R) || !s16(ld_w, 2)) return TXL_ERR_ALIGNMENT;
+    if (!encoder_ready()) return TXL_ERR_CUDA;
+    PosGenTcParams p;                  // carries the frequency table as kernel parameters
+    std::memset(&p, 0, sizeof(p));
+    const int HD = n_head * d_head;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(HD), static_cast<cuuint64_t>(d_model)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld_w * 2)};
+    const cuuint32_t box[2] = {64, 64};
+    const cuuint32_t estr[2] = {1, 1};
+    if (g_encode(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(W_R), dims, strides, box, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return TXL_ERR_CUDA;
+    p.r = r;
+    p.ld_r = ld_r;
+    p.n_rows = n_rows;
+    p.d_model = d_model;
+    p.H = n_head;
+    p.D = d_head;
+    p.n_ktiles = (d_model + 63) / 64;
+    p.err_flag = nullptr;
+    for (int k = 0; k < d_model / 2; ++k)
+        p.inv_freq[k] = static_cast<float>(std::pow(10000.0, -(2.0 * k) / static_cast<double>(d_model)));
+    return launch_pos_gen_tc(p, s) == cudaSuccess ? TXL_OK : TXL_ERR_CUDA;
+}
+
+size_t txl_rel_attn_workspace_size(int, int, int, int, const txl_mem*, txl_dtype) { return 0; }
+
+int txl_rel_attn_path(int B, int L, int H, int D, const txl_view* q, const txl_mem* mem, const txl_view* k_cur,
+                      const txl_view* v_cur, const void* r, int64_t ld_r, const txl_view* out, txl_dtype dtype)
+{
+    const txl_status st = check_attn(B, L, H, D, q, mem, k_cur, v_cur, r, ld_r, out, dtype);
+    if (st != TXL_OK) return -static_cast<int>(st);
+    return attn_tc_eligible(B, L, H, D, q, mem, k_cur, v_cur, r, ld_r, dtype) ? 1 : 2;
+}
+
+txl_status txl_rel_attn_fwd(int B, int L, int H, int D, int clamp_len, const txl_view* q, const txl_mem* mem,
+                            const txl_view* k_cur, const txl_view* v_cur, const float* u, const float* v_bias,
+                            const void* r, int64_t ld_r, int n_rows, float scale, const txl_view* out,
+                            txl_dtype dtype, void* workspace, size_t workspace_bytes, int* err_flag, void* stream)
+{
+    (void)workspace;
+    (void)workspace_bytes;
+    txl_status st = check_attn(B, L, H, D, q, mem, k_cur, v_cur, r, ld_r, out, dtype);
+    if (st != TXL_OK) return st;
+    if (clamp_len < 0 || !u || !v_bias) return TXL_ERR_INVALID_ARG;
+    const int M = (mem && mem->M > 0) ? mem->M : 0;
+    const int valid = M > 0 ? mem->valid : 0;
+    const int wp = M > 0 ? mem->wp : 0;
+    const int need_rows = std::min(M + L, clamp_len + 1);
+    if (n_rows < need_rows) return TXL_ERR_INVALID_ARG;
+    if (B == 0 || L == 0) return TXL_OK;
+    if (scale <= 0.f) scale = 1.0f / std::sqrt(static_cast<float>(D));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    if (attn_tc_eligible(B, L, H, D, q, mem, k_cur, v_cur, r, ld_r, dtype)) {
+        if (!encoder_ready()) return TXL_ERR_CUDA;
+        AttnTcParams p;
+        std::memset(&p, 0, sizeof(p));
+        bool ok = encode_view4(&p.tm_q, q->ptr, D, H, L, B, q->stride_h, q->stride_t, q->stride_b) &&
+                  encode_view4(&p.tm_kcur, k_cur->ptr, D, H, L, B, k_cur->stride_h, k_cur->stride_t, k_cur->stride_b) &&
+                  encode_view4(&p.tm_vcur, v_cur->ptr, D, H, L, B, v_cur->stride_h, v_cur->stride_t, v_cur->stride_b) &&
+                  encode_rtab(&p.tm_r, r, D, H, n_rows, ld_r);
+        if (ok && M > 0)
+            ok = encode_view4(&p.tm_kmem, mem->k, D, H, M, B, mem->stride_h, mem->stride_t, mem->stride_b) &&
+                 encode_view4(&p.tm_vmem, mem->v, D, H, M, B, mem->stride_h, mem->stride_t, mem->stride_b);
+        else if (ok) {
+            p.tm_kmem = p.tm_kcur;
+            p.tm_vmem = p.tm_vcur;
+        }
+        if (!ok) return TXL_ERR_CUDA;
+        p.u = u;
+        p.vb = v_bias;
+        p.out = out->ptr;
+        p.o_sb = out->stride_b;
+        p.o_st = out->stride_t;
+        p.o_sh = out->stride_h;
+        p.B = B; p.L = L; p.H = H; p.D = D; p.M = M;
+        p.lo = M - valid;
+        p.wp = wp;
+        p.C = clamp_len;
+        p.n_rows = n_rows;
+        p.n_qt = (L + 127) / 128;
+        p.n_atoms = D <= 64 ? 1 : 2;
+        p.k_steps = (D + 15) / 16;
+        p.qscale = scale * 1.4426950408889634f;
+        p.err_flag = err_flag;
+        if (B > 65535 || H > 65535) return TXL_ERR_UNSUPPORTED;
+        return launch_attn_tc(p, s) == cudaSuccess ? TXL_OK : TXL_ERR_CUDA;
+    }
+
+    AttnSimtParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.q = q->ptr; p.q_sb = q->stride_b; p.q_st = q->stride_t; p.q_sh = q->stride_h;
+    if (M > 0) {
+        p.kmem = mem->k; p.vmem = mem->v;
+        p.m_sb = mem->stride_b; p.m_st = mem->stride_t; p.m_sh = mem->stride_h;
+    }
+    p.kcur = k_cur->ptr; p.kc_sb = k_cur->stride_b; p.kc_st = k_cur->stride_t; p.kc_sh = k_cur->stride_h;
+    p.vcur = v_cur->ptr; p.vc_sb = v_cur->stride_b; p.vc_st = v_cur->stride_t; p.vc_sh = v_cur->stride_h;
+    p.out = out->ptr; p.o_sb = out->stride_b; p.o_st = out->stride_t; p.o_sh = out->stride_h;
+    p.u = u; p.vb = v_bias;
+    p.r = r; p.r_row = static_cast<int64_t>(H) * ld_r; p.r_head = ld_r;
+    p.B = B; p.L = L; p.H = H; p.D = D; p.M = M; p.lo = M - valid; p.wp = wp; p.C = clamp_len;
+    p.scale = scale;
+    return launch_attn_simt(p, dtype, s) == cudaSuccess ? TXL_OK : TXL_ERR_CUDA;
+}
+
+txl_status txl_mem_push(txl_mem* mem, const txl_view* k_new, const txl_view* v_new, int L, void* stream)
+{
+    if (!mem || !view_ok(k_new) || !view_ok(v_new) || L < 0) return TXL_ERR_INVALID_ARG;
+    if (mem->M < 0 || mem->B < 0 || mem->H <= 0 || mem->D <= 0) return TXL_ERR_INVALID_ARG;
+    if (mem->dtype != TXL_F32 && mem->dtype != TXL_BF16) return TXL_ERR_INVALID_ARG;
+    if (mem->M == 0) return mem->valid == 0 ? TXL_OK : TXL_ERR_INVALID_ARG;
+    if (!mem->k || !mem->v || mem->wp < 0 || mem->wp >= mem->M || mem->valid < 0 || mem->valid > mem->M)
+        return TXL_ERR_INVALID_ARG;
+    if (L == 0) return TXL_OK;
+    const int elem = mem->dtype == TXL_F32 ? 4 : 2;
+    MemPushParams p{};
+    p.k_new = k_new->ptr; p.v_new = v_new->ptr;
+    p.n_sb = k_new->stride_b; p.n_st = k_new->stride_t; p.n_sh = k_new->stride_h;
+    p.nv_sb = v_new->stride_b; p.nv_st = v_new->stride_t; p.nv_sh = v_new->stride_h;
+    p.k = mem->k; p.v = mem->v;
+    p.m_sb = mem->stride_b; p.m_st = mem->stride_t; p.m_sh = mem->stride_h;
+    p.B = mem->B; p.H = mem->H; p.D = mem->D; p.M = mem->M; p.wp = mem->wp;
+    p.t0 = L > mem->M ? L - mem->M : 0;
+    p.n_t = L - p.t0;
+    p.elem_bytes = elem;
+    const bool rows16 = ((static_cast<int64_t>(mem->D) * elem) & 15) == 0;
+    p.vec16 = rows16 && a16(k_new->ptr) && a16(v_new->ptr) && a16(mem->k) && a16(mem->v) &&
+              s16(k_new->stride_b, elem) && s16(k_new->stride_t, elem) && s16(k_new->stride_h, elem) &&
+              s16(v_new->stride_b, elem) && s16(v_new->stride_t, elem) && s16(v_new->stride_h, elem) &&
+              s16(mem->stride_b, elem) && s16(mem->stride_t, elem) && s16(mem->stride_h, elem);
+    if (launch_mem_push(p, static_cast<cudaStream_t>(stream)) != cudaSuccess) return TXL_ERR_CUDA;
+    mem->wp = static_cast<int>((static_cast<int64_t>(mem->wp) + L) % mem->M);
+    mem->valid = std::min(mem->valid + L, mem->M);
+    return TXL_OK;
+}
+
+txl_status txl_selftest_wait_timeout(int* err_flag, unsigned timeout_us, void* stream)
+{
+    if (!err_flag || timeout_us == 0 || timeout_us > 10000000u) return TXL_ERR_INVALID_ARG;
+    return launch_selftest_wait(err_flag, timeout_us, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? TXL_OK
+               : TXL_ERR_CUDA;
+}
+
+}  // extern "C"

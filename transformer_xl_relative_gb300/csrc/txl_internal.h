@@ -1,0 +1,86 @@
+// txl_internal.h -- kernel parameter blocks and launch entry points shared by the C-ABI host
+// code (txl_api.cu) and the kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/txl.h"
+
+namespace txl {
+
+constexpr int kMaxDModel = 4096;   // the bf16 path passes d_model/2 frequencies as parameters
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;   // 2 s: far above any healthy wait
+
+// ---------------------------------------------------------------- relative position table
+struct PosGenF32Params {
+    const float* W;      // [d_model][ld_w]
+    float* r;            // [n_rows][H][ld_r]
+    int64_t ld_w, ld_r;
+    int n_rows, d_model, H, D;
+};
+
+struct PosGenTcParams {
+    CUtensorMap tm_w;    // W_R as 2D (n = h*D+d, m): box 64 x 64, 128-byte swizzle
+    void* r;             // bf16 [n_rows][H][ld_r]
+    int64_t ld_r;
+    int n_rows, d_model, H, D;
+    int n_ktiles;        // ceil(d_model / 64)
+    int* err_flag;
+    float inv_freq[kMaxDModel / 2];   // 10000^(-2k/d_model), rounded from double on the host
+};
+
+cudaError_t launch_pos_gen_f32(const PosGenF32Params& p, cudaStream_t s);
+cudaError_t launch_pos_gen_tc(const PosGenTcParams& p, cudaStream_t s);
+
+// ---------------------------------------------------------------- attention (general SIMT)
+struct AttnSimtParams {
+    const void* q; int64_t q_sb, q_st, q_sh;
+    const void* kmem; const void* vmem; int64_t m_sb, m_st, m_sh;
+    const void* kcur; int64_t kc_sb, kc_st, kc_sh;
+    const void* vcur; int64_t vc_sb, vc_st, vc_sh;
+    void* out; int64_t o_sb, o_st, o_sh;
+    const float* u; const float* vb;
+    const void* r; int64_t r_row, r_head;       // element strides of the r table
+    int B, L, H, D, M, lo, wp, C;
+    float scale;
+};
+
+cudaError_t launch_attn_simt(const AttnSimtParams& p, txl_dtype dtype, cudaStream_t s);
+
+// ---------------------------------------------------------------- attention (fused tcgen05)
+struct AttnTcParams {
+    CUtensorMap tm_q;            // (d, h, t, b) box 64 x 1 x 128 x 1
+    CUtensorMap tm_kmem, tm_vmem;
+    CUtensorMap tm_kcur, tm_vcur;
+    CUtensorMap tm_r;            // (d, h, row) box 64 x 1 x 128
+    const float* u; const float* vb;   // [H][D] fp32
+    void* out; int64_t o_sb, o_st, o_sh;
+    int B, L, H, D, M, lo, wp, C, n_rows;
+    int n_qt;                    // query tiles of 128
+    int n_atoms;                 // 64-column atoms per row: 1 (D <= 64) or 2 (D <= 128)
+    int k_steps;                 // ceil(D / 16): UMMA K steps for the Q.K and Q.r products
+    float qscale;                // scale * log2(e)
+    int* err_flag;
+};
+
+cudaError_t launch_attn_tc(const AttnTcParams& p, cudaStream_t s);
+
+// ---------------------------------------------------------------- memory ring
+struct MemPushParams {
+    const void* k_new; const void* v_new;
+    int64_t n_sb, n_st, n_sh;           // strides of the k_new view
+    int64_t nv_sb, nv_st, nv_sh;        // strides of the v_new view
+    void* k; void* v;
+    int64_t m_sb, m_st, m_sh;           // ring strides
+    int B, H, D, M, wp, t0, n_t;        // copy positions t0 .. t0+n_t-1 of the segment
+    int elem_bytes;
+    int vec16;                          // 1: copy 16-byte chunks
+};
+
+cudaError_t launch_mem_push(const MemPushParams& p, cudaStream_t s);
+
+cudaError_t launch_selftest_wait(int* err_flag, unsigned timeout_us, cudaStream_t s);
+
+}  // namespace txl
