@@ -117,6 +117,17 @@ def _max_over_ranks(x: float, world: int, device) -> float:
     return float(t.item())
 
 
+def aggregate_value(world: int, step_flops: float, t_step_ms_max: float) -> float:
+    """Whole-job TFLOP/s of weak scaling: every rank runs one full replica of the workload per
+    step, and the job's step time is the slowest rank's."""
+    return world * step_flops / (t_step_ms_max * 1e-3) / 1e12
+
+
+def rank_seed(base: int, rank: int) -> int:
+    """Each replica draws its own inputs."""
+    return base + 7919 * rank
+
+
 def _barrier(world: int):
     if world > 1:
         import torch.distributed as dist
@@ -209,7 +220,7 @@ def run_txl(args):
     dt = cfg.torch_dtype
     n_rows = cfg.n_rows
     NSETS = 4
-    g = torch.Generator(device=device).manual_seed(cfg.seed + 7919 * rank)
+    g = torch.Generator(device=device).manual_seed(rank_seed(cfg.seed, rank))
     sets = []
     for _ in range(NSETS):
         q = torch.randn(B, L, H, D, generator=g, device=device).to(dt)
@@ -324,7 +335,7 @@ def run_txl(args):
     attn_flops, pos_flops = _flops(cfg)
     step_flops = attn_flops + pos_flops
     peak, peak_sust, _, peak_kind = _peaks()
-    value = world * step_flops / (t_step_ms * 1e-3) / 1e12
+    value = aggregate_value(world, step_flops, t_step_ms)
     achieved = attn_flops / (t_attn_ms * 1e-3) / 1e12
     kernel_src = os.path.join(ROOT, "transformer_xl_relative_gb300", "csrc", "txl_attn_tc.cu")
     line = {

@@ -31,7 +31,7 @@ class Config:
     seed: int
     segments: int = 1        # >1: streaming through the FIFO memory
     head_stride: int = 0     # elements between heads in q/k/v/out (0: D, dense)
-    ld_w: int = 0            # W_R row stride (0: H*D, dense)
+    ld_w: int = 0            # W_R row stride (0: H*D rounded up to a multiple of 8)
 
     @property
     def hs(self) -> int:
@@ -39,7 +39,7 @@ class Config:
 
     @property
     def ldw(self) -> int:
-        return self.ld_w or self.H * self.D
+        return self.ld_w or (self.H * self.D + 7) // 8 * 8
 
     @property
     def torch_dtype(self):
