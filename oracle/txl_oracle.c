@@ -129,7 +129,7 @@ static const double *txlo_rvec(txlo_job *J, int h, int delta_c, double *scratch)
     return scratch;
 }
 
-static void txlo_one_row(txlo_job *J, int b, int h, int i, double *s, double *rs)
+static void txlo_one_row(txlo_job *J, int b, int h, int i, double *s, double *rs, double *acc)
 {
     const int D = J->D, H = J->H, M = J->M, L = J->L;
     const int K = M + L;
@@ -156,15 +156,18 @@ static void txlo_one_row(txlo_job *J, int b, int h, int i, double *s, double *rs
         s[j] = exp(s[j] - mx);
         den += s[j];
     }
-    double *o = J->out + (((int64_t)b * L + i) * H + h) * D;
-    for (int d = 0; d < D; ++d) o[d] = 0.0;
+    /* accumulate in the caller's private buffer, then store the finished row: a row listed
+     * twice in a selection is then written twice with the same values, never raced on */
+    for (int d = 0; d < D; ++d) acc[d] = 0.0;
     for (int j = 0; j < K; ++j) {
         int visible = (j >= lo) && (j <= qpos);
         if (!visible) continue;
         double p = s[j] / den;
         const double *vj = J->v + (((int64_t)b * K + j) * H + h) * D;
-        for (int d = 0; d < D; ++d) o[d] += p * vj[d];
+        for (int d = 0; d < D; ++d) acc[d] += p * vj[d];
     }
+    double *o = J->out + (((int64_t)b * L + i) * H + h) * D;
+    for (int d = 0; d < D; ++d) o[d] = acc[d];
 }
 
 static void *txlo_worker(void *arg)
@@ -173,6 +176,7 @@ static void *txlo_worker(void *arg)
     const int K = J->M + J->L;
     double *s = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
     double *rs = (double *)malloc(sizeof(double) * (size_t)J->D);
+    double *acc = (double *)malloc(sizeof(double) * (size_t)J->D);
     int64_t total = J->sel ? J->n_sel : (int64_t)J->B * J->H * J->L;
     for (;;) {
         pthread_mutex_lock(&J->lock);
@@ -187,10 +191,11 @@ static void *txlo_worker(void *arg)
             h = (int)((w / J->L) % J->H);
             i = (int)(w % J->L);
         }
-        txlo_one_row(J, b, h, i, s, rs);
+        txlo_one_row(J, b, h, i, s, rs, acc);
     }
     free(s);
     free(rs);
+    free(acc);
     return NULL;
 }
 
@@ -323,6 +328,7 @@ static void *txlo_stream_worker(void *arg)
     const int T = J->n_seg * J->L, D = J->D, H = J->H;
     double *s = (double *)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
     double *rs = (double *)malloc(sizeof(double) * (size_t)D);
+    double *acc = (double *)malloc(sizeof(double) * (size_t)D);
     int64_t total = J->sel ? J->n_sel : (int64_t)J->B * H * T;
     for (;;) {
         pthread_mutex_lock(&J->lock);
@@ -350,16 +356,18 @@ static void *txlo_stream_worker(void *arg)
         }
         double den = 0.0;
         for (int g = g_lo; g <= t; ++g) { s[g] = exp(s[g] - mx); den += s[g]; }
-        double *o = J->out + (((int64_t)b * T + t) * H + h) * D;
-        for (int d = 0; d < D; ++d) o[d] = 0.0;
+        for (int d = 0; d < D; ++d) acc[d] = 0.0;        /* private, see txlo_one_row */
         for (int g = g_lo; g <= t; ++g) {
             double p = s[g] / den;
             const double *vg = J->v + (((int64_t)b * T + g) * H + h) * D;
-            for (int d = 0; d < D; ++d) o[d] += p * vg[d];
+            for (int d = 0; d < D; ++d) acc[d] += p * vg[d];
         }
+        double *o = J->out + (((int64_t)b * T + t) * H + h) * D;
+        for (int d = 0; d < D; ++d) o[d] = acc[d];
     }
     free(s);
     free(rs);
+    free(acc);
     return NULL;
 }
 

@@ -46,7 +46,7 @@ class Probe:
         self.kcur = torch.zeros(B, L, H, self.hs, dtype=torch.bfloat16, device=dev)[..., :D]
         self.vcur = torch.zeros(B, L, H, self.hs, dtype=torch.bfloat16, device=dev)[..., :D]
         self.kmem = torch.zeros(B, max(M, 1), H, self.hs, dtype=torch.bfloat16, device=dev)[:, :M, :, :D]
-        self.vmem = torch.zeros_like(self.kmem)
+        self.vmem = torch.zeros(B, max(M, 1), H, self.hs, dtype=torch.bfloat16, device=dev)[:, :M, :, :D]
         cv = torch.from_numpy(self.code).to(torch.bfloat16).to(dev)
         for j in range(M):
             self.vmem[:, (wp + j) % M] = cv[j][None, None, :]

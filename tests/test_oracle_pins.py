@@ -282,6 +282,21 @@ def test_row_subset_matches_full():
     assert np.isnan(part[0, 1, 1]).all()
 
 
+def test_repeated_rows_in_a_selection():
+    """A row listed several times in a multi-threaded selection gets the same value as alone."""
+    rng = np.random.default_rng(12)
+    q, k, v, u, vb, W = _rand_case(rng, 2, 2, 8, 16, 40, 30)
+    row = (1, 1, 33)
+    alone = oracle.rel_attn(q, k, v, u, vb, W, 30, 30, 1000, rows=[row], threads=1)
+    dup = oracle.rel_attn(q, k, v, u, vb, W, 30, 30, 1000, rows=[row] * 8 + [(0, 0, 1)], threads=8)
+    assert np.array_equal(alone[1, 33, 1], dup[1, 33, 1])
+    T = 3 * 16
+    qs, ks, vs = (rng.standard_normal((2, T, 2, 8)) for _ in range(3))
+    alone = oracle.stream_attn(qs, ks, vs, u, vb, W, 16, 20, 1000, rows=[(1, 0, 40)], threads=1)
+    dup = oracle.stream_attn(qs, ks, vs, u, vb, W, 16, 20, 1000, rows=[(1, 0, 40)] * 8, threads=8)
+    assert np.array_equal(alone[1, 40, 0], dup[1, 40, 0])
+
+
 # ---------------------------------------------------------------- recurrence and FIFO memory
 def test_stream_equals_single_calls_over_fifo_memory():
     """Transformer-XL 和相对位置编码 §2.3.1 + Transformer-XL架构解析 §1.1: segment s attends
