@@ -203,6 +203,14 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
         : "memory");
 }
 
+// Commit form taking the barrier's shared-memory address (hoisted out of issue loops).
+__device__ __forceinline__ void umma_commit_addr(uint32_t bar_saddr)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+        ::"r"(bar_saddr) : "memory");
+}
+
 // Arrive on an mbarrier once every tcgen05 operation issued so far by this thread completes.
 __device__ __forceinline__ void umma_commit(uint64_t* bar)
 {
@@ -225,6 +233,12 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r)
           "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
           "=r"(r[31])
         : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t* r)
+{
+    tmem_ld32(taddr, r);
+    tmem_ld32(taddr + 32, r + 32);
 }
 
 __device__ __forceinline__ void tmem_ld1(uint32_t taddr, uint32_t& r0)
@@ -314,6 +328,47 @@ __device__ __forceinline__ float add_bf16lo_f32(uint32_t w, float c)
     asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.bf16 %0, lo, %2;\n\t}"
         : "=f"(r) : "r"(w), "f"(c));
     return r;
+}
+
+// Packed fp32x2 arithmetic (sm_100+): two lanes of work per instruction.
+__device__ __forceinline__ uint64_t f2_pack(float a, float b)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& a, float& b)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c)
+{
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+__device__ __forceinline__ void sts_u16(uint32_t saddr, uint16_t v)
+{
+    asm volatile("st.shared.u16 [%0], %1;" ::"r"(saddr), "h"(v) : "memory");
 }
 
 __device__ __forceinline__ float ex2_approx(float x)
