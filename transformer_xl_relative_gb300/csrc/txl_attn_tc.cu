@@ -28,8 +28,10 @@
 // sums until the epilogue.
 //
 // Roles (352 threads): warps 0-7 softmax / correction / epilogue (two warpgroups), warp 8 TMA
-// producer of q, K and r tiles, warp 9 UMMA issuer and TMEM owner, warp 10 TMA producer of V
-// tiles (kept apart so that K and r prefetch is never held up behind a V slot).  Every wait is bounded (2 s) and aborts the CTA
+// producer of q, K and r tiles, warp 9 TMEM owner and issuer of the S and BD products, warp 10
+// TMA producer of V tiles (kept apart so that K and r prefetch is never held up behind a V slot).
+// For D <= 64 warp 10 also issues P.V, so the S/BD issue of the next tile and the P.V issue of
+// the current one proceed in two threads.  Every wait is bounded (2 s) and aborts the CTA
 // cleanly; every softmax thread executes every named barrier of the tile loop even after an
 // abort, so no warp can be left behind at a barrier.
 #include <cuda_bf16.h>
@@ -65,15 +67,15 @@ struct AttnSmem {
     static constexpr int BD = R + NS * NA * kTile;     // also the raw-Q staging area
     static constexpr int Bars = BD + kBdBytes;
     // q_full q_ready | k_full k_empty r_full r_empty (NS each) v_full v_empty (NV each) |
-    // s_full[2] bd_full bd_free p_full[2] pv_done o_full drain s_free[2]
-    static constexpr int NumBars = 2 + 4 * NS + 2 * NV + 11;
+    // s_full[2] bd_full bd_free p_full[2] pv_done o_full drain s_free[2] drain_v
+    static constexpr int NumBars = 2 + 4 * NS + 2 * NV + 12;
     static constexpr int Misc = Bars + NumBars * 8;
     static constexpr int Size = Misc + 16;
 };
 
 struct Bars {
     uint64_t *q_full, *q_ready, *k_full, *k_empty, *v_full, *v_empty, *r_full, *r_empty;
-    uint64_t *s_full, *bd_full, *bd_free, *p_full, *pv_done, *o_full, *drain, *s_free;
+    uint64_t *s_full, *bd_full, *bd_free, *p_full, *pv_done, *o_full, *drain, *s_free, *drain_v;
 };
 
 template <int NS, int NV>
@@ -90,6 +92,7 @@ __device__ __forceinline__ Bars carve_bars(uint8_t* base)
     r.p_full = r.bd_free + 1;
     r.pv_done = r.p_full + 2; r.o_full = r.pv_done + 1; r.drain = r.o_full + 1;
     r.s_free = r.drain + 1;
+    r.drain_v = r.s_free + 2;
     return r;
 }
 
@@ -208,6 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         mbar_init(&bar.p_full[0], 8); mbar_init(&bar.p_full[1], 8);
         mbar_init(bar.pv_done, 1); mbar_init(bar.o_full, 1); mbar_init(bar.drain, 1);
         mbar_init(&bar.s_free[0], 8); mbar_init(&bar.s_free[1], 8);
+        mbar_init(bar.drain_v, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -289,22 +293,54 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             }
         }
     } else if (warp == kValueWarp) {
-        // =========================================================== TMA producer: V
+        // =========================================================== TMA producer: V (+ P.V)
         if (lane == 0) {
             tma_prefetch_desc(&p.tm_vcur);
             if (M > 0) tma_prefetch_desc(&p.tm_vmem);
             int vc = 0;
-            for (int t = 0; t < n_t; ++t) {
+            auto load_v = [&](int t) -> bool {
                 const CUtensorMap* km;
                 const CUtensorMap* vm;
                 int row;
                 key_tile(t, km, vm, row);
                 const int s = t % NV;
-                if (!mbar_wait(&bar.v_empty[s], ((t / NV) & 1) ^ 1, wc, 12)) break;
+                if (!mbar_wait(&bar.v_empty[s], ((t / NV) & 1) ^ 1, wc, 12)) return false;
                 mbar_expect_tx(&bar.v_full[s], NA * kTile);
                 for (int a = 0; a < NA; ++a)
                     tma_load_4d(smem + S::V + (s * NA + a) * kTile, vm, 64 * a, h, row, b, &bar.v_full[s]);
                 ++vc;
+                return true;
+            };
+            if (!kSeparateP) {
+                for (int t = 0; t < n_t; ++t)
+                    if (!load_v(t)) break;
+            } else {
+                // O += P_t V_t from the P buffer, V of tile t + 1 requested before P_t is awaited
+                constexpr uint32_t idesc_pv = idesc_bf16(128, NPV, 0, 1);
+                const uint64_t v_d = sdesc_mn_sw128(smem_u32(smem + S::V), kTile);
+                constexpr uint64_t kStage = (NA * kTile) >> 4;
+                const uint32_t b_vempty = smem_u32(bar.v_empty), b_pvdone = smem_u32(bar.pv_done);
+                bool ok = load_v(0);
+                for (int t = 0; t < n_t && ok; ++t) {
+                    if (t + 1 < n_t && !(ok = load_v(t + 1))) break;
+                    const int s = t % NV;
+                    if (!(ok = mbar_wait(&bar.p_full[t & 1], (t >> 1) & 1, wc, 23))) break;
+                    if (!(ok = mbar_wait(&bar.v_full[s], (t / NV) & 1, wc, 24))) break;
+                    tc_fence_after();
+                    const uint64_t vb = v_d + kStage * s;
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        umma_ts(tmem + kColO, tmem + kColP + (kk >> 2) * 32 + (kk & 3) * 8,
+                                vb + kk * (2048 >> 4), idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
+                    umma_commit_addr(b_vempty + 8 * s);
+                    umma_commit_addr(b_pvdone);
+                }
+                umma_commit(ok ? bar.o_full : bar.drain_v);
+                if (!ok) {
+                    int never = 0;
+                    const WaitCtl dw{&never, nullptr, 100000000ull};
+                    (void)mbar_wait(bar.drain_v, 0, dw, 28);
+                }
             }
             if (*abort_flag) {
                 int never = 0;
@@ -354,19 +390,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                 ++bd_uses;
                 return true;
             };
-            // P of tile t: with a separate P buffer, keys 0-63 in its columns 0-31 and keys 64-127
-            // in 32-63; otherwise in the S buffer of t, keys 0-63 in columns 0-31 and keys
-            // 64-127 in columns 64-95 (each softmax half writes inside its own S columns).
+            // P of tile t (D = 128; for D <= 64 the V warp issues P.V from the separate P buffer,
+            // keys 0-63 in its columns 0-31 and keys 64-127 in 32-63): in the S buffer of t, keys
+            // 0-63 in columns 0-31 and keys 64-127 in columns 64-95 (each softmax half writes
+            // inside its own S columns).
             auto mma_pv = [&](int t) -> bool {
                 const int s = t % NV;
                 if (!mbar_wait(&bar.p_full[t & 1], (t >> 1) & 1, wc, 23)) return false;
                 if (!mbar_wait(&bar.v_full[s], (t / NV) & 1, wc, 24)) return false;
                 tc_fence_after();
                 const uint64_t vb = v_d + kStage * s;
-                const uint32_t pcol = kSeparateP ? tmem + kColP : tmem + ((t & 1) ? kColS1 : kColS0);
+                const uint32_t pcol = tmem + ((t & 1) ? kColS1 : kColS0);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    umma_ts(tmem + kColO, pcol + (kk >> 2) * (kSeparateP ? 32 : 64) + (kk & 3) * 8,
+                    umma_ts(tmem + kColO, pcol + (kk >> 2) * 64 + (kk & 3) * 8,
                             vb + kk * (2048 >> 4), idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
                 umma_commit_addr(b_vempty + 8 * s);
                 umma_commit_addr(b_pvdone);
@@ -397,15 +434,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             if (ok) ok = mma_s(0);
             if (ok && plan.need_chunk(0, C)) ok = mma_bd();
             // tile t + 1's products are issued while the softmax of tile t runs; P.V of tile t
-            // follows once its P is in TMEM
+            // (D = 128) follows once its P is in TMEM
             for (int t = 0; t < n_t && ok; ++t) {
                 if (t + 1 < n_t) {
                     if (!(ok = mma_s(t + 1))) break;
                     if (plan.need_chunk(t + 1, C) && !(ok = mma_bd())) break;
                 }
-                if (!(ok = mma_pv(t))) break;
+                if (!kSeparateP && !(ok = mma_pv(t))) break;
             }
-            umma_commit(ok ? bar.o_full : bar.drain);
+            // every S and BD product is awaited by the softmax before the CTA ends; O is complete
+            // when the issuer of P.V commits o_full
+            if (!kSeparateP || !ok) umma_commit(ok ? bar.o_full : bar.drain);
             if (!ok) {
                 int never = 0;
                 const WaitCtl dw{&never, nullptr, 100000000ull};
