@@ -257,6 +257,14 @@ def run_txl(args):
         for s in range(NSETS):
             q, k, v = sets[s]
             txl.rel_attn_fwd(q, mems[s], k[:, M:], v[:, M:], u, vb, r, n_rows, C, outs[s])
+    pos_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(pos_graph, stream=stream):
+        for s in range(NSETS):
+            txl.rel_pos_gen(W, r, n_rows, cfg.d_model, H, D)
+    push_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(push_graph, stream=stream):
+        for s in range(NSETS):
+            txl.mem_push(ring, sets[s][1][:, M:], sets[s][2][:, M:])
 
     reps = max(1, math.ceil(args.steps / NSETS))
     steps = reps * NSETS
@@ -296,6 +304,22 @@ def run_txl(args):
         a1.record(stream)
     torch.cuda.synchronize()
     t_attn_ms = a0.elapsed_time(a1) / steps
+
+    def graph_ms(g, reps_):
+        with torch.cuda.stream(stream):
+            g.replay()
+        torch.cuda.synchronize()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            g0.record(stream)
+            for _ in range(reps_):
+                g.replay()
+            g1.record(stream)
+        torch.cuda.synchronize()
+        return g0.elapsed_time(g1) / (reps_ * NSETS)
+
+    t_pos_ms = graph_ms(pos_graph, max(1, reps // 4))
+    t_push_ms = graph_ms(push_graph, max(1, reps // 4))
     sampler.stop()
     clocks = sampler.summary(wall0, wall1)
 
@@ -357,6 +381,8 @@ def run_txl(args):
                    "parallelism": "dp%d: independent replicas, no collective on the data path" % world},
         "tokens_per_s": world * B * L / (t_step_ms * 1e-3),
         "attn_tflops": achieved,
+        "kernel_us": {"rel_attn_fwd": 1e3 * t_attn_ms, "rel_pos_gen": 1e3 * t_pos_ms,
+                      "mem_push": 1e3 * t_push_ms},
         "frac_of_bf16_peak_step": value / world / peak,
         "clocks": clocks,
         "e2e": {"value": world * step_flops / (t_e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",

@@ -284,7 +284,9 @@ txl_status txl_mem_push(txl_mem* mem, const txl_view* k_new, const txl_view* v_n
     p.vec16 = rows16 && a16(k_new->ptr) && a16(v_new->ptr) && a16(mem->k) && a16(mem->v) &&
               s16(k_new->stride_b, elem) && s16(k_new->stride_t, elem) && s16(k_new->stride_h, elem) &&
               s16(v_new->stride_b, elem) && s16(v_new->stride_t, elem) && s16(v_new->stride_h, elem) &&
-              s16(mem->stride_b, elem) && s16(mem->stride_t, elem) && s16(mem->stride_h, elem);
+              s16(mem->stride_b, elem) && s16(mem->stride_t, elem) && s16(mem->stride_h, elem) &&
+              static_cast<int64_t>(mem->B) * p.n_t <= INT32_MAX &&
+              static_cast<int64_t>(mem->M) + L <= INT32_MAX;         // 32-bit row and slot arithmetic
     if (launch_mem_push(p, static_cast<cudaStream_t>(stream)) != cudaSuccess) return TXL_ERR_CUDA;
     mem->wp = static_cast<int>((static_cast<int64_t>(mem->wp) + L) % mem->M);
     mem->valid = std::min(mem->valid + L, mem->M);

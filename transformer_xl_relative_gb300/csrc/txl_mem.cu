@@ -4,7 +4,7 @@
 //
 // Pure data movement, HBM-bound: every 16-byte chunk of k_new/v_new that survives the push is
 // read once and written once to its ring slot (wp + t) mod M.  Consecutive threads handle
-// consecutive chunks of one (b, t, h) row, so loads and stores are coalesced 16-byte accesses.
+// consecutive chunks of one (b, t) row, so loads and stores are coalesced 16-byte accesses.
 #include "txl_internal.h"
 #include "txl_ptx.cuh"
 
@@ -12,29 +12,46 @@ namespace txl {
 
 namespace {
 
-constexpr int kPushThreads = 256;
+constexpr int kPushThreads = 128;
+constexpr int kPushRows = 4;            // (b, t) rows per block pass: 4 loads in flight per thread
 
+// Grid (row groups, 2): blockIdx.y selects keys (0) or values (1).  Thread c of a block copies
+// 16-byte chunk c (head c / cpr, chunk c mod cpr) of kPushRows consecutive (b, t) rows, issuing
+// all loads before the stores.  Index arithmetic is 32-bit (the host guarantees B * n_t and
+// M + L fit) and is done once per row, not per byte.
 __global__ void __launch_bounds__(kPushThreads) mem_push_vec16(MemPushParams p)
 {
-    const int cpr = (p.D * p.elem_bytes) >> 4;             // 16-byte chunks per head row
-    const int64_t per_tensor = static_cast<int64_t>(p.B) * p.n_t * p.H * cpr;
-    const int64_t total = 2 * per_tensor;
-    for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
-         idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int which = idx >= per_tensor;               // 0: keys, 1: values
-        int64_t rem = idx - which * per_tensor;
-        const int c = static_cast<int>(rem % cpr); rem /= cpr;
-        const int h = static_cast<int>(rem % p.H); rem /= p.H;
-        const int t = static_cast<int>(rem % p.n_t) + p.t0;
-        const int b = static_cast<int>(rem / p.n_t);
-        const int slot = static_cast<int>((static_cast<int64_t>(p.wp) + t) % p.M);
-        const char* src = static_cast<const char*>(which ? p.v_new : p.k_new);
-        char* dst = static_cast<char*>(which ? p.v : p.k);
-        const int64_t so = which ? (b * p.nv_sb + t * p.nv_st + h * p.nv_sh)
-                                 : (b * p.n_sb + t * p.n_st + h * p.n_sh);
-        const int64_t d_off = b * p.m_sb + slot * p.m_st + h * p.m_sh;
-        const uint4 val = __ldg(reinterpret_cast<const uint4*>(src + so * p.elem_bytes) + c);
-        reinterpret_cast<uint4*>(dst + d_off * p.elem_bytes)[c] = val;
+    const int which = blockIdx.y;
+    const int eb = p.elem_bytes;
+    const int cpr = (p.D * eb) >> 4;                       // 16-byte chunks per head row
+    const int per_row = p.H * cpr;
+    const char* src = static_cast<const char*>(which ? p.v_new : p.k_new);
+    char* dst = static_cast<char*>(which ? p.v : p.k);
+    const int64_t ssb = (which ? p.nv_sb : p.n_sb) * eb, sst = (which ? p.nv_st : p.n_st) * eb;
+    const int64_t ssh = (which ? p.nv_sh : p.n_sh) * eb;
+    const int64_t dsb = p.m_sb * eb, dst_t = p.m_st * eb, dsh = p.m_sh * eb;
+    const int rows = p.B * p.n_t;
+    for (int c = threadIdx.x; c < per_row; c += kPushThreads) {
+        const int h = c / cpr, cc = c - h * cpr;
+        const int64_t so = h * ssh + 16 * cc, dso = h * dsh + 16 * cc;
+        for (int r0 = blockIdx.x * kPushRows; r0 < rows; r0 += gridDim.x * kPushRows) {
+            int b = r0 / p.n_t, t = r0 - b * p.n_t;
+            uint4 val[kPushRows];
+            int64_t doff[kPushRows];
+#pragma unroll
+            for (int k = 0; k < kPushRows; ++k) {
+                const int tt = t + p.t0;                   // position inside the segment
+                if (r0 + k < rows) {
+                    const int slot = (p.wp + tt) % p.M;
+                    val[k] = __ldg(reinterpret_cast<const uint4*>(src + b * ssb + tt * sst + so));
+                    doff[k] = b * dsb + slot * dst_t + dso;
+                }
+                if (++t == p.n_t) { t = 0; ++b; }
+            }
+#pragma unroll
+            for (int k = 0; k < kPushRows; ++k)
+                if (r0 + k < rows) *reinterpret_cast<uint4*>(dst + doff[k]) = val[k];
+        }
     }
 }
 
@@ -90,13 +107,17 @@ cudaError_t launch_mem_push(const MemPushParams& p, cudaStream_t s)
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    int64_t blocks = (work + kPushThreads - 1) / kPushThreads;
-    const int64_t cap = static_cast<int64_t>(sms) * 8;     // grid-stride beyond 8 CTAs per SM
-    if (blocks > cap) blocks = cap;
-    if (p.vec16)
-        mem_push_vec16<<<static_cast<unsigned>(blocks), kPushThreads, 0, s>>>(p);
-    else
+    const int64_t cap = static_cast<int64_t>(sms) * 16;    // grid-stride beyond 16 CTAs per SM
+    if (p.vec16) {
+        const int64_t rows = static_cast<int64_t>(p.B) * p.n_t;
+        int64_t blocks = (rows + kPushRows - 1) / kPushRows;
+        if (blocks > cap / 2) blocks = cap / 2;
+        mem_push_vec16<<<dim3(static_cast<unsigned>(blocks), 2), kPushThreads, 0, s>>>(p);
+    } else {
+        int64_t blocks = (work + kPushThreads - 1) / kPushThreads;
+        if (blocks > cap) blocks = cap;
         mem_push_scalar<<<static_cast<unsigned>(blocks), kPushThreads, 0, s>>>(p);
+    }
     return cudaGetLastError();
 }
 

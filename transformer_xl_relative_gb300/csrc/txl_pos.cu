@@ -5,12 +5,14 @@
 //   position projection W_{k,R}, r_proj without bias in "TransformerXL 相对位置编码" §3.1).
 //
 // bf16 path: one tcgen05 GEMM per 128 x 128 output tile.  The A operand (128 distances x 64
-// sinusoid columns) is generated on chip by four warps straight into the 128-byte-swizzled
+// sinusoid columns) is generated on chip by eight warps straight into the 128-byte-swizzled
 // shared-memory layout the tensor core reads; it never exists in HBM.  W_R tiles arrive by TMA.
-// Generation uses angle addition from two small tables per K tile:
-//   angle(delta0 + 16a + b) = angle(delta0 + 16a) + angle(b),  a in [0,8), b in [0,16)
-// so each CTA evaluates 768 sin/cos pairs per 64-column K tile instead of 4096, and each element
-// costs one complex multiply.  Warp 4 issues TMA, warp 5 issues UMMA (fp32 accumulator in TMEM).
+// Generation advances along the distance axis by angle addition,
+//   angle((delta + 1) w) = angle(delta w) + angle(w),
+// so each thread evaluates two sines/cosines per K tile and each further element costs one
+// complex multiply.  Sixteen generator warps (four per scheduler) keep the short dependency
+// chains of the generation overlapped; warp 16 issues TMA, warp 17 issues UMMA (fp32
+// accumulator in TMEM).
 #include <cmath>
 
 #include <cuda_bf16.h>
@@ -48,22 +50,46 @@ __global__ void __launch_bounds__(kPosF32Threads) pos_gen_f32_kernel(PosGenF32Pa
 }
 
 // ------------------------------------------------------------------------------- bf16 tcgen05
-constexpr int kPosStages = 4;
-constexpr int kPosThreads = 192;            // warps 0-3 generate + epilogue, 4 TMA, 5 UMMA
+constexpr int kPosStages = 6;
+constexpr int kPosGenWarps = 16;                            // generate the A operand + epilogue
+constexpr int kPosTmaWarp = kPosGenWarps;                   // W_R tiles
+constexpr int kPosMmaWarp = kPosGenWarps + 1;               // UMMA issue, TMEM owner
+constexpr int kPosThreads = 32 * (kPosGenWarps + 2);
 constexpr int kTileBytes = 128 * 128;       // 16 KB: 128 rows x 128 B (A tile) or 2 x 8 KB (B)
+constexpr int kRowsPerWarp = 128 / kPosGenWarps;            // distances one generator warp covers
 
 struct PosSmem {
     // offsets from a 1024-byte aligned base
     static constexpr int A = 0;                                   // kPosStages x 16 KB
     static constexpr int Bt = A + kPosStages * kTileBytes;        // kPosStages x 16 KB
-    static constexpr int TabBase = Bt + kPosStages * kTileBytes;  // float2 [32 k][8 a]
-    static constexpr int TabStep = TabBase + 32 * 8 * 8;          // float2 [32 k][16 b]
-    static constexpr int Bars = TabStep + 32 * 16 * 8;
+    static constexpr int Freq = Bt + kPosStages * kTileBytes;     // float [kMaxDModel / 2]
+    static constexpr int Bars = Freq + kMaxDModel / 2 * 4;
     static constexpr int NumBars = 3 * kPosStages + 2;
     static constexpr int Misc = Bars + NumBars * 8;                // tmem base, abort flag
     static constexpr int Size = Misc + 16;
 };
 
+// sin and cos of an angle of moderate size (|x| < 2^20): Cody-Waite reduction modulo 2 pi with
+// a two-constant split of 2 pi (fp32(2 pi) and the fp32 remainder), then the hardware sine and
+// cosine on [-pi, pi], whose absolute error there is about 2^-21.
+__device__ __forceinline__ void sincos_reduced(float x, float& sv, float& cv)
+{
+    constexpr float kTwoPiHi = 6.28318548202514648f;        // fp32(2 pi)
+    constexpr float kTwoPiLo = -1.74845553146951717e-07f;   // fp32(2 pi - kTwoPiHi)
+    constexpr float kInvTwoPi = 0.159154936671257019f;
+    const float n = rintf(x * kInvTwoPi);
+    float r = fmaf(-n, kTwoPiHi, x);
+    r = fmaf(-n, kTwoPiLo, r);
+    sv = __sinf(r);
+    cv = __cosf(r);
+}
+
+// Grid: (row tiles of 128 distances, column tiles of 128 (h, d) columns).  Per 64-column K tile
+// of the sinusoid, generator lane k owns frequency w_k of the tile and warp g the 8 distances
+// delta0 + 8 g + b, b = 0..7: it evaluates the angle of the first of them and of one step w_k,
+// then advances by rotation, (sin, cos)(x + w) = (s cw + c sw, c cw - s sw), writing each bf16
+// (sin, cos) pair as one 32-bit word into the 128-byte-swizzled K-major layout the tensor core
+// reads (a warp writes one full 128-byte row per store: no bank conflicts).
 __global__ void __launch_bounds__(kPosThreads, 1) pos_gen_tc_kernel(const __grid_constant__ PosGenTcParams p)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -77,14 +103,17 @@ __global__ void __launch_bounds__(kPosThreads, 1) pos_gen_tc_kernel(const __grid
     uint64_t* drain = acc_full + 1;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + PosSmem::Misc);
     int* abort_flag = reinterpret_cast<int*>(smem + PosSmem::Misc + 4);
+    float* freq = reinterpret_cast<float*>(smem + PosSmem::Freq);
 
     if ((smem_u32(smem) & 1023u) != 0) {        // the swizzled layouts need a 1 KB aligned base
         if (tid == 0 && p.err_flag) atomicCAS(p.err_flag, 0, TXL_ERR_ALIGNMENT);
         return;
     }
+    const int half = p.d_model >> 1;
+    for (int k = tid; k < half; k += kPosThreads) freq[k] = p.inv_freq[k];
     if (tid == 0) {
         for (int s = 0; s < kPosStages; ++s) {
-            mbar_init(&full_a[s], 4);
+            mbar_init(&full_a[s], kPosGenWarps);
             mbar_init(&full_b[s], 1);
             mbar_init(&empty[s], 1);
         }
@@ -93,7 +122,7 @@ __global__ void __launch_bounds__(kPosThreads, 1) pos_gen_tc_kernel(const __grid
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 5) tmem_alloc(tmem_holder, 128);
+    if (warp == kPosMmaWarp) tmem_alloc(tmem_holder, 128);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -104,7 +133,7 @@ __global__ void __launch_bounds__(kPosThreads, 1) pos_gen_tc_kernel(const __grid
     const int n0 = blockIdx.y * 128;
     const int nk = p.n_ktiles;
 
-    if (warp == 4) {
+    if (warp == kPosTmaWarp) {
         // ------------------------------------------------ TMA producer: W_R tiles
         if (lane == 0) {
             tma_prefetch_desc(&p.tm_w);
@@ -127,7 +156,7 @@ __global__ void __launch_bounds__(kPosThreads, 1) pos_gen_tc_kernel(const __grid
                     if (kt >= 0) (void)mbar_wait(&full_b[kt % kPosStages], (kt / kPosStages) & 1, drain_wc, 2);
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == kPosMmaWarp) {
         // ------------------------------------------------ UMMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_bf16(128, 128, 0, 1);
@@ -157,67 +186,50 @@ __global__ void __launch_bounds__(kPosThreads, 1) pos_gen_tc_kernel(const __grid
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------ generators (warps 0-3), row = tid
-        float2* tab_base = reinterpret_cast<float2*>(smem + PosSmem::TabBase);   // [k][a]
-        float2* tab_step = reinterpret_cast<float2*>(smem + PosSmem::TabStep);   // [k][b]
-        const int a = tid >> 4, b = tid & 15;
-        const int half = p.d_model >> 1;
+        // ------------------------------------------------ generators (warps 0-7)
+        const int row0 = kRowsPerWarp * warp;                 // first local distance of the warp
+        const float first = static_cast<float>(delta0 + row0);
         bool ok = true;
-        // Every generator warp runs all nk iterations and both named barriers of each, even
-        // after an abort (work is then skipped), so no warp can be left at a barrier.
-        for (int kt = 0; kt < nk; ++kt) {
+        for (int kt = 0; kt < nk && ok; ++kt) {
             const int s = kt % kPosStages;
-            named_bar_sync(1, 128);                      // previous tables fully consumed
-            if (ok) {
-                for (int e = tid; e < 32 * 24; e += 128) {   // angle tables of this K tile
-                    int kl, mult;
-                    float2* dst;
-                    if (e < 256) { kl = e >> 3; mult = delta0 + 16 * (e & 7); dst = tab_base + e; }
-                    else { kl = (e - 256) >> 4; mult = (e - 256) & 15; dst = tab_step + (e - 256); }
-                    const int kg = kt * 32 + kl;
-                    float sv = 0.f, cv = 1.f;
-                    if (kg < half) sincosf(static_cast<float>(mult) * p.inv_freq[kg], &sv, &cv);
-                    *dst = make_float2(sv, cv);
-                }
+            const int kg = kt * 32 + lane;
+            float sv = 0.f, cv = 0.f, sw = 0.f, cw = 1.f;     // frequencies past d_model/2: zero
+            if (kg < half) {
+                const float w = freq[kg];
+                sincos_reduced(first * w, sv, cv);
+                sincos_reduced(w, sw, cw);
             }
-            named_bar_sync(1, 128);
-            if (ok) ok = warp_wait(&empty[s], ((kt / kPosStages) & 1) ^ 1, wc, 6);
-            if (!ok) continue;
-            uint8_t* row = smem + PosSmem::A + s * kTileBytes + tid * 128;
+            ok = warp_wait(&empty[s], ((kt / kPosStages) & 1) ^ 1, wc, 6);
+            if (!ok) break;
+            const uint32_t tile = smem_u32(smem + PosSmem::A + s * kTileBytes);
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {                // 16-byte chunk c = frequencies 4c..4c+3
-                uint32_t w[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int kl = 4 * c + j;
-                    const int kg = kt * 32 + kl;
-                    const float2 x = tab_base[kl * 8 + a];
-                    const float2 y = tab_step[kl * 16 + b];
-                    float sv = fmaf(x.x, y.y, x.y * y.x);          // sin(A+B)
-                    float cv = fmaf(x.y, y.y, -(x.x * y.x));       // cos(A+B)
-                    if (kg >= half) { sv = 0.f; cv = 0.f; }
-                    w[j] = pack_bf16x2(sv, cv);
-                }
-                const int pc = c ^ (tid & 7);
-                *reinterpret_cast<uint4*>(row + pc * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+            for (int b = 0; b < kRowsPerWarp; ++b) {
+                const int row = row0 + b;
+                const uint32_t addr = tile + row * 128 + ((((lane >> 2) ^ (row & 7)) << 4) | ((lane & 3) << 2));
+                asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(pack_bf16x2(sv, cv)) : "memory");
+                const float sn = fmaf(sv, cw, cv * sw);
+                const float cn = fmaf(cv, cw, -(sv * sw));
+                sv = sn;
+                cv = cn;
             }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&full_a[s]);
         }
+        if (ok) ok = warp_wait(acc_full, 0, wc, 7);
         if (ok) {
-            ok = warp_wait(acc_full, 0, wc, 7);
-        }
-        if (ok) {
+            // epilogue: warp g reads TMEM lanes 32 (g mod 4) .. +32, columns 32 (g / 4) .. +32
             tc_fence_after();
-            const int delta = delta0 + tid;
+            const int li = 32 * (warp & 3) + lane;
+            const int delta = delta0 + li;
             const int HD = p.H * p.D;
             const bool dense = (p.ld_r == p.D) && (HD % 8 == 0);
             __nv_bfloat16* rrow = static_cast<__nv_bfloat16*>(p.r) + static_cast<int64_t>(delta) * p.H * p.ld_r;
 #pragma unroll 1
-            for (int cb = 0; cb < 4; ++cb) {
+            constexpr int kColBlocks = 16 / kPosGenWarps;          // 32-column blocks per warp
+            for (int cb = (warp >> 2) * kColBlocks; cb < ((warp >> 2) + 1) * kColBlocks; ++cb) {
                 uint32_t v[32];
-                tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + cb * 32, v);
+                tmem_ld32(tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + cb * 32, v);
                 tmem_ld_wait();
                 if (delta >= p.n_rows) continue;
                 const int nb = n0 + cb * 32;
@@ -244,7 +256,7 @@ __global__ void __launch_bounds__(kPosThreads, 1) pos_gen_tc_kernel(const __grid
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kPosMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, 128);
     }
