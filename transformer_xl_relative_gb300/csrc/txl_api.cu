@@ -35,9 +35,9 @@ bool encoder_ready()
 inline bool a16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool s16(int64_t stride_elems, int elem) { return ((stride_elems * elem) & 15) == 0; }
 
-// [B][T][H][D] view -> TMA dims (d, h, t, b), box (64, 1, 128, 1), 128-byte swizzle, bf16.
+// [B][T][H][D] view -> TMA dims (d, h, t, b), box (64, 1, box_t, 1), 128-byte swizzle, bf16.
 bool encode_view4(CUtensorMap* map, const void* ptr, int D, int H, int T, int B, int64_t sh,
-                  int64_t st, int64_t sb)
+                  int64_t st, int64_t sb, unsigned box_t = 128)
 {
     const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
                                 static_cast<cuuint64_t>(T > 0 ? T : 1), static_cast<cuuint64_t>(B)};
@@ -47,7 +47,7 @@ bool encode_view4(CUtensorMap* map, const void* ptr, int D, int H, int T, int B,
         static_cast<cuuint64_t>(H > 1 ? sh * 2 : biggest),
         static_cast<cuuint64_t>(T > 1 ? st * 2 : biggest),
         static_cast<cuuint64_t>(B > 1 ? sb * 2 : biggest)};
-    const cuuint32_t box[4] = {64, 1, 128, 1};
+    const cuuint32_t box[4] = {64, 1, box_t, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -68,6 +68,19 @@ bool encode_rtab(CUtensorMap* map, const void* r, int D, int H, int n_rows, int6
 }
 
 bool view_ok(const txl_view* v) { return v && v->ptr; }
+
+// Streaming multiprocessors of the current device (queried once per device).
+int sm_count()
+{
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64) cache[dev] = n;
+    return n;
+}
 
 bool view_tma_ok(const txl_view* v, int T, int H, int B)
 {
@@ -239,6 +252,24 @@ txl_status txl_rel_attn_fwd(int B, int L, int H, int D, int clamp_len, const txl
         p.k_steps = (D + 15) / 16;
         p.qscale = scale * 1.4426950408889634f;
         p.err_flag = err_flag;
+        if (p.n_atoms == 1) {
+            if (static_cast<int64_t>(p.n_qt) * H * B > INT32_MAX) return TXL_ERR_UNSUPPORTED;
+            // even and odd query rows as two maps stepping two tokens per row; the odd map starts
+            // one token in and has floor(L/2) rows, so no load reads past the tensor (with L = 1
+            // the odd rows are taken from the even map: they belong to no query and are not stored)
+            const char* q0 = static_cast<const char*>(q->ptr);
+            bool okq = encode_view4(&p.tm_qe, q0, D, H, (L + 1) / 2, B, q->stride_h, 2 * q->stride_t,
+                                    q->stride_b, 64);
+            if (okq && L / 2 > 0)
+                okq = encode_view4(&p.tm_qo, q0 + q->stride_t * 2, D, H, L / 2, B, q->stride_h,
+                                   2 * q->stride_t, q->stride_b, 64);
+            else
+                p.tm_qo = p.tm_qe;
+            if (!okq) return TXL_ERR_CUDA;
+            const int sms = sm_count();
+            if (sms <= 0) return TXL_ERR_CUDA;
+            return launch_attn_persist(p, sms, s) == cudaSuccess ? TXL_OK : TXL_ERR_CUDA;
+        }
         if (B > 65535 || H > 65535) return TXL_ERR_UNSUPPORTED;
         return launch_attn_tc(p, s) == cudaSuccess ? TXL_OK : TXL_ERR_CUDA;
     }

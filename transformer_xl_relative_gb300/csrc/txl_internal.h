@@ -55,6 +55,10 @@ struct AttnTcParams {
     CUtensorMap tm_kmem, tm_vmem;
     CUtensorMap tm_kcur, tm_vcur;
     CUtensorMap tm_r;            // (d, h, row) box 64 x 1 x 128
+    // d_head <= 64 (persistent kernel): q rows i0, i0+2, .. (tm_qe) and i0+1, i0+3, .. (tm_qo),
+    // (d, h, t/2, b) box 64 x 1 x 64 x 1, so one tile lands with even queries in rows 0-63 and
+    // odd queries in rows 64-127
+    CUtensorMap tm_qe, tm_qo;
     const float* u; const float* vb;   // [H][D] fp32
     void* out; int64_t o_sb, o_st, o_sh;
     int B, L, H, D, M, lo, wp, C, n_rows;
@@ -66,6 +70,8 @@ struct AttnTcParams {
 };
 
 cudaError_t launch_attn_tc(const AttnTcParams& p, cudaStream_t s);
+// d_head <= 64: one persistent CTA per SM (at most sm_count CTAs) over all query tiles
+cudaError_t launch_attn_persist(const AttnTcParams& p, int sm_count, cudaStream_t s);
 
 // ---------------------------------------------------------------- memory ring
 struct MemPushParams {

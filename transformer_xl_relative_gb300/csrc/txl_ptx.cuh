@@ -43,15 +43,20 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes)
                  ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
 }
 
+// A thread that finds the phase incomplete may be suspended inside try_wait; the hint bounds that
+// suspension (ns) so that a waiter is never left asleep long after the phase has completed (a
+// waiter resumed only by the default limit was observed microseconds late).
+constexpr uint32_t kTryWaitSuspendNs = 200;
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
 {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(smem_u32(bar)), "r"(parity), "n"(kTryWaitSuspendNs)
         : "memory");
     return ok != 0;
 }
