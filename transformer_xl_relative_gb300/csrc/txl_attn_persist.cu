@@ -261,7 +261,7 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_persist_kernel(const __grid
             }
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bar.q_ready[qb]);
+            mbar_arrive_if(&bar.q_ready[qb], lane == 0);
         }
     } else if (warp == kPMmaWarp) {
         // =========================================================== UMMA issuer: S and BD
@@ -448,7 +448,7 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_persist_kernel(const __grid
                     bdc_bits = v0;
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(bar.bd_free);
+                    mbar_arrive_if(bar.bd_free, lane == 0);
                 }
                 ++bd;
             }
@@ -471,7 +471,7 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_persist_kernel(const __grid
                             tmem_ld_wait();
                             tc_fence_before();
                             __syncwarp();
-                            if (lane == 0) mbar_arrive(bar.bd_free);
+                            mbar_arrive_if(bar.bd_free, lane == 0);
                             const int cc = C - 128 * t - 64 * hf;   // first local column at the clamp
                             if (it.clampc && cc < 64) {
 #pragma unroll
@@ -488,7 +488,7 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_persist_kernel(const __grid
                     tmem_ld_wait();
                     tc_fence_before();                  // the S buffer may now take S of T + 2
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&bar.s_free[T & 1]);
+                    mbar_arrive_if(&bar.s_free[T & 1], lane == 0);
 #pragma unroll
                     for (int k = 0; k < 64; ++k) s[k] = __uint_as_float(su[k]);
                 }
@@ -566,7 +566,7 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_persist_kernel(const __grid
                     tmem_st_wait();
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0 && ok) mbar_arrive(&bar.p_full[T & 1]);
+                    mbar_arrive_if(&bar.p_full[T & 1], lane == 0 && ok);
                 }
             }
 
@@ -582,7 +582,7 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_persist_kernel(const __grid
                 tmem_ld_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar.o_free);
+                mbar_arrive_if(bar.o_free, lane == 0);
                 const float l_row = l_half + xchg[2 * (it.n_t & 1) + (hf ^ 1)];
                 const int i = it.i0 + pi;
                 const float inv_l = 1.f / l_row;

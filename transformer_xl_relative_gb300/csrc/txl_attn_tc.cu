@@ -427,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             }
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar.q_ready);
+            mbar_arrive_if(bar.q_ready, lane == 0);
         }
         named_bar_sync(1, kSoftmaxThreads);    // all staging reads done before the ring reuses it
 
@@ -459,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                 bdc_bits = v0;
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar.bd_free);
+                mbar_arrive_if(bar.bd_free, lane == 0);
             }
             ++bd_uses;
         }
@@ -484,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                         tmem_ld_wait();
                         tc_fence_before();
                         __syncwarp();
-                        if (lane == 0) mbar_arrive(bar.bd_free);
+                        mbar_arrive_if(bar.bd_free, lane == 0);
                         const int cc = C - 128 * t - 64 * hf;   // first local column at the clamp
                         if (plan.clampc && cc < 64) {
 #pragma unroll
@@ -502,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                 if (kSeparateP) {                       // S buffer may now take S_{t+2}
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&bar.s_free[t & 1]);
+                    mbar_arrive_if(&bar.s_free[t & 1], lane == 0);
                 }
 #pragma unroll
                 for (int k = 0; k < 64; ++k) s[k] = __uint_as_float(su[k]);
@@ -587,7 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0 && ok) mbar_arrive(&bar.p_full[t & 1]);
+                mbar_arrive_if(&bar.p_full[t & 1], lane == 0 && ok);
             }
         }
 

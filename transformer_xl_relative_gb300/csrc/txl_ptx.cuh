@@ -37,10 +37,32 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar)
                  ::"r"(smem_u32(bar)) : "memory");
 }
 
+// Arrive from the lanes whose predicate is set, without a branch (no warp divergence).
+__device__ __forceinline__ void mbar_arrive_if(uint64_t* bar, bool pred)
+{
+    asm volatile("{\n\t.reg .pred p;\n\t.reg .b64 st;\n\tsetp.ne.b32 p, %1, 0;\n\t"
+                 "@p mbarrier.arrive.shared::cta.b64 st, [%0];\n\t}"
+                 ::"r"(smem_u32(bar)), "r"(static_cast<uint32_t>(pred)) : "memory");
+}
+
 __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes)
 {
     asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}"
                  ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+// Non-blocking test of a phase (about as cheap as a shared-memory load).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
 }
 
 // A thread that finds the phase incomplete may be suspended inside try_wait; the hint bounds that
@@ -101,17 +123,19 @@ static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parit
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtl& w,
                                           int where)
 {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_test_wait(bar, parity)) return true;
     return mbar_wait_slow(bar, parity, w, where);
 }
 
-// Warp-wide wait: lane 0 runs the bounded wait, the verdict is broadcast, and on success every
-// lane observes the completed phase itself (so each lane acquires what the phase publishes).
-// The phase cannot move on meanwhile: every caller's next phase needs this warp's own arrival.
+// Warp-wide wait.  Fast path: every lane tests the phase and the warp votes (no divergence).
+// Otherwise lane 0 runs the bounded wait, the verdict is broadcast, and on success every lane
+// observes the completed phase itself (so each lane acquires what the phase publishes).  The
+// phase cannot move on meanwhile: every caller's next phase needs this warp's own arrival.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const WaitCtl& w, int where)
 {
+    if (__all_sync(0xffffffffu, mbar_test_wait(bar, parity))) return true;
     bool ok = true;
-    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, w, where);
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait_slow(bar, parity, w, where);
     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     if (ok) (void)mbar_try_wait(bar, parity);
     __syncwarp();
