@@ -268,6 +268,13 @@ txl_status txl_rel_attn_fwd(int B, int L, int H, int D, int clamp_len, const txl
             if (!okq) return TXL_ERR_CUDA;
             const int sms = sm_count();
             if (sms <= 0) return TXL_ERR_CUDA;
+            const int64_t items = static_cast<int64_t>(p.n_qt) * H * B;
+            const int G = static_cast<int>(std::min<int64_t>(items, sms));
+            const int64_t per_cls = static_cast<int64_t>(H) * B;
+            p.sched_mode = (p.n_qt <= kMaxSchedClasses && per_cls <= INT32_MAX &&
+                            schedule_items(G, p.n_qt, static_cast<int>(per_cls), (M + 127 - p.lo) / 128 + 1,
+                                           p.sched_counts, kSchedCapacity))
+                               ? 1 : 0;
             return launch_attn_persist(p, sms, s) == cudaSuccess ? TXL_OK : TXL_ERR_CUDA;
         }
         if (B > 65535 || H > 65535) return TXL_ERR_UNSUPPORTED;

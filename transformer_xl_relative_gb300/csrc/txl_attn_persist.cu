@@ -57,7 +57,8 @@ struct PSmem {
     __device__ static constexpr int qu(int qb) { return Q + 2 * qb * kTile; }
     __device__ static constexpr int qv(int qb) { return Q + (2 * qb + 1) * kTile; }
     static constexpr int Misc = Bars + NumBars * 8;
-    static constexpr int Size = Misc + 16;
+    static constexpr int Sched = Misc + 16;             // int first[32], int count[32]
+    static constexpr int Size = Sched + 2 * kMaxSchedClasses * 4;
 };
 
 struct PBars {
@@ -88,17 +89,31 @@ struct Item {
     bool clampc;             // some distance of the item reaches clamp_len
 };
 
-// The n-th item of this CTA (false once the CTA has none left).  Items are numbered longest
-// first: all query tiles qt = n_qt - 1 (the most key tiles) of every (b, h), then qt = n_qt - 2, ...
-__device__ __forceinline__ bool item_at(const AttnTcParams& p, int n, Item& it)
+// The n-th item of this CTA (false once the CTA has none left), longest first.  With a count table
+// (sched_mode 1) the CTA takes count[qt] items of each query tile qt, items first[qt] .. of that
+// tile's (b, h) list (first/count: this CTA's row of the table and its prefix sums, in shared
+// memory).  Otherwise items are numbered longest first (every (b, h) of qt = n_qt - 1, then of
+// qt = n_qt - 2, ...) and dealt in serpentine rounds.
+__device__ __forceinline__ bool item_at(const AttnTcParams& p, const int* first, const int* count, int n, Item& it)
 {
-    const int G = gridDim.x, c = blockIdx.x;
-    const int64_t per_qt = static_cast<int64_t>(p.H) * p.B;
-    const int64_t idx = static_cast<int64_t>(n) * G + ((n & 1) ? (G - 1 - c) : c);
-    if (idx >= per_qt * p.n_qt) return false;
-    const int64_t g = idx / per_qt;
-    const int rem = static_cast<int>(idx - g * per_qt);
-    const int qt = p.n_qt - 1 - static_cast<int>(g);
+    int qt, rem;
+    if (p.sched_mode) {
+        qt = p.n_qt - 1;
+        while (qt >= 0 && n >= count[qt]) {
+            n -= count[qt];
+            --qt;
+        }
+        if (qt < 0) return false;
+        rem = first[qt] + n;
+    } else {
+        const int G = gridDim.x, c = blockIdx.x;
+        const int64_t per_qt = static_cast<int64_t>(p.H) * p.B;
+        const int64_t idx = static_cast<int64_t>(n) * G + ((n & 1) ? (G - 1 - c) : c);
+        if (idx >= per_qt * p.n_qt) return false;
+        const int64_t g = idx / per_qt;
+        rem = static_cast<int>(idx - g * per_qt);
+        qt = p.n_qt - 1 - static_cast<int>(g);
+    }
     it.h = rem % p.H;
     it.b = rem / p.H;
     it.i0 = qt * 128;
@@ -155,6 +170,15 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_persist_kernel(const __grid
         *abort_flag = 0;
         fence_mbar_init();
     }
+    int* sched_first = reinterpret_cast<int*>(smem + PSmem::Sched);
+    int* sched_count = sched_first + kMaxSchedClasses;
+    if (p.sched_mode && tid < p.n_qt) {                  // this CTA's row of the table, prefix sums
+        const int q = tid;
+        int f = 0;
+        for (int c = 0; c < static_cast<int>(blockIdx.x); ++c) f += p.sched_counts[c * p.n_qt + q];
+        sched_first[q] = f;
+        sched_count[q] = p.sched_counts[blockIdx.x * p.n_qt + q];
+    }
     if (warp == kPMmaWarp) tmem_alloc(tmem_holder, 512);
     tc_fence_before();
     __syncthreads();
@@ -185,7 +209,7 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_persist_kernel(const __grid
                 return true;
             };
             Item it;
-            for (int n = 0; ok && item_at(p, n, it); ++n) {
+            for (int n = 0; ok && item_at(p, sched_first, sched_count, n, it); ++n) {
                 // raw q rows in TMEM-lane order: even queries of the tile to rows 0-63, odd
                 // queries to rows 64-127 (the even and odd row maps both step two tokens per row)
                 const int qb = n & 1;
@@ -225,7 +249,7 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_persist_kernel(const __grid
         const int c = lane & 7;
         bool ok = true;
         Item it;
-        for (int n = 0; ok && item_at(p, n, it); ++n) {
+        for (int n = 0; ok && item_at(p, sched_first, sched_count, n, it); ++n) {
             const int qb = n & 1;
             float us[8], vs[8];
 #pragma unroll
@@ -313,7 +337,7 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_persist_kernel(const __grid
                 return true;
             };
             Item it;
-            for (int n = 0; ok && item_at(p, n, it); ++n) {
+            for (int n = 0; ok && item_at(p, sched_first, sched_count, n, it); ++n) {
                 const int qb = n & 1;
                 if (!(ok = mbar_wait(&bar.q_ready[qb], (n >> 1) & 1, wc, 20))) break;
                 tc_fence_after();
@@ -357,11 +381,11 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_persist_kernel(const __grid
                 if (++cu.t >= cu.it.n_t) {
                     ++cu.n;
                     cu.t = 0;
-                    cu.valid = item_at(p, cu.n, cu.it);
+                    cu.valid = item_at(p, sched_first, sched_count, cu.n, cu.it);
                 }
             };
             Cursor ld, cs;
-            ld.n = 0; ld.t = 0; ld.valid = item_at(p, 0, ld.it);
+            ld.n = 0; ld.t = 0; ld.valid = item_at(p, sched_first, sched_count, 0, ld.it);
             cs = ld;
             int vc = 0, T = 0;
             bool ok = true;
@@ -425,7 +449,7 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_persist_kernel(const __grid
         bool ok = true;
         int T = 0, bd = 0;                           // tiles and BD products consumed so far
         Item it;
-        for (int n = 0; item_at(p, n, it); ++n) {
+        for (int n = 0; item_at(p, sched_first, sched_count, n, it); ++n) {
             const int M = p.M;
             float m_run = -INFINITY, l_half = 0.f;
             uint32_t bdc_bits = 0;                  // fp32 bits of (q+v).r[clamp_len] for this row

@@ -12,6 +12,12 @@ namespace txl {
 
 constexpr int kMaxDModel = 4096;   // the bf16 path passes d_model/2 frequencies as parameters
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;   // 2 s: far above any healthy wait
+constexpr int kSchedCapacity = 4096;   // bytes of per-CTA item counts carried as kernel parameters
+constexpr int kMaxSchedClasses = 32;   // query tiles per sequence the count table can describe
+
+// Balanced static assignment of n_cls classes of per_cls interchangeable items (class q costs
+// len0 + q key tiles) to G CTAs: counts[c * n_cls + q].  False if it does not fit `capacity`.
+bool schedule_items(int G, int n_cls, int per_cls, int len0, uint8_t* counts, int capacity);
 
 // ---------------------------------------------------------------- relative position table
 struct PosGenF32Params {
@@ -67,6 +73,10 @@ struct AttnTcParams {
     int k_steps;                 // ceil(D / 16): UMMA K steps for the Q.K and Q.r products
     float qscale;                // scale * log2(e)
     int* err_flag;
+    // persistent kernel only: sched_counts[c * n_qt + qt] = items of query tile qt that CTA c
+    // processes (0 entries when sched_mode == 0: serpentine order instead)
+    int sched_mode;
+    uint8_t sched_counts[kSchedCapacity];
 };
 
 cudaError_t launch_attn_tc(const AttnTcParams& p, cudaStream_t s);
