@@ -361,7 +361,7 @@ def run_txl(args):
     peak, peak_sust, _, peak_kind = _peaks()
     value = aggregate_value(world, step_flops, t_step_ms)
     achieved = attn_flops / (t_attn_ms * 1e-3) / 1e12
-    kernel_src = os.path.join(ROOT, "transformer_xl_relative_gb300", "csrc", "txl_attn_tc.cu")
+    kernel_src = os.path.join(ROOT, "transformer_xl_relative_gb300", "csrc", "txl_attn_persist.cu")
     line = {
         "metric": "rel-attn TFLOP/s (L384 M384 H16 D64 bf16), whole step: pos-gen + fused attention + memory push",
         "value": value,
@@ -389,7 +389,7 @@ def run_txl(args):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": t_e2e_ms},
         "gpu_launches": 3 * steps,
-        "roofline": {"kernel": "txl_rel_attn_fwd (attn_tc_kernel<1>)", "bound": "tensor",
+        "roofline": {"kernel": "txl_rel_attn_fwd (attn_persist_kernel)", "bound": "tensor",
                      "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "peak_source": "%s bf16 burst (MEASURED_PEAKS.json)" % peak_kind
                      if peak_kind == "measured" else "fallback 1.9 PFLOP/s",

@@ -71,6 +71,14 @@ SHAPES = [
     (1, 2, 96, 192, 200, 128, 128, 1000, 0),       # two 64-column atoms
     (1, 2, 128, 256, 256, 256, 256, 1000, 0),      # D = 128
     (1, 1, 128, 128, 130, 300, 250, 200, 0),       # D = 128, partial memory, clamp
+    # one CTA per SM over all (b, h, query tile) items: odd L (the odd-row q map has fewer rows),
+    # tiny L, more items than SMs in odd counts, and more than 32 query tiles per sequence (items
+    # dealt in serpentine order instead of the balanced count table)
+    (1, 2, 64, 64, 129, 128, 128, 1000, 0),
+    (1, 1, 64, 64, 3, 5, 5, 1000, 0),
+    (3, 5, 64, 128, 257, 200, 180, 300, 0),
+    (13, 16, 64, 128, 256, 128, 128, 1000, 0),
+    (1, 1, 64, 64, 4160, 0, 0, 1000, 0),
 ]
 
 

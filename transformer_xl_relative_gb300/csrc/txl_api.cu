@@ -167,7 +167,7 @@ txl_status txl_rel_pos_gen(int n_rows, int d_model, int n_head, int d_head, cons
     }
     if (!a16(W_R) || !s16(ld_w, 2)) return TXL_ERR_ALIGNMENT;
     if (!encoder_ready()) return TXL_ERR_CUDA;
-    PosGenTcParams p;                  // carries the frequency table as kernel parameters
+    PosGenTcParams p;
     std::memset(&p, 0, sizeof(p));
     const int HD = n_head * d_head;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(HD), static_cast<cuuint64_t>(d_model)};
@@ -186,8 +186,7 @@ txl_status txl_rel_pos_gen(int n_rows, int d_model, int n_head, int d_head, cons
     p.D = d_head;
     p.n_ktiles = (d_model + 63) / 64;
     p.err_flag = nullptr;
-    for (int k = 0; k < d_model / 2; ++k)
-        p.inv_freq[k] = static_cast<float>(std::pow(10000.0, -(2.0 * k) / static_cast<double>(d_model)));
+    p.log2_freq_step = static_cast<float>(-2.0 * std::log2(10000.0) / static_cast<double>(d_model));
     return launch_pos_gen_tc(p, s) == cudaSuccess ? TXL_OK : TXL_ERR_CUDA;
 }
 

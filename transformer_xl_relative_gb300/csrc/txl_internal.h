@@ -10,7 +10,7 @@
 
 namespace txl {
 
-constexpr int kMaxDModel = 4096;   // the bf16 path passes d_model/2 frequencies as parameters
+constexpr int kMaxDModel = 4096;   // the bf16 path keeps d_model/2 frequencies in shared memory
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;   // 2 s: far above any healthy wait
 constexpr int kSchedCapacity = 4096;   // bytes of per-CTA item counts carried as kernel parameters
 constexpr int kMaxSchedClasses = 32;   // query tiles per sequence the count table can describe
@@ -34,7 +34,7 @@ struct PosGenTcParams {
     int n_rows, d_model, H, D;
     int n_ktiles;        // ceil(d_model / 64)
     int* err_flag;
-    float inv_freq[kMaxDModel / 2];   // 10000^(-2k/d_model), rounded from double on the host
+    float log2_freq_step;        // -2 log2(10000) / d_model: w_k = 2^(k * log2_freq_step)
 };
 
 cudaError_t launch_pos_gen_f32(const PosGenF32Params& p, cudaStream_t s);

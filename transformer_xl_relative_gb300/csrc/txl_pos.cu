@@ -110,7 +110,8 @@ __global__ void __launch_bounds__(kPosThreads, 1) pos_gen_tc_kernel(const __grid
         return;
     }
     const int half = p.d_model >> 1;
-    for (int k = tid; k < half; k += kPosThreads) freq[k] = p.inv_freq[k];
+    // w_k = 10000^(-2k/d_model) = 2^(k * log2_freq_step)
+    for (int k = tid; k < half; k += kPosThreads) freq[k] = exp2f(static_cast<float>(k) * p.log2_freq_step);
     if (tid == 0) {
         for (int s = 0; s < kPosStages; ++s) {
             mbar_init(&full_a[s], kPosGenWarps);
