@@ -203,6 +203,65 @@ def run_reference(args):
     return 0
 
 
+def bench_decode(txl, device, stream, rank, args):
+    """One new token per (b, h) over a long memory (txl_rel_attn_decode): B8 H16 D64 L1 M4096,
+    clamp 1000, bf16.  HBM-bound: reported as algorithmic bytes (K and V of every key, the r rows,
+    q and out) per call over the call time, against the measured HBM copy bandwidth.  Two input
+    sets of 134 MB alternate so no call reads L2-warm K/V."""
+    import torch
+    B, H, D, L, M, C, dm = 8, 16, 64, 1, 4096, 1000, 1024
+    dt = torch.bfloat16
+    g = torch.Generator(device=device).manual_seed(rank_seed(4242, rank))
+    n_rows = min(M + L, C + 1)
+    W = (torch.randn(dm, H * D, generator=g, device=device) * dm ** -0.5).to(dt)
+    r = torch.empty(n_rows, H, D, dtype=dt, device=device)
+    txl.rel_pos_gen(W, r, n_rows, dm, H, D)
+    u = (0.02 * torch.randn(H, D, generator=g, device=device)).float()
+    vb = (0.02 * torch.randn(H, D, generator=g, device=device)).float()
+    sets = []
+    for _ in range(2):
+        kv = torch.randn(2, B, M + L, H, D, generator=g, device=device).to(dt)
+        q = torch.randn(B, L, H, D, generator=g, device=device).to(dt)
+        mem = txl.Memory(kv[0, :, :M], kv[1, :, :M], 0, M)
+        sets.append((q, kv, mem, torch.empty(B, L, H, D, dtype=dt, device=device)))
+    ws = torch.empty(txl.rel_attn_decode_workspace_size(sets[0][0], sets[0][2]), dtype=torch.uint8,
+                     device=device)
+
+    def call(s_):
+        q, kv, mem, out = sets[s_]
+        txl.rel_attn_decode(q, mem, kv[0, :, M:], kv[1, :, M:], u, vb, r, n_rows, C, out, workspace=ws)
+
+    with torch.cuda.stream(stream):
+        for i in range(4):
+            call(i & 1)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        call(0)
+        call(1)
+    reps = 50
+    with torch.cuda.stream(stream):
+        graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    t_us = e0.elapsed_time(e1) * 1e3 / (2 * reps)
+    nbytes = (2 * B * H * (M + L) * D + H * n_rows * D + 2 * B * H * L * D) * 2
+    _, _, hbm, kind = _peaks()
+    gbs = nbytes / (t_us * 1e-6) / 1e9
+    return {"workload": "decode: B8 H16 D64 L1 M4096 clamp1000 bf16 (one new token per (b, h))",
+            "us_per_call": t_us, "tokens_per_s": B * L / (t_us * 1e-6),
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                         "frac": gbs / hbm, "peak_source": "%s HBM copy" % kind,
+                         "algorithmic_bytes_per_call": nbytes},
+            "gpu_launches_per_call": 2}
+
+
 def run_txl(args):
     import torch
 
@@ -356,6 +415,8 @@ def run_txl(args):
     h2d = sum(t.numel() * t.element_size() for t in (dq, dk, dv))
     d2h = ho.numel() * ho.element_size()
 
+    decode = bench_decode(txl, device, stream, rank, args)
+
     attn_flops, pos_flops = _flops(cfg)
     step_flops = attn_flops + pos_flops
     peak, peak_sust, _, peak_kind = _peaks()
@@ -389,6 +450,7 @@ def run_txl(args):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": t_e2e_ms},
         "gpu_launches": 3 * steps,
+        "decode": decode,
         "roofline": {"kernel": "txl_rel_attn_fwd (attn_persist_kernel)", "bound": "tensor",
                      "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "peak_source": "%s bf16 burst (MEASURED_PEAKS.json)" % peak_kind

@@ -142,6 +142,33 @@ int txl_rel_attn_path(int B, int L, int H, int D, const txl_view* q, const txl_m
                       int64_t ld_r, const txl_view* out, txl_dtype dtype);
 
 /*
+ * txl_rel_attn_decode -- the same attention as txl_rel_attn_fwd for a few queries (1 <= L <= 16)
+ * over a long memory: the incremental-generation case ("Transformer-XL架构解析" §3.2,
+ * "Transformer-XL 和相对位置编码" §2.2: each new token attends to the cached memory and itself).
+ * Arguments, layouts, masks, clamp and result are those of txl_rel_attn_fwd (f32 or bf16, any
+ * ring), except:
+ *   L         : 1 .. 16 queries per (b, h) (TXL_ERR_UNSUPPORTED above).
+ *   workspace : device scratch, 16-byte aligned, of at least
+ *               txl_rel_attn_decode_workspace_size(B, L, H, D, mem) bytes (TXL_ERR_WORKSPACE
+ *               otherwise).  It holds per-chunk partial results between the two kernels of the
+ *               call; its contents on entry do not matter and are overwritten.
+ * The keys of every (b, h) are split into chunks of 256 processed by separate CTAs on the CUDA
+ * cores (the work is bound by HBM bandwidth: about one flop per byte at L = 1), then the chunks
+ * are merged (split-K softmax).  Calls that share a workspace must not overlap on the GPU.
+ */
+txl_status txl_rel_attn_decode(int B, int L, int H, int D, int clamp_len,
+                               const txl_view* q, const txl_mem* mem,
+                               const txl_view* k_cur, const txl_view* v_cur,
+                               const float* u, const float* v_bias,
+                               const void* r, int64_t ld_r, int n_rows,
+                               float scale, const txl_view* out, txl_dtype dtype,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of device workspace txl_rel_attn_decode needs: B*H*L*ceil((M+L)/256)*(D+2)*4
+ * (0 when the shape is outside the decode path). */
+size_t txl_rel_attn_decode_workspace_size(int B, int L, int H, int D, const txl_mem* mem);
+
+/*
  * txl_mem_push -- append L positions to the FIFO memory ("Transformer-XL架构解析" §1.1;
  * "Transformer-XL 和相对位置编码" §2.3.1: the cached states of the previous segment).
  * Copies k_new/v_new [B][L][H][D] (device views) into slots (wp + t) mod M for

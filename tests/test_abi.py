@@ -121,6 +121,21 @@ def test_rejections_before_any_launch(native):
     mem = native.TxlMem(FAKE, FAKE, 64, 8, 8, 1, 8, 1, 8, 1, 3, 5)
     assert lib.txl_mem_push(ctypes.byref(mem), ctypes.byref(q), ctypes.byref(q), 0, None) == native.TXL_OK
     assert (mem.wp, mem.valid) == (3, 5)
+    # decode path: more than 16 queries, a missing or short workspace; the workspace formula
+    ws = lib.txl_rel_attn_decode_workspace_size(2, 3, 4, 64, None)
+    assert ws == 2 * 4 * 3 * 1 * (64 + 2) * 4
+    mem = native.TxlMem(FAKE, FAKE, 64, 8, 8, 2, 700, 4, 64, 1, 0, 700)
+    assert lib.txl_rel_attn_decode_workspace_size(2, 1, 4, 64, ctypes.byref(mem)) == 2 * 4 * 1 * 3 * 66 * 4
+    assert lib.txl_rel_attn_decode_workspace_size(1, 17, 1, 8, None) == 0
+    assert lib.txl_rel_attn_decode(1, 17, 1, 8, 16, ctypes.byref(q), None, ctypes.byref(q), ctypes.byref(q),
+                                   FAKE, FAKE, FAKE, 8, 32, 0.0, ctypes.byref(q), 1, FAKE, 1 << 20,
+                                   None) == native.TXL_ERR_UNSUPPORTED
+    assert lib.txl_rel_attn_decode(1, 4, 1, 8, 16, ctypes.byref(q), None, ctypes.byref(q), ctypes.byref(q),
+                                   FAKE, FAKE, FAKE, 8, 16, 0.0, ctypes.byref(q), 1, None, 0,
+                                   None) == native.TXL_ERR_WORKSPACE
+    assert lib.txl_rel_attn_decode(1, 4, 1, 8, 16, ctypes.byref(q), None, ctypes.byref(q), ctypes.byref(q),
+                                   FAKE, FAKE, FAKE, 8, 16, 0.0, ctypes.byref(q), 1, FAKE, 16,
+                                   None) == native.TXL_ERR_WORKSPACE
     # self-test limits
     assert lib.txl_selftest_wait_timeout(FAKE, 0, None) == native.TXL_ERR_INVALID_ARG
     assert lib.txl_selftest_wait_timeout(None, 10, None) == native.TXL_ERR_INVALID_ARG

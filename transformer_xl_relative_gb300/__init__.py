@@ -8,6 +8,8 @@ from . import native
 from .api import (  # noqa: F401
     Memory,
     mem_push,
+    rel_attn_decode,
+    rel_attn_decode_workspace_size,
     rel_attn_fwd,
     rel_attn_path,
     rel_pos_gen,

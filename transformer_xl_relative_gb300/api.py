@@ -134,6 +134,37 @@ def rel_attn_fwd(q: torch.Tensor, mem: Memory | None, k_cur: torch.Tensor, v_cur
     return out
 
 
+def rel_attn_decode_workspace_size(q: torch.Tensor, mem: Memory | None) -> int:
+    """Bytes of workspace rel_attn_decode needs (txl_rel_attn_decode_workspace_size)."""
+    B, L, H, D = q.shape
+    memc = ctypes.byref(mem.c_struct) if mem is not None else None
+    return int(_lib().txl_rel_attn_decode_workspace_size(B, L, H, D, memc))
+
+
+def rel_attn_decode(q: torch.Tensor, mem: Memory | None, k_cur: torch.Tensor, v_cur: torch.Tensor,
+                    u: torch.Tensor, v_bias: torch.Tensor, r: torch.Tensor, n_rows: int,
+                    clamp_len: int, out: torch.Tensor, scale: float = 0.0,
+                    workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Attention of 1..16 queries per (b, h) over a long memory, keys split across CTAs
+    (txl_rel_attn_decode).  Without `workspace`, a device buffer of the required size is taken
+    from torch's allocator for the call."""
+    (B, L, H, D), memc, vq, vk, vv, vo = _attn_args(q, mem, k_cur, v_cur, r, out)
+    if u.dtype != torch.float32 or v_bias.dtype != torch.float32:
+        raise TypeError("u and v_bias are fp32 [H, D]")
+    if not (u.is_contiguous() and v_bias.is_contiguous()):
+        raise ValueError("u and v_bias must be contiguous [H, D]")
+    need = rel_attn_decode_workspace_size(q, mem)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    nbytes = workspace.numel() * workspace.element_size()
+    st = _lib().txl_rel_attn_decode(
+        B, L, H, D, int(clamp_len), ctypes.byref(vq), memc, ctypes.byref(vk), ctypes.byref(vv),
+        u.data_ptr(), v_bias.data_ptr(), r.data_ptr(), r.stride(1), int(n_rows), float(scale),
+        ctypes.byref(vo), dtype_code(q), workspace.data_ptr(), nbytes, _stream(stream))
+    check(st, "txl_rel_attn_decode")
+    return out
+
+
 def rel_attn_path(q, mem, k_cur, v_cur, r, out) -> int:
     """1 = fused tcgen05 kernel, 2 = SIMT kernel (txl_rel_attn_path)."""
     (B, L, H, D), memc, vq, vk, vv, vo = _attn_args(q, mem, k_cur, v_cur, r, out)

@@ -1,0 +1,340 @@
+// txl_decode.cu -- relative attention for a few queries (L <= 16) over a long memory: split-K
+// ("flash decoding").  The incremental-generation case of "Transformer-XL架构解析" §3.2 and
+// "Transformer-XL 和相对位置编码" §2.2: each new token attends to the cached memory plus itself.
+//
+// Same arithmetic as the other attention paths ("跨窗口的相对位置编码" §3, terms (a)-(d); the clamp
+// of "TransformerXL 相对位置编码" §2.4; the causal-with-memory mask of §4.2/§4.3):
+//     s_ij = scale * [ (q_i+u).k_j + (q_i+v).r[min(M+i-j, C)] ],  out_i = softmax_j(s_ij) V
+// With a handful of queries per (b, h) there is almost no reuse of K and V: the work is bound by
+// HBM (about one flop per byte at L = 1), so it runs on the CUDA cores and spreads the keys of each
+// (b, h) over many CTAs.
+//
+// decode_partial_kernel: one CTA per (chunk of 256 keys, h, b), 256 threads.
+//   1. q+u and q+v in fp32 shared memory.
+//   2. The position term of the chunk as a band: the chunk's keys and the L queries touch the
+//      CK + L - 1 distances delta_top - rho (rho = 0 ..), delta_top = M + L - 1 - j0; thread rho
+//      reads r[min(delta, C)] once and forms e(i, rho) = (q_i+v).r for every query.  Query i and
+//      key j meet at rho = (L - 1 - i) + (j - j0): the relative shift is this index.
+//   3. One key per thread: (q_i+u).k_j + e(i, rho) for every query, masked (key before the valid
+//      memory, or in the future of the query) to -inf, in the log2 domain.
+//   4. Per query: the chunk's maximum m and sum l of 2^(s - m) (block reductions).
+//   5. O_i = sum_j 2^(s_ij - m_i) v_j: each warp takes 32 keys, lane = head dimension pairs; the
+//      eight warps' partial sums meet in shared memory.  (m, l, O) go to the workspace.
+// decode_combine_kernel: per (b, h, i), merges the chunks: M = max m_c, w_c = 2^(m_c - M),
+//   out = sum w_c O_c / sum w_c l_c.
+#include <cuda_bf16.h>
+
+#include "txl_internal.h"
+
+namespace txl {
+
+namespace {
+
+constexpr int kDecThreads = 256;
+constexpr int kDecWarps = kDecThreads / 32;
+
+template <typename T> __device__ __forceinline__ float to_f(T x);
+template <> __device__ __forceinline__ float to_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// Eight consecutive elements d0 .. d0+7 of a row as fp32; elements at or past D read as 0.
+// vec: the row start and d0 are 16-byte aligned and d0 + 8 <= D may use one or two vector loads.
+template <typename T>
+__device__ __forceinline__ void load8(const T* row, int d0, int D, bool vec, float* o)
+{
+    if (vec && d0 + 8 <= D) {
+        if constexpr (sizeof(T) == 2) {
+            const uint4 x = __ldg(reinterpret_cast<const uint4*>(row + d0));
+            const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                o[2 * e] = __uint_as_float(w[e] << 16);
+                o[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+            }
+        } else {
+            const float4 a = __ldg(reinterpret_cast<const float4*>(row + d0));
+            const float4 b = __ldg(reinterpret_cast<const float4*>(row + d0 + 4));
+            o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
+            o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[e] = d0 + e < D ? to_f(row[d0 + e]) : 0.f;
+    }
+}
+
+// Key/value row of logical key j (memory slot (wp + j) mod M, or current-segment row j - M).
+template <typename T>
+__device__ __forceinline__ const T* kv_row(const DecodeParams& p, int b, int h, int j, bool values)
+{
+    if (j < p.M) {
+        const int slot = static_cast<int>((static_cast<int64_t>(p.wp) + j) % p.M);
+        const T* base = static_cast<const T*>(values ? p.vmem : p.kmem);
+        return base + b * p.m_sb + static_cast<int64_t>(slot) * p.m_st + h * p.m_sh;
+    }
+    const int t = j - p.M;
+    if (values)
+        return static_cast<const T*>(p.vcur) + b * p.vc_sb + static_cast<int64_t>(t) * p.vc_st + h * p.vc_sh;
+    return static_cast<const T*>(p.kcur) + b * p.kc_sb + static_cast<int64_t>(t) * p.kc_st + h * p.kc_sh;
+}
+
+template <typename T, int LQ>
+__global__ void __launch_bounds__(kDecThreads) decode_partial_kernel(const __grid_constant__ DecodeParams p)
+{
+    extern __shared__ __align__(16) float dsm[];
+    const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int L = p.L, D = p.D, Dp = p.Dp;
+    const int K = p.M + L;
+    const int j0 = c * kDecodeChunk;
+    const int BW = kDecodeChunk + LQ;                         // band row pitch
+    float* qu = dsm;                                          // [LQ][Dp]
+    float* qv = qu + LQ * Dp;                                 // [LQ][Dp]
+    float* band = qv + LQ * Dp;                               // [LQ][BW]
+    float* sp = band + LQ * BW;                               // [LQ][kDecodeChunk]
+    float* red = sp + LQ * kDecodeChunk;                      // [2][kDecWarps][LQ]
+    float* obuf = red + 2 * kDecWarps * LQ;                   // [kDecWarps][LQ][Do]
+
+    // 1. q + u, q + v (fp32)
+    for (int x = tid; x < LQ * Dp; x += kDecThreads) {
+        const int i = x / Dp, d = x - i * Dp;
+        float qq = 0.f, uu = 0.f, vv = 0.f;
+        if (i < L && d < D) {
+            qq = to_f(static_cast<const T*>(p.q)[b * p.q_sb + static_cast<int64_t>(i) * p.q_st + h * p.q_sh + d]);
+            uu = __ldg(p.u + h * D + d);
+            vv = __ldg(p.vb + h * D + d);
+        }
+        qu[x] = (i < L && d < D) ? qq + uu : 0.f;
+        qv[x] = (i < L && d < D) ? qq + vv : 0.f;
+    }
+    __syncthreads();
+
+    // 2. position band e(i, rho) = (q_i + v) . r[min(delta_top - rho, C)]
+    const int delta_top = p.M + L - 1 - j0;
+    const int n_band = kDecodeChunk + L - 1;
+    for (int rho = tid; rho < n_band; rho += kDecThreads) {
+        const int delta = delta_top - rho;
+        float acc[LQ];
+#pragma unroll
+        for (int i = 0; i < LQ; ++i) acc[i] = 0.f;
+        if (delta >= 0) {
+            const int dc = delta < p.C ? delta : p.C;
+            const T* rrow = static_cast<const T*>(p.r) + static_cast<int64_t>(dc) * p.r_row + h * p.r_head;
+            for (int d0 = 0; d0 < D; d0 += 8) {
+                float r8[8];
+                load8(rrow, d0, D, p.vec_r, r8);
+#pragma unroll
+                for (int i = 0; i < LQ; ++i) {
+                    const float4 a = *reinterpret_cast<const float4*>(qv + i * Dp + d0);
+                    const float4 e = *reinterpret_cast<const float4*>(qv + i * Dp + d0 + 4);
+                    acc[i] = fmaf(a.x, r8[0], fmaf(a.y, r8[1], fmaf(a.z, r8[2], fmaf(a.w, r8[3], acc[i]))));
+                    acc[i] = fmaf(e.x, r8[4], fmaf(e.y, r8[5], fmaf(e.z, r8[6], fmaf(e.w, r8[7], acc[i]))));
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < LQ; ++i) band[i * BW + rho] = acc[i];
+    }
+    __syncthreads();
+
+    // 3. scores of key j = j0 + tid against every query (log2 domain), masked keys -inf
+    const int j = j0 + tid;
+    const bool live = j < K && j >= p.lo;
+    float s[LQ];
+    {
+        float acc[LQ];
+#pragma unroll
+        for (int i = 0; i < LQ; ++i) acc[i] = 0.f;
+        if (live) {
+            const T* krow = kv_row<T>(p, b, h, j, false);
+            for (int d0 = 0; d0 < D; d0 += 8) {
+                float k8[8];
+                load8(krow, d0, D, p.vec_kv, k8);
+#pragma unroll
+                for (int i = 0; i < LQ; ++i) {
+                    const float4 a = *reinterpret_cast<const float4*>(qu + i * Dp + d0);
+                    const float4 e = *reinterpret_cast<const float4*>(qu + i * Dp + d0 + 4);
+                    acc[i] = fmaf(a.x, k8[0], fmaf(a.y, k8[1], fmaf(a.z, k8[2], fmaf(a.w, k8[3], acc[i]))));
+                    acc[i] = fmaf(e.x, k8[4], fmaf(e.y, k8[5], fmaf(e.z, k8[6], fmaf(e.w, k8[7], acc[i]))));
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < LQ; ++i) {
+            const bool vis = live && i < L && j <= p.M + i;
+            s[i] = vis ? (acc[i] + band[i * BW + (L - 1 - i) + tid]) * p.qscale : -INFINITY;
+        }
+    }
+
+    // 4. per query: chunk maximum, probabilities, chunk sum
+    float m[LQ];
+#pragma unroll
+    for (int i = 0; i < LQ; ++i) {
+        float x = s[i];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, off));
+        if (lane == 0) red[warp * LQ + i] = x;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < LQ; ++i) {
+        float x = red[i];
+#pragma unroll
+        for (int w = 1; w < kDecWarps; ++w) x = fmaxf(x, red[w * LQ + i]);
+        m[i] = x;
+        const float pv = x == -INFINITY ? 0.f : exp2f(s[i] - x);
+        sp[i * kDecodeChunk + tid] = pv;
+        float y = pv;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) y += __shfl_xor_sync(0xffffffffu, y, off);
+        if (lane == 0) red[(kDecWarps + warp) * LQ + i] = y;
+    }
+    __syncthreads();
+
+    // 5. O_i over this warp's 32 keys; lane owns dims 2 lane + 64 g, 2 lane + 1 + 64 g
+    constexpr int kG = 2;                                     // D <= 128
+    float o[LQ][2 * kG];
+#pragma unroll
+    for (int i = 0; i < LQ; ++i)
+#pragma unroll
+        for (int e = 0; e < 2 * kG; ++e) o[i][e] = 0.f;
+    const int kb = 32 * warp;
+#pragma unroll 4
+    for (int kk = 0; kk < 32; ++kk) {
+        const int t = kb + kk;
+        const int jj = j0 + t;
+        if (jj >= K || jj < p.lo) continue;                   // uniform across the warp
+        const T* vrow = kv_row<T>(p, b, h, jj, true);
+        float vx[2 * kG];
+#pragma unroll
+        for (int g = 0; g < kG; ++g) {
+            const int d = 2 * lane + 64 * g;
+            if (p.vec_kv && d + 1 < D) {
+                if constexpr (sizeof(T) == 2) {
+                    const uint32_t w = __ldg(reinterpret_cast<const unsigned int*>(vrow + d));
+                    vx[2 * g] = __uint_as_float(w << 16);
+                    vx[2 * g + 1] = __uint_as_float(w & 0xffff0000u);
+                } else {
+                    const float2 w = __ldg(reinterpret_cast<const float2*>(vrow + d));
+                    vx[2 * g] = w.x;
+                    vx[2 * g + 1] = w.y;
+                }
+            } else {
+                vx[2 * g] = d < D ? to_f(vrow[d]) : 0.f;
+                vx[2 * g + 1] = d + 1 < D ? to_f(vrow[d + 1]) : 0.f;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < LQ; ++i) {
+            const float pij = sp[i * kDecodeChunk + t];
+#pragma unroll
+            for (int e = 0; e < 2 * kG; ++e) o[i][e] = fmaf(pij, vx[e], o[i][e]);
+        }
+    }
+    constexpr int Do = 64 * kG;
+#pragma unroll
+    for (int i = 0; i < LQ; ++i)
+#pragma unroll
+        for (int g = 0; g < kG; ++g) {
+            obuf[(warp * LQ + i) * Do + 2 * lane + 64 * g] = o[i][2 * g];
+            obuf[(warp * LQ + i) * Do + 2 * lane + 1 + 64 * g] = o[i][2 * g + 1];
+        }
+    __syncthreads();
+
+    // partial (m, l, O) of every query of this chunk
+    const int Dw = D + 2;
+    for (int x = tid; x < L * Dw; x += kDecThreads) {
+        const int i = x / Dw, e = x - i * Dw;
+        float val;
+        if (e == 0) {
+            val = red[i];
+#pragma unroll
+            for (int w = 1; w < kDecWarps; ++w) val = fmaxf(val, red[w * LQ + i]);
+        } else if (e == 1) {
+            val = 0.f;
+#pragma unroll
+            for (int w = 0; w < kDecWarps; ++w) val += red[(kDecWarps + w) * LQ + i];
+        } else {
+            val = 0.f;
+#pragma unroll
+            for (int w = 0; w < kDecWarps; ++w) val += obuf[(w * LQ + i) * Do + (e - 2)];
+        }
+        p.part[((static_cast<int64_t>(b) * p.H + h) * L + i) * p.n_chunks * Dw + static_cast<int64_t>(c) * Dw + e] = val;
+    }
+    (void)m;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_constant__ DecodeParams p)
+{
+    const int bhi = blockIdx.x;                               // (b * H + h) * L + i
+    const int i = bhi % p.L;
+    const int bh = bhi / p.L;
+    const int h = bh % p.H, b = bh / p.H;
+    const int Dw = p.D + 2;
+    const float* part = p.part + static_cast<int64_t>(bhi) * p.n_chunks * Dw;
+    float mx = -INFINITY;
+    for (int c = 0; c < p.n_chunks; ++c) mx = fmaxf(mx, part[c * Dw]);
+    for (int d = threadIdx.x; d < p.D; d += blockDim.x) {
+        float num = 0.f, den = 0.f;
+        for (int c = 0; c < p.n_chunks; ++c) {
+            const float mc = part[c * Dw];
+            if (mc == -INFINITY) continue;
+            const float w = exp2f(mc - mx);
+            den = fmaf(w, part[c * Dw + 1], den);
+            num = fmaf(w, part[c * Dw + 2 + d], num);
+        }
+        T* o = static_cast<T*>(p.out) + b * p.o_sb + static_cast<int64_t>(i) * p.o_st + h * p.o_sh + d;
+        const float val = num / den;
+        if constexpr (sizeof(T) == 2) *o = __float2bfloat16_rn(val);
+        else *o = val;
+    }
+}
+
+template <typename T, int LQ>
+cudaError_t launch_lq(const DecodeParams& p, cudaStream_t s)
+{
+    const size_t smem = decode_smem_bytes(LQ, p.Dp);
+    static bool attr_done = false;
+    if (!attr_done) {
+        cudaError_t e = cudaFuncSetAttribute(decode_partial_kernel<T, LQ>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(decode_smem_bytes(LQ, 128)));
+        if (e != cudaSuccess) return e;
+        attr_done = true;
+    }
+    dim3 grid(p.n_chunks, p.H, p.B);
+    decode_partial_kernel<T, LQ><<<grid, kDecThreads, smem, s>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    decode_combine_kernel<T><<<p.B * p.H * p.L, 128, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_t(const DecodeParams& p, cudaStream_t s)
+{
+    if (p.L <= 1) return launch_lq<T, 1>(p, s);
+    if (p.L <= 2) return launch_lq<T, 2>(p, s);
+    if (p.L <= 4) return launch_lq<T, 4>(p, s);
+    if (p.L <= 8) return launch_lq<T, 8>(p, s);
+    return launch_lq<T, 16>(p, s);
+}
+
+}  // namespace
+
+size_t decode_smem_bytes(int lq, int Dp)
+{
+    const size_t floats = 2ull * lq * Dp + static_cast<size_t>(lq) * (kDecodeChunk + lq) +
+                          static_cast<size_t>(lq) * kDecodeChunk + 2ull * kDecWarps * lq +
+                          static_cast<size_t>(kDecWarps) * lq * 128;
+    return floats * sizeof(float);
+}
+
+cudaError_t launch_decode(const DecodeParams& p, txl_dtype dtype, cudaStream_t s)
+{
+    if (p.B == 0 || p.L == 0) return cudaSuccess;
+    return dtype == TXL_F32 ? launch_t<float>(p, s) : launch_t<__nv_bfloat16>(p, s);
+}
+
+}  // namespace txl

@@ -83,6 +83,28 @@ cudaError_t launch_attn_tc(const AttnTcParams& p, cudaStream_t s);
 // d_head <= 64: one persistent CTA per SM (at most sm_count CTAs) over all query tiles
 cudaError_t launch_attn_persist(const AttnTcParams& p, int sm_count, cudaStream_t s);
 
+// ---------------------------------------------------------------- decode (few queries, split keys)
+constexpr int kDecodeChunk = 256;   // keys per CTA
+constexpr int kDecodeMaxL = 16;     // queries per (b, h) the decode path takes
+
+struct DecodeParams {
+    const void* q; int64_t q_sb, q_st, q_sh;
+    const void* kmem; const void* vmem; int64_t m_sb, m_st, m_sh;
+    const void* kcur; int64_t kc_sb, kc_st, kc_sh;
+    const void* vcur; int64_t vc_sb, vc_st, vc_sh;
+    void* out; int64_t o_sb, o_st, o_sh;
+    const float* u; const float* vb;
+    const void* r; int64_t r_row, r_head;       // element strides of the r table
+    int B, L, H, D, Dp, M, lo, wp, C;           // Dp: D rounded up to 8
+    float qscale;                               // scale * log2(e)
+    int n_chunks;                               // ceil((M + L) / kDecodeChunk)
+    float* part;                                // [B][H][L][n_chunks][D + 2]: (m, l, O[D])
+    int vec_kv, vec_r;                          // rows 16-byte aligned: vector loads allowed
+};
+
+size_t decode_smem_bytes(int lq, int Dp);
+cudaError_t launch_decode(const DecodeParams& p, txl_dtype dtype, cudaStream_t s);
+
 // ---------------------------------------------------------------- memory ring
 struct MemPushParams {
     const void* k_new; const void* v_new;

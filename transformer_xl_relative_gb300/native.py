@@ -17,7 +17,8 @@ TXL_F32, TXL_BF16 = 0, 1
 # every function include/txl.h declares
 EXPORTS = (
     "txl_status_str", "txl_version", "txl_rel_pos_gen", "txl_rel_attn_fwd",
-    "txl_rel_attn_workspace_size", "txl_rel_attn_path", "txl_mem_push", "txl_selftest_wait_timeout",
+    "txl_rel_attn_workspace_size", "txl_rel_attn_path", "txl_rel_attn_decode",
+    "txl_rel_attn_decode_workspace_size", "txl_mem_push", "txl_selftest_wait_timeout",
 )
 
 
@@ -68,6 +69,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.txl_rel_attn_workspace_size.restype = ctypes.c_size_t
     lib.txl_rel_attn_path.argtypes = [i, i, i, i, V, Mp, V, V, vp, i64, V, i]
     lib.txl_rel_attn_path.restype = i
+    lib.txl_rel_attn_decode.argtypes = [i, i, i, i, i, V, Mp, V, V, vp, vp, vp, i64, i, fp, V, i,
+                                        vp, ctypes.c_size_t, vp]
+    lib.txl_rel_attn_decode.restype = i
+    lib.txl_rel_attn_decode_workspace_size.argtypes = [i, i, i, i, Mp]
+    lib.txl_rel_attn_decode_workspace_size.restype = ctypes.c_size_t
     lib.txl_mem_push.argtypes = [Mp, V, V, i, vp]
     lib.txl_mem_push.restype = i
     lib.txl_selftest_wait_timeout.argtypes = [vp, ctypes.c_uint, vp]
