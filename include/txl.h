@@ -169,6 +169,34 @@ txl_status txl_rel_attn_decode(int B, int L, int H, int D, int clamp_len,
 size_t txl_rel_attn_decode_workspace_size(int B, int L, int H, int D, const txl_mem* mem);
 
 /*
+ * txl_rel_attn_decode_noalloc -- txl_rel_attn_decode without a caller workspace, for callers that
+ * cannot obtain device memory at call time.  The pages have no counterpart to this entry point: it
+ * is a service of this library.  Examples of such callers: a serving process whose device memory
+ * is owned by a pre-sized arena that forbids allocations once it runs; a plugin reached through an
+ * interface that passes only inputs and outputs; a per-token generation loop that cannot afford
+ * cudaMalloc, which may synchronise the device.  Nothing here allocates: no cudaMalloc, cudaFree
+ * or allocating library routine is called.
+ * Arguments, layouts and results are those of txl_rel_attn_decode minus the workspace.  The
+ * per-chunk partial results live instead in a fixed 8 MiB scratch array inside the library, which
+ * every GPU that loads the library holds until the process exits:
+ *   - B*H*L*ceil((M+L)/256)*(D+2)*4 must not exceed 8388608 bytes (TXL_ERR_WORKSPACE otherwise;
+ *     use txl_rel_attn_decode with a workspace for such shapes);
+ *   - the first call on a device looks up the array's device address (cudaGetSymbolAddress, with
+ *     that device current) and caches it; make that first call before any stream capture;
+ *   - every call shares the array.  Each call writes every partial it reads, so nothing has to
+ *     start at zero, but calls that overlap on the GPU (two streams, or two host threads on
+ *     different streams) race on it and their results are undefined: keep them ordered, for
+ *     instance on one stream.
+ */
+txl_status txl_rel_attn_decode_noalloc(int B, int L, int H, int D, int clamp_len,
+                                       const txl_view* q, const txl_mem* mem,
+                                       const txl_view* k_cur, const txl_view* v_cur,
+                                       const float* u, const float* v_bias,
+                                       const void* r, int64_t ld_r, int n_rows,
+                                       float scale, const txl_view* out, txl_dtype dtype,
+                                       void* stream);
+
+/*
  * txl_mem_push -- append L positions to the FIFO memory ("Transformer-XL架构解析" §1.1;
  * "Transformer-XL 和相对位置编码" §2.3.1: the cached states of the previous segment).
  * Copies k_new/v_new [B][L][H][D] (device views) into slots (wp + t) mod M for

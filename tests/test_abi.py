@@ -136,6 +136,12 @@ def test_rejections_before_any_launch(native):
     assert lib.txl_rel_attn_decode(1, 4, 1, 8, 16, ctypes.byref(q), None, ctypes.byref(q), ctypes.byref(q),
                                    FAKE, FAKE, FAKE, 8, 16, 0.0, ctypes.byref(q), 1, FAKE, 16,
                                    None) == native.TXL_ERR_WORKSPACE
+    # the entry point without a workspace refuses partial results beyond its 8 MiB scratch
+    # (B*H*L*ceil((M+L)/256)*(D+2)*4 = 64*16*16*17*66*4 bytes here) before touching the GPU
+    mem = native.TxlMem(FAKE, FAKE, 64, 8, 8, 64, 4096, 16, 64, 1, 0, 4096)
+    assert lib.txl_rel_attn_decode_noalloc(64, 16, 16, 64, 1000, ctypes.byref(q), ctypes.byref(mem),
+                                           ctypes.byref(q), ctypes.byref(q), FAKE, FAKE, FAKE, 64, 4112,
+                                           0.0, ctypes.byref(q), 1, None) == native.TXL_ERR_WORKSPACE
     # self-test limits
     assert lib.txl_selftest_wait_timeout(FAKE, 0, None) == native.TXL_ERR_INVALID_ARG
     assert lib.txl_selftest_wait_timeout(None, 10, None) == native.TXL_ERR_INVALID_ARG

@@ -352,6 +352,58 @@ txl_status txl_rel_attn_decode(int B, int L, int H, int D, int clamp_len, const 
     return launch_decode(p, dtype, static_cast<cudaStream_t>(stream)) == cudaSuccess ? TXL_OK : TXL_ERR_CUDA;
 }
 
+txl_status txl_rel_attn_decode_noalloc(int B, int L, int H, int D, int clamp_len, const txl_view* q,
+                                       const txl_mem* mem, const txl_view* k_cur, const txl_view* v_cur,
+                                       const float* u, const float* v_bias, const void* r, int64_t ld_r,
+                                       int n_rows, float scale, const txl_view* out, txl_dtype dtype,
+                                       void* stream)
+{
+    txl_status st = check_attn(B, L, H, D, q, mem, k_cur, v_cur, r, ld_r, out, dtype);
+    if (st != TXL_OK) return st;
+    if (L > kDecodeMaxL) return TXL_ERR_UNSUPPORTED;
+    if (clamp_len < 0 || !u || !v_bias) return TXL_ERR_INVALID_ARG;
+    const int M = (mem && mem->M > 0) ? mem->M : 0;
+    const int valid = M > 0 ? mem->valid : 0;
+    const int wp = M > 0 ? mem->wp : 0;
+    if (n_rows < std::min(M + L, clamp_len + 1)) return TXL_ERR_INVALID_ARG;
+    if (B == 0 || L == 0) return TXL_OK;
+    // the partial results must fit the library's static scratch
+    const int64_t n_chunks = (static_cast<int64_t>(M) + L + kDecodeChunk - 1) / kDecodeChunk;
+    const double need = static_cast<double>(B) * H * L * n_chunks * (D + 2) * sizeof(float);
+    if (need > static_cast<double>(kDecodeStaticScratchBytes)) return TXL_ERR_WORKSPACE;
+    if (B > 65535 || H > 65535) return TXL_ERR_UNSUPPORTED;
+    float* scratch = nullptr;
+    if (decode_static_scratch(&scratch) != cudaSuccess || !scratch) return TXL_ERR_CUDA;
+    if (scale <= 0.f) scale = 1.0f / std::sqrt(static_cast<float>(D));
+    const int elem = dtype == TXL_F32 ? 4 : 2;
+    auto rows16 = [&](const void* ptr, int64_t sb, int64_t st_, int64_t sh) {
+        return a16(ptr) && s16(sb, elem) && s16(st_, elem) && s16(sh, elem);
+    };
+    DecodeParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.q = q->ptr; p.q_sb = q->stride_b; p.q_st = q->stride_t; p.q_sh = q->stride_h;
+    if (M > 0) {
+        p.kmem = mem->k; p.vmem = mem->v;
+        p.m_sb = mem->stride_b; p.m_st = mem->stride_t; p.m_sh = mem->stride_h;
+    }
+    p.kcur = k_cur->ptr; p.kc_sb = k_cur->stride_b; p.kc_st = k_cur->stride_t; p.kc_sh = k_cur->stride_h;
+    p.vcur = v_cur->ptr; p.vc_sb = v_cur->stride_b; p.vc_st = v_cur->stride_t; p.vc_sh = v_cur->stride_h;
+    p.out = out->ptr; p.o_sb = out->stride_b; p.o_st = out->stride_t; p.o_sh = out->stride_h;
+    p.u = u; p.vb = v_bias;
+    p.r = r; p.r_row = static_cast<int64_t>(H) * ld_r; p.r_head = ld_r;
+    p.B = B; p.L = L; p.H = H; p.D = D; p.Dp = (D + 7) / 8 * 8; p.M = M; p.lo = M - valid; p.wp = wp;
+    p.C = clamp_len;
+    p.qscale = scale * 1.4426950408889634f;
+    p.n_chunks = static_cast<int>(n_chunks);
+    p.part = scratch;
+    p.vec_kv = rows16(k_cur->ptr, k_cur->stride_b, k_cur->stride_t, k_cur->stride_h) &&
+               rows16(v_cur->ptr, v_cur->stride_b, v_cur->stride_t, v_cur->stride_h) &&
+               (M == 0 || (rows16(mem->k, mem->stride_b, mem->stride_t, mem->stride_h) &&
+                           rows16(mem->v, mem->stride_b, mem->stride_t, mem->stride_h)));
+    p.vec_r = a16(r) && s16(ld_r, elem);
+    return launch_decode(p, dtype, static_cast<cudaStream_t>(stream)) == cudaSuccess ? TXL_OK : TXL_ERR_CUDA;
+}
+
 txl_status txl_mem_push(txl_mem* mem, const txl_view* k_new, const txl_view* v_new, int L, void* stream)
 {
     if (!mem || !view_ok(k_new) || !view_ok(v_new) || L < 0) return TXL_ERR_INVALID_ARG;

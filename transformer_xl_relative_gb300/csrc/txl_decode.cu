@@ -22,6 +22,8 @@
 //      eight warps' partial sums meet in shared memory.  (m, l, O) go to the workspace.
 // decode_combine_kernel: per (b, h, i), merges the chunks: M = max m_c, w_c = 2^(m_c - M),
 //   out = sum w_c O_c / sum w_c l_c.
+#include <mutex>
+
 #include <cuda_bf16.h>
 
 #include "txl_internal.h"
@@ -321,7 +323,35 @@ cudaError_t launch_t(const DecodeParams& p, cudaStream_t s)
     return launch_lq<T, 16>(p, s);
 }
 
+// Scratch of the variant of the decode path that allocates nothing (txl_rel_attn_decode_noalloc):
+// every GPU that loads the library holds these kDecodeStaticScratchBytes until the process exits.
+// All calls share it; the partial kernel writes every entry the merge reads, so nothing in it has
+// to start at zero, but two calls that overlap on the GPU overwrite each other's partials.
+static __device__ __align__(256) float g_decode_scratch[kDecodeStaticScratchBytes / sizeof(float)];
+
 }  // namespace
+
+// Device address of the static scratch on the current device.  In host code the array's name is
+// only a host-side stand-in, so the address is looked up with cudaGetSymbolAddress, once per
+// device with that device current (the first call on a device does it), and cached.
+cudaError_t decode_static_scratch(float** out)
+{
+    static std::mutex mu;
+    static float* addr[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void* ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_decode_scratch);
+        if (e != cudaSuccess) return e;
+        addr[dev] = static_cast<float*>(ptr);
+    }
+    *out = addr[dev];
+    return cudaSuccess;
+}
 
 size_t decode_smem_bytes(int lq, int Dp)
 {

@@ -105,6 +105,11 @@ struct DecodeParams {
 size_t decode_smem_bytes(int lq, int Dp);
 cudaError_t launch_decode(const DecodeParams& p, txl_dtype dtype, cudaStream_t s);
 
+// Static per-device scratch of txl_rel_attn_decode_noalloc (8 MiB) and its device address.
+constexpr size_t kDecodeStaticScratchBytes = 8u << 20;
+constexpr int kMaxDevices = 64;
+cudaError_t decode_static_scratch(float** out);
+
 // ---------------------------------------------------------------- memory ring
 struct MemPushParams {
     const void* k_new; const void* v_new;

@@ -18,7 +18,8 @@ TXL_F32, TXL_BF16 = 0, 1
 EXPORTS = (
     "txl_status_str", "txl_version", "txl_rel_pos_gen", "txl_rel_attn_fwd",
     "txl_rel_attn_workspace_size", "txl_rel_attn_path", "txl_rel_attn_decode",
-    "txl_rel_attn_decode_workspace_size", "txl_mem_push", "txl_selftest_wait_timeout",
+    "txl_rel_attn_decode_workspace_size", "txl_rel_attn_decode_noalloc", "txl_mem_push",
+    "txl_selftest_wait_timeout",
 )
 
 
@@ -74,6 +75,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.txl_rel_attn_decode.restype = i
     lib.txl_rel_attn_decode_workspace_size.argtypes = [i, i, i, i, Mp]
     lib.txl_rel_attn_decode_workspace_size.restype = ctypes.c_size_t
+    lib.txl_rel_attn_decode_noalloc.argtypes = [i, i, i, i, i, V, Mp, V, V, vp, vp, vp, i64, i, fp, V,
+                                                i, vp]
+    lib.txl_rel_attn_decode_noalloc.restype = i
     lib.txl_mem_push.argtypes = [Mp, V, V, i, vp]
     lib.txl_mem_push.restype = i
     lib.txl_selftest_wait_timeout.argtypes = [vp, ctypes.c_uint, vp]
