@@ -205,9 +205,10 @@ def run_reference(args):
 
 def bench_decode(txl, device, stream, rank, args):
     """One new token per (b, h) over a long memory (txl_rel_attn_decode): B8 H16 D64 L1 M4096,
-    clamp 1000, bf16.  HBM-bound: reported as algorithmic bytes (K and V of every key, the r rows,
-    q and out) per call over the call time, against the measured HBM copy bandwidth.  Two input
-    sets of 134 MB alternate so no call reads L2-warm K/V."""
+    clamp 1000, bf16, the K/V cache head-major ([B][H][T][D]: each (b, h) stream contiguous).
+    HBM-bound: reported as algorithmic bytes (K and V of every key, the r rows, q and out) per
+    call over the call time, against the measured HBM copy bandwidth.  Two input sets of 134 MB
+    alternate so no call reads L2-warm K/V."""
     import torch
     B, H, D, L, M, C, dm = 8, 16, 64, 1, 4096, 1000, 1024
     dt = torch.bfloat16
@@ -220,7 +221,8 @@ def bench_decode(txl, device, stream, rank, args):
     vb = (0.02 * torch.randn(H, D, generator=g, device=device)).float()
     sets = []
     for _ in range(2):
-        kv = torch.randn(2, B, M + L, H, D, generator=g, device=device).to(dt)
+        # head-major cache [B][H][M + L][D] (each (b, h) key stream contiguous), viewed [B][T][H][D]
+        kv = torch.randn(2, B, H, M + L, D, generator=g, device=device).to(dt).permute(0, 1, 3, 2, 4)
         q = torch.randn(B, L, H, D, generator=g, device=device).to(dt)
         mem = txl.Memory(kv[0, :, :M], kv[1, :, :M], 0, M)
         sets.append((q, kv, mem, torch.empty(B, L, H, D, dtype=dt, device=device)))
@@ -254,7 +256,7 @@ def bench_decode(txl, device, stream, rank, args):
     nbytes = (2 * B * H * (M + L) * D + H * n_rows * D + 2 * B * H * L * D) * 2
     _, _, hbm, kind = _peaks()
     gbs = nbytes / (t_us * 1e-6) / 1e9
-    return {"workload": "decode: B8 H16 D64 L1 M4096 clamp1000 bf16 (one new token per (b, h))",
+    return {"workload": "decode: B8 H16 D64 L1 M4096 clamp1000 bf16, head-major K/V cache (one new token per (b, h))",
             "us_per_call": t_us, "tokens_per_s": B * L / (t_us * 1e-6),
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
                          "frac": gbs / hbm, "peak_source": "%s HBM copy" % kind,

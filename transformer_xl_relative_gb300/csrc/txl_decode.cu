@@ -70,7 +70,7 @@ template <typename T>
 __device__ __forceinline__ const T* kv_row(const DecodeParams& p, int b, int h, int j, bool values)
 {
     if (j < p.M) {
-        const int slot = static_cast<int>((static_cast<int64_t>(p.wp) + j) % p.M);
+        const int slot = p.wp + j >= p.M ? p.wp + j - p.M : p.wp + j;   // wp < M and j < M
         const T* base = static_cast<const T*>(values ? p.vmem : p.kmem);
         return base + b * p.m_sb + static_cast<int64_t>(slot) * p.m_st + h * p.m_sh;
     }
@@ -111,18 +111,24 @@ __global__ void __launch_bounds__(kDecThreads) decode_partial_kernel(const __gri
     }
     __syncthreads();
 
+    // Rows are read cooperatively: the eight lanes of group rg = lane / 8 read one row together,
+    // lane part = lane mod 8 taking the 16-byte pieces part, part + 8, ... (four whole rows per
+    // warp instruction), and their partial dot products meet in three shuffles.
+    const int rg = lane >> 3, part = lane & 7;
+
     // 2. position band e(i, rho) = (q_i + v) . r[min(delta_top - rho, C)]
     const int delta_top = p.M + L - 1 - j0;
     const int n_band = kDecodeChunk + L - 1;
-    for (int rho = tid; rho < n_band; rho += kDecThreads) {
+    for (int rho0 = 4 * warp; rho0 < n_band; rho0 += 4 * kDecWarps) {
+        const int rho = rho0 + rg;
         const int delta = delta_top - rho;
         float acc[LQ];
 #pragma unroll
         for (int i = 0; i < LQ; ++i) acc[i] = 0.f;
-        if (delta >= 0) {
+        if (rho < n_band && delta >= 0) {
             const int dc = delta < p.C ? delta : p.C;
             const T* rrow = static_cast<const T*>(p.r) + static_cast<int64_t>(dc) * p.r_row + h * p.r_head;
-            for (int d0 = 0; d0 < D; d0 += 8) {
+            for (int d0 = 8 * part; d0 < D; d0 += 64) {
                 float r8[8];
                 load8(rrow, d0, D, p.vec_r, r8);
 #pragma unroll
@@ -135,21 +141,28 @@ __global__ void __launch_bounds__(kDecThreads) decode_partial_kernel(const __gri
             }
         }
 #pragma unroll
-        for (int i = 0; i < LQ; ++i) band[i * BW + rho] = acc[i];
+        for (int i = 0; i < LQ; ++i) {
+            float x = acc[i];
+            x += __shfl_xor_sync(0xffffffffu, x, 1);
+            x += __shfl_xor_sync(0xffffffffu, x, 2);
+            x += __shfl_xor_sync(0xffffffffu, x, 4);
+            if (part == 0 && rho < n_band) band[i * BW + rho] = x;
+        }
     }
     __syncthreads();
 
-    // 3. scores of key j = j0 + tid against every query (log2 domain), masked keys -inf
-    const int j = j0 + tid;
-    const bool live = j < K && j >= p.lo;
-    float s[LQ];
-    {
+    // 3. scores of every key of the chunk against every query (log2 domain), masked keys -inf:
+    //    key t = t0 + rg of this warp's 32 in groups of four, into sp[i][t]
+    for (int t0 = 32 * warp; t0 < 32 * warp + 32; t0 += 4) {
+        const int t = t0 + rg;
+        const int jj = j0 + t;
+        const bool live = jj < K && jj >= p.lo;
         float acc[LQ];
 #pragma unroll
         for (int i = 0; i < LQ; ++i) acc[i] = 0.f;
         if (live) {
-            const T* krow = kv_row<T>(p, b, h, j, false);
-            for (int d0 = 0; d0 < D; d0 += 8) {
+            const T* krow = kv_row<T>(p, b, h, jj, false);
+            for (int d0 = 8 * part; d0 < D; d0 += 64) {
                 float k8[8];
                 load8(krow, d0, D, p.vec_kv, k8);
 #pragma unroll
@@ -163,10 +176,18 @@ __global__ void __launch_bounds__(kDecThreads) decode_partial_kernel(const __gri
         }
 #pragma unroll
         for (int i = 0; i < LQ; ++i) {
-            const bool vis = live && i < L && j <= p.M + i;
-            s[i] = vis ? (acc[i] + band[i * BW + (L - 1 - i) + tid]) * p.qscale : -INFINITY;
+            float x = acc[i];
+            x += __shfl_xor_sync(0xffffffffu, x, 1);
+            x += __shfl_xor_sync(0xffffffffu, x, 2);
+            x += __shfl_xor_sync(0xffffffffu, x, 4);
+            const bool vis = live && i < L && jj <= p.M + i;
+            if (part == 0) sp[i * kDecodeChunk + t] = vis ? (x + band[i * BW + (L - 1 - i) + t]) * p.qscale : -INFINITY;
         }
     }
+    __syncthreads();
+    float s[LQ];
+#pragma unroll
+    for (int i = 0; i < LQ; ++i) s[i] = sp[i * kDecodeChunk + tid];
 
     // 4. per query: chunk maximum, probabilities, chunk sum
     float m[LQ];
@@ -193,44 +214,59 @@ __global__ void __launch_bounds__(kDecThreads) decode_partial_kernel(const __gri
     }
     __syncthreads();
 
-    // 5. O_i over this warp's 32 keys; lane owns dims 2 lane + 64 g, 2 lane + 1 + 64 g
+    // 5. O_i over this warp's 32 keys; lane owns dims 2 lane + 64 g, 2 lane + 1 + 64 g.  Rows are
+    //    requested eight at a time before any of them is used (a key outside [lo, K) reads the
+    //    chunk's first valid row and weighs 0), so each lane keeps eight loads in flight.
     constexpr int kG = 2;                                     // D <= 128
+    constexpr int kBatch = 8;
+    const int ng = D > 64 ? 2 : 1;
     float o[LQ][2 * kG];
 #pragma unroll
     for (int i = 0; i < LQ; ++i)
 #pragma unroll
         for (int e = 0; e < 2 * kG; ++e) o[i][e] = 0.f;
     const int kb = 32 * warp;
-#pragma unroll 4
-    for (int kk = 0; kk < 32; ++kk) {
-        const int t = kb + kk;
-        const int jj = j0 + t;
-        if (jj >= K || jj < p.lo) continue;                   // uniform across the warp
-        const T* vrow = kv_row<T>(p, b, h, jj, true);
-        float vx[2 * kG];
+    const int jfirst = max(j0, p.lo);                         // some valid key of the chunk
+    if (jfirst < K && j0 + kb < K) {
 #pragma unroll
         for (int g = 0; g < kG; ++g) {
+            if (g >= ng) break;
             const int d = 2 * lane + 64 * g;
-            if (p.vec_kv && d + 1 < D) {
-                if constexpr (sizeof(T) == 2) {
-                    const uint32_t w = __ldg(reinterpret_cast<const unsigned int*>(vrow + d));
-                    vx[2 * g] = __uint_as_float(w << 16);
-                    vx[2 * g + 1] = __uint_as_float(w & 0xffff0000u);
-                } else {
-                    const float2 w = __ldg(reinterpret_cast<const float2*>(vrow + d));
-                    vx[2 * g] = w.x;
-                    vx[2 * g + 1] = w.y;
+            const bool vec = p.vec_kv && d + 1 < D;
+#pragma unroll 1
+            for (int k8 = 0; k8 < 32; k8 += kBatch) {
+                float v0[kBatch], v1[kBatch];
+#pragma unroll
+                for (int e = 0; e < kBatch; ++e) {
+                    const int jj0 = j0 + kb + k8 + e;
+                    const int jj = (jj0 >= K || jj0 < p.lo) ? jfirst : jj0;
+                    const T* vrow = kv_row<T>(p, b, h, jj, true);
+                    if (vec) {
+                        if constexpr (sizeof(T) == 2) {
+                            const uint32_t w = __ldg(reinterpret_cast<const unsigned int*>(vrow + d));
+                            v0[e] = __uint_as_float(w << 16);
+                            v1[e] = __uint_as_float(w & 0xffff0000u);
+                        } else {
+                            const float2 w = __ldg(reinterpret_cast<const float2*>(vrow + d));
+                            v0[e] = w.x;
+                            v1[e] = w.y;
+                        }
+                    } else {
+                        v0[e] = d < D ? to_f(vrow[d]) : 0.f;
+                        v1[e] = d + 1 < D ? to_f(vrow[d + 1]) : 0.f;
+                    }
                 }
-            } else {
-                vx[2 * g] = d < D ? to_f(vrow[d]) : 0.f;
-                vx[2 * g + 1] = d + 1 < D ? to_f(vrow[d + 1]) : 0.f;
+#pragma unroll
+                for (int e = 0; e < kBatch; ++e) {
+                    const int t = kb + k8 + e;
+#pragma unroll
+                    for (int i = 0; i < LQ; ++i) {
+                        const float pij = sp[i * kDecodeChunk + t];   // 0 for masked and absent keys
+                        o[i][2 * g] = fmaf(pij, v0[e], o[i][2 * g]);
+                        o[i][2 * g + 1] = fmaf(pij, v1[e], o[i][2 * g + 1]);
+                    }
+                }
             }
-        }
-#pragma unroll
-        for (int i = 0; i < LQ; ++i) {
-            const float pij = sp[i * kDecodeChunk + t];
-#pragma unroll
-            for (int e = 0; e < 2 * kG; ++e) o[i][e] = fmaf(pij, vx[e], o[i][e]);
         }
     }
     constexpr int Do = 64 * kG;
@@ -266,6 +302,266 @@ __global__ void __launch_bounds__(kDecThreads) decode_partial_kernel(const __gri
     (void)m;
 }
 
+// ------------------------------------------------------------------------------------------
+// Staged variant for bf16 rows of D <= 64 (D a multiple of 8) whose starts are 16-byte aligned:
+// every thread first requests its share of the chunk's key rows, value rows and position-band
+// rows as 16-byte asynchronous copies into shared memory (absent rows are zero-filled without
+// reading memory), so a CTA has its ~96 KB in flight at once; the phases then read shared memory.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool live)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;"
+                 ::"r"(dst), "l"(src), "r"(live ? 16 : 0) : "memory");
+}
+
+constexpr int kStRowBytes = 128;                     // 64 bf16 per staged row
+constexpr int kStBandRows = kDecodeChunk + kDecodeMaxL;
+
+__device__ __forceinline__ void unpack8(uint4 x, float* o)
+{
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        o[2 * e] = __uint_as_float(w[e] << 16);
+        o[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+    }
+}
+
+template <int LQ>
+__global__ void __launch_bounds__(kDecThreads) decode_staged_kernel(const __grid_constant__ DecodeParams p)
+{
+    extern __shared__ __align__(16) float dsm[];
+    const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int rg = lane >> 3, part = lane & 7;
+    const int L = p.L, D = p.D, dch = D >> 3;
+    const int K = p.M + L;
+    const int j0 = c * kDecodeChunk;
+    uint8_t* ks = reinterpret_cast<uint8_t*>(dsm);                       // [CK][128 B]
+    uint8_t* vs = ks + kDecodeChunk * kStRowBytes;                         // [CK][128 B]
+    uint8_t* rs = vs + kDecodeChunk * kStRowBytes;                         // [CK + 16][128 B]
+    float* qu = reinterpret_cast<float*>(rs + kStBandRows * kStRowBytes);  // [LQ][64]
+    float* qv = qu + LQ * 64;
+    const int BW = kDecodeChunk + LQ;
+    float* band = qv + LQ * 64;                                            // [LQ][BW]
+    float* sp = band + LQ * BW;                                            // [LQ][CK]
+    float* red = sp + LQ * kDecodeChunk;                                   // [2][warps][LQ]
+    float* obuf = red + 2 * kDecWarps * LQ;                                // [warps][LQ][64]
+
+    // 0. all copies of the chunk in flight at once.  Thread tid moves 16-byte piece pc = tid mod 8
+    //    of rows tid/8 + 32 k (k = 0..7) of K and V, and of the position band unless every
+    //    distance of the chunk reaches clamp_len (then the band is one value per query).
+    const int delta_top = p.M + L - 1 - j0;
+    const int n_band = kDecodeChunk + L - 1;
+    const bool band_const = delta_top - (n_band - 1) >= p.C;
+    const int pc = tid & 7, r0 = tid >> 3;
+    if (pc < dch) {
+        const __nv_bfloat16* kmem = static_cast<const __nv_bfloat16*>(p.kmem) + b * p.m_sb + h * p.m_sh + 8 * pc;
+        const __nv_bfloat16* vmem = static_cast<const __nv_bfloat16*>(p.vmem) + b * p.m_sb + h * p.m_sh + 8 * pc;
+        const __nv_bfloat16* kcur = static_cast<const __nv_bfloat16*>(p.kcur) + b * p.kc_sb + h * p.kc_sh + 8 * pc;
+        const __nv_bfloat16* vcur = static_cast<const __nv_bfloat16*>(p.vcur) + b * p.vc_sb + h * p.vc_sh + 8 * pc;
+        const __nv_bfloat16* dummy = static_cast<const __nv_bfloat16*>(p.q);
+        const uint32_t ks_s = static_cast<uint32_t>(__cvta_generic_to_shared(ks)) + r0 * kStRowBytes + 16 * pc;
+        const uint32_t vs_s = static_cast<uint32_t>(__cvta_generic_to_shared(vs)) + r0 * kStRowBytes + 16 * pc;
+#pragma unroll
+        for (int k = 0; k < kDecodeChunk / 32; ++k) {
+            const int j = j0 + r0 + 32 * k;
+            const bool live = j < K && j >= p.lo;
+            const __nv_bfloat16* ksrc = dummy;
+            const __nv_bfloat16* vsrc = dummy;
+            if (live) {
+                if (j < p.M) {
+                    const int slot = p.wp + j >= p.M ? p.wp + j - p.M : p.wp + j;
+                    ksrc = kmem + static_cast<int64_t>(slot) * p.m_st;
+                    vsrc = vmem + static_cast<int64_t>(slot) * p.m_st;
+                } else {
+                    ksrc = kcur + static_cast<int64_t>(j - p.M) * p.kc_st;
+                    vsrc = vcur + static_cast<int64_t>(j - p.M) * p.vc_st;
+                }
+            }
+            cp_async16(ks_s + 32 * k * kStRowBytes, ksrc, live);
+            cp_async16(vs_s + 32 * k * kStRowBytes, vsrc, live);
+        }
+        if (!band_const) {
+            const __nv_bfloat16* rbase = static_cast<const __nv_bfloat16*>(p.r) + h * p.r_head + 8 * pc;
+            const uint32_t rs_s = static_cast<uint32_t>(__cvta_generic_to_shared(rs)) + r0 * kStRowBytes + 16 * pc;
+#pragma unroll
+            for (int k = 0; k < (kStBandRows + 31) / 32; ++k) {
+                const int rho = r0 + 32 * k;                  // rows < n_band <= kStBandRows - 1
+                if (rho >= n_band) break;
+                const int delta = delta_top - rho;
+                const bool live = delta >= 0;
+                const int dc = delta < p.C ? delta : p.C;
+                cp_async16(rs_s + 32 * k * kStRowBytes, live ? rbase + static_cast<int64_t>(dc) * p.r_row : dummy, live);
+            }
+        }
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+
+    // 1. q + u, q + v (fp32) while the copies fly (staged rows: Dp = 64)
+    for (int x = tid; x < LQ * 64; x += kDecThreads) {
+        const int i = x >> 6, d = x & 63;
+        const bool in = i < L && d < D;
+        const float qq = in ? __bfloat162float(static_cast<const __nv_bfloat16*>(p.q)[
+                                  b * p.q_sb + static_cast<int64_t>(i) * p.q_st + h * p.q_sh + d]) : 0.f;
+        qu[x] = in ? qq + __ldg(p.u + h * D + d) : 0.f;
+        qv[x] = in ? qq + __ldg(p.vb + h * D + d) : 0.f;
+    }
+    if (band_const) {
+        // every key of the chunk sits at distance >= clamp_len: e(i) = (q_i + v) . r[clamp_len]
+        __syncthreads();
+        if (warp == 0) {
+            const __nv_bfloat16* rrow = static_cast<const __nv_bfloat16*>(p.r) + static_cast<int64_t>(p.C) * p.r_row + h * p.r_head;
+            for (int i = 0; i < L; ++i) {
+                float x = 0.f;
+                for (int d = lane; d < D; d += 32) x = fmaf(qv[i * 64 + d], __bfloat162float(rrow[d]), x);
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+                if (lane == 0) band[i * BW] = x;
+            }
+        }
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
+
+    // 2. position band, eight lanes per row (lane part holds 16-byte piece part)
+    for (int rho0 = 4 * warp; rho0 < n_band && !band_const; rho0 += 4 * kDecWarps) {
+        const int rho = rho0 + rg;
+        float acc[LQ];
+#pragma unroll
+        for (int i = 0; i < LQ; ++i) acc[i] = 0.f;
+        if (rho < n_band && part < dch) {
+            float r8[8];
+            unpack8(*reinterpret_cast<const uint4*>(rs + rho * kStRowBytes + 16 * part), r8);
+#pragma unroll
+            for (int i = 0; i < LQ; ++i) {
+                const float4 a = *reinterpret_cast<const float4*>(qv + i * 64 + 8 * part);
+                const float4 e = *reinterpret_cast<const float4*>(qv + i * 64 + 8 * part + 4);
+                acc[i] = fmaf(a.x, r8[0], fmaf(a.y, r8[1], fmaf(a.z, r8[2], fmaf(a.w, r8[3], acc[i]))));
+                acc[i] = fmaf(e.x, r8[4], fmaf(e.y, r8[5], fmaf(e.z, r8[6], fmaf(e.w, r8[7], acc[i]))));
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < LQ; ++i) {
+            float x = acc[i];
+            x += __shfl_xor_sync(0xffffffffu, x, 1);
+            x += __shfl_xor_sync(0xffffffffu, x, 2);
+            x += __shfl_xor_sync(0xffffffffu, x, 4);
+            if (part == 0 && rho < n_band) band[i * BW + rho] = x;
+        }
+    }
+    __syncthreads();
+
+    // 3. scores, eight lanes per key row
+    for (int t0 = 32 * warp; t0 < 32 * warp + 32; t0 += 4) {
+        const int t = t0 + rg;
+        const int jj = j0 + t;
+        const bool live = jj < K && jj >= p.lo;
+        float acc[LQ];
+#pragma unroll
+        for (int i = 0; i < LQ; ++i) acc[i] = 0.f;
+        if (part < dch) {
+            float k8[8];
+            unpack8(*reinterpret_cast<const uint4*>(ks + t * kStRowBytes + 16 * part), k8);
+#pragma unroll
+            for (int i = 0; i < LQ; ++i) {
+                const float4 a = *reinterpret_cast<const float4*>(qu + i * 64 + 8 * part);
+                const float4 e = *reinterpret_cast<const float4*>(qu + i * 64 + 8 * part + 4);
+                acc[i] = fmaf(a.x, k8[0], fmaf(a.y, k8[1], fmaf(a.z, k8[2], fmaf(a.w, k8[3], acc[i]))));
+                acc[i] = fmaf(e.x, k8[4], fmaf(e.y, k8[5], fmaf(e.z, k8[6], fmaf(e.w, k8[7], acc[i]))));
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < LQ; ++i) {
+            float x = acc[i];
+            x += __shfl_xor_sync(0xffffffffu, x, 1);
+            x += __shfl_xor_sync(0xffffffffu, x, 2);
+            x += __shfl_xor_sync(0xffffffffu, x, 4);
+            const bool vis = live && i < L && jj <= p.M + i;
+            const float e = band[i * BW + (band_const ? 0 : (L - 1 - i) + t)];
+            if (part == 0) sp[i * kDecodeChunk + t] = vis ? (x + e) * p.qscale : -INFINITY;
+        }
+    }
+    __syncthreads();
+
+    // 4. per query: chunk maximum, probabilities, chunk sum
+    float s[LQ];
+#pragma unroll
+    for (int i = 0; i < LQ; ++i) {
+        s[i] = sp[i * kDecodeChunk + tid];
+        float x = s[i];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, off));
+        if (lane == 0) red[warp * LQ + i] = x;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < LQ; ++i) {
+        float x = red[i];
+#pragma unroll
+        for (int w = 1; w < kDecWarps; ++w) x = fmaxf(x, red[w * LQ + i]);
+        const float pv = x == -INFINITY ? 0.f : exp2f(s[i] - x);
+        sp[i * kDecodeChunk + tid] = pv;
+        float y = pv;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) y += __shfl_xor_sync(0xffffffffu, y, off);
+        if (lane == 0) red[(kDecWarps + warp) * LQ + i] = y;
+    }
+    __syncthreads();
+
+    // 5. O_i over this warp's 32 keys from shared memory; lane owns dims 2 lane, 2 lane + 1
+    //    (zero-filled absent rows weigh 0)
+    float o[LQ][2];
+#pragma unroll
+    for (int i = 0; i < LQ; ++i) o[i][0] = o[i][1] = 0.f;
+    if (2 * lane < D) {
+#pragma unroll 8
+        for (int kk = 0; kk < 32; ++kk) {
+            const int t = 32 * warp + kk;
+            const uint32_t w = *reinterpret_cast<const uint32_t*>(vs + t * kStRowBytes + 4 * lane);
+            const float v0 = __uint_as_float(w << 16), v1 = __uint_as_float(w & 0xffff0000u);
+#pragma unroll
+            for (int i = 0; i < LQ; ++i) {
+                const float pij = sp[i * kDecodeChunk + t];
+                o[i][0] = fmaf(pij, v0, o[i][0]);
+                o[i][1] = fmaf(pij, v1, o[i][1]);
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < LQ; ++i) {
+        obuf[(warp * LQ + i) * 64 + 2 * lane] = o[i][0];
+        obuf[(warp * LQ + i) * 64 + 2 * lane + 1] = o[i][1];
+    }
+    __syncthreads();
+
+    const int Dw = D + 2;
+    for (int x = tid; x < L * Dw; x += kDecThreads) {
+        const int i = x / Dw, e = x - i * Dw;
+        float val;
+        if (e == 0) {
+            val = red[i];
+#pragma unroll
+            for (int w = 1; w < kDecWarps; ++w) val = fmaxf(val, red[w * LQ + i]);
+        } else if (e == 1) {
+            val = 0.f;
+#pragma unroll
+            for (int w = 0; w < kDecWarps; ++w) val += red[(kDecWarps + w) * LQ + i];
+        } else {
+            val = 0.f;
+#pragma unroll
+            for (int w = 0; w < kDecWarps; ++w) val += obuf[(w * LQ + i) * 64 + (e - 2)];
+        }
+        p.part[((static_cast<int64_t>(b) * p.H + h) * L + i) * p.n_chunks * Dw + static_cast<int64_t>(c) * Dw + e] = val;
+    }
+}
+
+size_t decode_staged_smem_bytes(int lq)
+{
+    return static_cast<size_t>(2 * kDecodeChunk + kStBandRows) * kStRowBytes +
+           (2ull * lq * 64 + static_cast<size_t>(lq) * (kDecodeChunk + lq) + static_cast<size_t>(lq) * kDecodeChunk +
+            2ull * kDecWarps * lq + static_cast<size_t>(kDecWarps) * lq * 64) * sizeof(float);
+}
+
 template <typename T>
 __global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_constant__ DecodeParams p)
 {
@@ -296,17 +592,28 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_consta
 template <typename T, int LQ>
 cudaError_t launch_lq(const DecodeParams& p, cudaStream_t s)
 {
-    const size_t smem = decode_smem_bytes(LQ, p.Dp);
-    static bool attr_done = false;
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(decode_partial_kernel<T, LQ>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(decode_smem_bytes(LQ, 128)));
-        if (e != cudaSuccess) return e;
-        attr_done = true;
-    }
     dim3 grid(p.n_chunks, p.H, p.B);
-    decode_partial_kernel<T, LQ><<<grid, kDecThreads, smem, s>>>(p);
+    const bool staged = sizeof(T) == 2 && p.vec_kv && p.vec_r && (p.D % 8) == 0 && p.D <= 64;
+    if (staged) {
+        static bool attr_st = false;
+        if (!attr_st) {
+            cudaError_t e = cudaFuncSetAttribute(decode_staged_kernel<LQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 static_cast<int>(decode_staged_smem_bytes(LQ)));
+            if (e != cudaSuccess) return e;
+            attr_st = true;
+        }
+        decode_staged_kernel<LQ><<<grid, kDecThreads, decode_staged_smem_bytes(LQ), s>>>(p);
+    } else {
+        static bool attr_done = false;
+        if (!attr_done) {
+            cudaError_t e = cudaFuncSetAttribute(decode_partial_kernel<T, LQ>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 static_cast<int>(decode_smem_bytes(LQ, 128)));
+            if (e != cudaSuccess) return e;
+            attr_done = true;
+        }
+        decode_partial_kernel<T, LQ><<<grid, kDecThreads, decode_smem_bytes(LQ, p.Dp), s>>>(p);
+    }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     decode_combine_kernel<T><<<p.B * p.H * p.L, 128, 0, s>>>(p);
