@@ -314,7 +314,6 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool l
 }
 
 constexpr int kStRowBytes = 128;                     // 64 bf16 per staged row
-constexpr int kStBandRows = kDecodeChunk + kDecodeMaxL;
 
 __device__ __forceinline__ void unpack8(uint4 x, float* o)
 {
@@ -338,8 +337,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_staged_kernel(const __grid
     const int j0 = c * kDecodeChunk;
     uint8_t* ks = reinterpret_cast<uint8_t*>(dsm);                       // [CK][128 B]
     uint8_t* vs = ks + kDecodeChunk * kStRowBytes;                         // [CK][128 B]
-    uint8_t* rs = vs + kDecodeChunk * kStRowBytes;                         // [CK + 16][128 B]
-    float* qu = reinterpret_cast<float*>(rs + kStBandRows * kStRowBytes);  // [LQ][64]
+    float* qu = reinterpret_cast<float*>(vs + kDecodeChunk * kStRowBytes); // [LQ][64]
     float* qv = qu + LQ * 64;
     const int BW = kDecodeChunk + LQ;
     float* band = qv + LQ * 64;                                            // [LQ][BW]
@@ -348,8 +346,9 @@ __global__ void __launch_bounds__(kDecThreads) decode_staged_kernel(const __grid
     float* obuf = red + 2 * kDecWarps * LQ;                                // [warps][LQ][64]
 
     // 0. all copies of the chunk in flight at once.  Thread tid moves 16-byte piece pc = tid mod 8
-    //    of rows tid/8 + 32 k (k = 0..7) of K and V, and of the position band unless every
-    //    distance of the chunk reaches clamp_len (then the band is one value per query).
+    //    of rows tid/8 + 32 k (k = 0..7) of K and V.  (The position band reads r, small and
+    //    L2-resident, straight from global memory; when every distance of the chunk reaches
+    //    clamp_len it is one value per query.)
     const int delta_top = p.M + L - 1 - j0;
     const int n_band = kDecodeChunk + L - 1;
     const bool band_const = delta_top - (n_band - 1) >= p.C;
@@ -381,19 +380,6 @@ __global__ void __launch_bounds__(kDecThreads) decode_staged_kernel(const __grid
             cp_async16(ks_s + 32 * k * kStRowBytes, ksrc, live);
             cp_async16(vs_s + 32 * k * kStRowBytes, vsrc, live);
         }
-        if (!band_const) {
-            const __nv_bfloat16* rbase = static_cast<const __nv_bfloat16*>(p.r) + h * p.r_head + 8 * pc;
-            const uint32_t rs_s = static_cast<uint32_t>(__cvta_generic_to_shared(rs)) + r0 * kStRowBytes + 16 * pc;
-#pragma unroll
-            for (int k = 0; k < (kStBandRows + 31) / 32; ++k) {
-                const int rho = r0 + 32 * k;                  // rows < n_band <= kStBandRows - 1
-                if (rho >= n_band) break;
-                const int delta = delta_top - rho;
-                const bool live = delta >= 0;
-                const int dc = delta < p.C ? delta : p.C;
-                cp_async16(rs_s + 32 * k * kStRowBytes, live ? rbase + static_cast<int64_t>(dc) * p.r_row : dummy, live);
-            }
-        }
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
 
@@ -423,30 +409,47 @@ __global__ void __launch_bounds__(kDecThreads) decode_staged_kernel(const __grid
     asm volatile("cp.async.wait_group 0;" ::: "memory");
     __syncthreads();
 
-    // 2. position band, eight lanes per row (lane part holds 16-byte piece part)
-    for (int rho0 = 4 * warp; rho0 < n_band && !band_const; rho0 += 4 * kDecWarps) {
-        const int rho = rho0 + rg;
-        float acc[LQ];
+    // 2. position band, eight lanes per row (lane part holds 16-byte piece part); each lane
+    //    requests its pieces of all its rows before using any
+    if (!band_const) {
+        constexpr int kBandIter = (kDecodeChunk + kDecodeMaxL + 31) / 32;
+        uint4 raw[kBandIter];
 #pragma unroll
-        for (int i = 0; i < LQ; ++i) acc[i] = 0.f;
-        if (rho < n_band && part < dch) {
-            float r8[8];
-            unpack8(*reinterpret_cast<const uint4*>(rs + rho * kStRowBytes + 16 * part), r8);
-#pragma unroll
-            for (int i = 0; i < LQ; ++i) {
-                const float4 a = *reinterpret_cast<const float4*>(qv + i * 64 + 8 * part);
-                const float4 e = *reinterpret_cast<const float4*>(qv + i * 64 + 8 * part + 4);
-                acc[i] = fmaf(a.x, r8[0], fmaf(a.y, r8[1], fmaf(a.z, r8[2], fmaf(a.w, r8[3], acc[i]))));
-                acc[i] = fmaf(e.x, r8[4], fmaf(e.y, r8[5], fmaf(e.z, r8[6], fmaf(e.w, r8[7], acc[i]))));
+        for (int k = 0; k < kBandIter; ++k) {
+            const int rho = 4 * warp + 32 * k + rg;
+            const int delta = delta_top - rho;
+            raw[k] = make_uint4(0u, 0u, 0u, 0u);
+            if (rho < n_band && delta >= 0 && part < dch) {
+                const int dc = delta < p.C ? delta : p.C;
+                raw[k] = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.r) +
+                                                              static_cast<int64_t>(dc) * p.r_row + h * p.r_head + 8 * part));
             }
         }
 #pragma unroll
-        for (int i = 0; i < LQ; ++i) {
-            float x = acc[i];
-            x += __shfl_xor_sync(0xffffffffu, x, 1);
-            x += __shfl_xor_sync(0xffffffffu, x, 2);
-            x += __shfl_xor_sync(0xffffffffu, x, 4);
-            if (part == 0 && rho < n_band) band[i * BW + rho] = x;
+        for (int k = 0; k < kBandIter; ++k) {
+            const int rho = 4 * warp + 32 * k + rg;
+            float acc[LQ];
+#pragma unroll
+            for (int i = 0; i < LQ; ++i) acc[i] = 0.f;
+            if (part < dch) {
+                float r8[8];
+                unpack8(raw[k], r8);
+#pragma unroll
+                for (int i = 0; i < LQ; ++i) {
+                    const float4 a = *reinterpret_cast<const float4*>(qv + i * 64 + 8 * part);
+                    const float4 e = *reinterpret_cast<const float4*>(qv + i * 64 + 8 * part + 4);
+                    acc[i] = fmaf(a.x, r8[0], fmaf(a.y, r8[1], fmaf(a.z, r8[2], fmaf(a.w, r8[3], acc[i]))));
+                    acc[i] = fmaf(e.x, r8[4], fmaf(e.y, r8[5], fmaf(e.z, r8[6], fmaf(e.w, r8[7], acc[i]))));
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < LQ; ++i) {
+                float x = acc[i];
+                x += __shfl_xor_sync(0xffffffffu, x, 1);
+                x += __shfl_xor_sync(0xffffffffu, x, 2);
+                x += __shfl_xor_sync(0xffffffffu, x, 4);
+                if (part == 0 && rho < n_band) band[i * BW + rho] = x;
+            }
         }
     }
     __syncthreads();
@@ -557,7 +560,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_staged_kernel(const __grid
 
 size_t decode_staged_smem_bytes(int lq)
 {
-    return static_cast<size_t>(2 * kDecodeChunk + kStBandRows) * kStRowBytes +
+    return static_cast<size_t>(2 * kDecodeChunk) * kStRowBytes +
            (2ull * lq * 64 + static_cast<size_t>(lq) * (kDecodeChunk + lq) + static_cast<size_t>(lq) * kDecodeChunk +
             2ull * kDecWarps * lq + static_cast<size_t>(kDecWarps) * lq * 64) * sizeof(float);
 }
@@ -565,21 +568,50 @@ size_t decode_staged_smem_bytes(int lq)
 template <typename T>
 __global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_constant__ DecodeParams p)
 {
+    // weights of the chunks first (in parallel), then every output dimension reads its chunks'
+    // partial sums with independent loads
+    __shared__ float wsh[1024];
+    __shared__ float mred[4];
     const int bhi = blockIdx.x;                               // (b * H + h) * L + i
     const int i = bhi % p.L;
     const int bh = bhi / p.L;
     const int h = bh % p.H, b = bh / p.H;
     const int Dw = p.D + 2;
-    const float* part = p.part + static_cast<int64_t>(bhi) * p.n_chunks * Dw;
+    const int nc = p.n_chunks;
+    const float* part = p.part + static_cast<int64_t>(bhi) * nc * Dw;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     float mx = -INFINITY;
-    for (int c = 0; c < p.n_chunks; ++c) mx = fmaxf(mx, part[c * Dw]);
-    for (int d = threadIdx.x; d < p.D; d += blockDim.x) {
-        float num = 0.f, den = 0.f;
-        for (int c = 0; c < p.n_chunks; ++c) {
-            const float mc = part[c * Dw];
-            if (mc == -INFINITY) continue;
-            const float w = exp2f(mc - mx);
-            den = fmaf(w, part[c * Dw + 1], den);
+    for (int c = tid; c < nc; c += blockDim.x) mx = fmaxf(mx, part[c * Dw]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if (lane == 0) mred[warp] = mx;
+    __syncthreads();
+    mx = fmaxf(fmaxf(mred[0], mred[1]), fmaxf(mred[2], mred[3]));
+    float den = 0.f;
+    const bool in_smem = nc <= 1024;
+    for (int c = tid; c < nc; c += blockDim.x) {
+        const float mc = part[c * Dw];
+        const float w = mc == -INFINITY ? 0.f : exp2f(mc - mx);
+        if (in_smem) wsh[c] = w;
+        den = fmaf(w, part[c * Dw + 1], den);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+    __syncthreads();
+    if (lane == 0) mred[warp] = den;
+    __syncthreads();
+    den = (mred[0] + mred[1]) + (mred[2] + mred[3]);
+    for (int d = tid; d < p.D; d += blockDim.x) {
+        float num = 0.f;
+#pragma unroll 4
+        for (int c = 0; c < nc; ++c) {
+            float w;
+            if (in_smem) {
+                w = wsh[c];
+            } else {
+                const float mc = part[c * Dw];
+                w = mc == -INFINITY ? 0.f : exp2f(mc - mx);
+            }
             num = fmaf(w, part[c * Dw + 2 + d], num);
         }
         T* o = static_cast<T*>(p.out) + b * p.o_sb + static_cast<int64_t>(i) * p.o_st + h * p.o_sh + d;
