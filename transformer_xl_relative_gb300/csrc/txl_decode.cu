@@ -455,33 +455,89 @@ __global__ void __launch_bounds__(kDecThreads) decode_staged_kernel(const __grid
     __syncthreads();
 
     // 3. scores, eight lanes per key row
-    for (int t0 = 32 * warp; t0 < 32 * warp + 32; t0 += 4) {
-        const int t = t0 + rg;
-        const int jj = j0 + t;
-        const bool live = jj < K && jj >= p.lo;
-        float acc[LQ];
+    if constexpr (LQ <= 4) {
+        // q + u of the lane's piece stays in registers; lane (rg, part) forms the partial dots of
+        // its piece for rows t = 32 warp + 4 k + rg (k = 0..7), then a transposing butterfly over
+        // the group's eight lanes leaves lane part with the whole dot of row k = part.
+        float qr[LQ][8];
 #pragma unroll
-        for (int i = 0; i < LQ; ++i) acc[i] = 0.f;
-        if (part < dch) {
+        for (int i = 0; i < LQ; ++i)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) qr[i][e] = part < dch ? qu[i * 64 + 8 * part + e] : 0.f;
+        float acc[LQ][8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int t = 32 * warp + 4 * k + rg;
             float k8[8];
-            unpack8(*reinterpret_cast<const uint4*>(ks + t * kStRowBytes + 16 * part), k8);
+            if (part < dch) {
+                unpack8(*reinterpret_cast<const uint4*>(ks + t * kStRowBytes + 16 * part), k8);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) k8[e] = 0.f;
+            }
 #pragma unroll
             for (int i = 0; i < LQ; ++i) {
-                const float4 a = *reinterpret_cast<const float4*>(qu + i * 64 + 8 * part);
-                const float4 e = *reinterpret_cast<const float4*>(qu + i * 64 + 8 * part + 4);
-                acc[i] = fmaf(a.x, k8[0], fmaf(a.y, k8[1], fmaf(a.z, k8[2], fmaf(a.w, k8[3], acc[i]))));
-                acc[i] = fmaf(e.x, k8[4], fmaf(e.y, k8[5], fmaf(e.z, k8[6], fmaf(e.w, k8[7], acc[i]))));
+                float x = 0.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x = fmaf(qr[i][e], k8[e], x);
+                acc[i][k] = x;
             }
         }
+        const bool b4 = part & 4, b2 = part & 2, b1 = part & 1;
+        const int t = 32 * warp + 4 * part + rg;
+        const int jj = j0 + t;
+        const bool live = jj < K && jj >= p.lo;
 #pragma unroll
         for (int i = 0; i < LQ; ++i) {
-            float x = acc[i];
-            x += __shfl_xor_sync(0xffffffffu, x, 1);
-            x += __shfl_xor_sync(0xffffffffu, x, 2);
-            x += __shfl_xor_sync(0xffffffffu, x, 4);
+            float v4[4], v2[2];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const float keep = b4 ? acc[i][m + 4] : acc[i][m];
+                const float send = b4 ? acc[i][m] : acc[i][m + 4];
+                v4[m] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+            }
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+                const float keep = b2 ? v4[m + 2] : v4[m];
+                const float send = b2 ? v4[m] : v4[m + 2];
+                v2[m] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+            }
+            const float keep = b1 ? v2[1] : v2[0];
+            const float send = b1 ? v2[0] : v2[1];
+            const float x = keep + __shfl_xor_sync(0xffffffffu, send, 1);
             const bool vis = live && i < L && jj <= p.M + i;
             const float e = band[i * BW + (band_const ? 0 : (L - 1 - i) + t)];
-            if (part == 0) sp[i * kDecodeChunk + t] = vis ? (x + e) * p.qscale : -INFINITY;
+            sp[i * kDecodeChunk + t] = vis ? (x + e) * p.qscale : -INFINITY;
+        }
+    } else {
+        for (int t0 = 32 * warp; t0 < 32 * warp + 32; t0 += 4) {
+            const int t = t0 + rg;
+            const int jj = j0 + t;
+            const bool live = jj < K && jj >= p.lo;
+            float acc[LQ];
+    #pragma unroll
+            for (int i = 0; i < LQ; ++i) acc[i] = 0.f;
+            if (part < dch) {
+                float k8[8];
+                unpack8(*reinterpret_cast<const uint4*>(ks + t * kStRowBytes + 16 * part), k8);
+    #pragma unroll
+                for (int i = 0; i < LQ; ++i) {
+                    const float4 a = *reinterpret_cast<const float4*>(qu + i * 64 + 8 * part);
+                    const float4 e = *reinterpret_cast<const float4*>(qu + i * 64 + 8 * part + 4);
+                    acc[i] = fmaf(a.x, k8[0], fmaf(a.y, k8[1], fmaf(a.z, k8[2], fmaf(a.w, k8[3], acc[i]))));
+                    acc[i] = fmaf(e.x, k8[4], fmaf(e.y, k8[5], fmaf(e.z, k8[6], fmaf(e.w, k8[7], acc[i]))));
+                }
+            }
+    #pragma unroll
+            for (int i = 0; i < LQ; ++i) {
+                float x = acc[i];
+                x += __shfl_xor_sync(0xffffffffu, x, 1);
+                x += __shfl_xor_sync(0xffffffffu, x, 2);
+                x += __shfl_xor_sync(0xffffffffu, x, 4);
+                const bool vis = live && i < L && jj <= p.M + i;
+                const float e = band[i * BW + (band_const ? 0 : (L - 1 - i) + t)];
+                if (part == 0) sp[i * kDecodeChunk + t] = vis ? (x + e) * p.qscale : -INFINITY;
+            }
         }
     }
     __syncthreads();
