@@ -28,6 +28,9 @@ def txl():
     ("bf16", 10, 41, 410, 300, 416),
     ("bf16", 2, 64, 96, 200, 0),          # d_model not a multiple of 64
     ("bf16", 16, 128, 2048, 1001, 0),
+    ("bf16", 4, 64, 96, 300, 0),          # two column tiles: clusters of 2, K tail
+    ("bf16", 12, 64, 768, 257, 0),        # six column tiles: clusters of 2
+    ("bf16", 6, 64, 384, 130, 0),         # three column tiles: one CTA per tile
 ])
 def test_rel_pos_gen(txl, dtype, H, D, d_model, n_rows, ld_w):
     cfg = txl_inputs.custom(H=H, D=D, d_model=d_model, dtype=dtype, seed=3, ld_w=ld_w)

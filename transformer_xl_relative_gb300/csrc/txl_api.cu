@@ -172,7 +172,7 @@ txl_status txl_rel_pos_gen(int n_rows, int d_model, int n_head, int d_head, cons
     const int HD = n_head * d_head;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(HD), static_cast<cuuint64_t>(d_model)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld_w * 2)};
-    const cuuint32_t box[2] = {64, 64};
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kPosKTile)};
     const cuuint32_t estr[2] = {1, 1};
     if (g_encode(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(W_R), dims, strides, box, estr,
                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -184,7 +184,8 @@ txl_status txl_rel_pos_gen(int n_rows, int d_model, int n_head, int d_head, cons
     p.d_model = d_model;
     p.H = n_head;
     p.D = d_head;
-    p.n_ktiles = (d_model + 63) / 64;
+    p.n_ktiles = (d_model + kPosKTile - 1) / kPosKTile;
+    p.dense = (ld_r == d_head && HD % 8 == 0 && a16(r)) ? 1 : 0;
     p.err_flag = nullptr;
     p.log2_freq_step = static_cast<float>(-2.0 * std::log2(10000.0) / static_cast<double>(d_model));
     return launch_pos_gen_tc(p, s) == cudaSuccess ? TXL_OK : TXL_ERR_CUDA;

@@ -27,12 +27,15 @@ struct PosGenF32Params {
     int n_rows, d_model, H, D;
 };
 
+constexpr int kPosKTile = 128;   // sinusoid columns (K) per pipeline stage of the bf16 kernel
+
 struct PosGenTcParams {
-    CUtensorMap tm_w;    // W_R as 2D (n = h*D+d, m): box 64 x 64, 128-byte swizzle
+    CUtensorMap tm_w;    // W_R as 2D (n = h*D+d, m): box 64 x kPosKTile, 128-byte swizzle
     void* r;             // bf16 [n_rows][H][ld_r]
     int64_t ld_r;
     int n_rows, d_model, H, D;
-    int n_ktiles;        // ceil(d_model / 64)
+    int n_ktiles;        // ceil(d_model / kPosKTile)
+    int dense;           // ld_r == D, H*D a multiple of 8 and r 16-byte aligned: row-vector stores
     int* err_flag;
     float log2_freq_step;        // -2 log2(10000) / d_model: w_k = 2^(k * log2_freq_step)
 };

@@ -192,6 +192,19 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// bar.sync over `nthreads` threads that also returns the AND of every thread's predicate.
+__device__ __forceinline__ bool named_bar_and(int id, int nthreads, bool pred)
+{
+    uint32_t out;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %3, 0;\n\t"
+        "bar.red.and.pred q, %1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(out)
+        : "r"(id), "r"(nthreads), "r"(static_cast<uint32_t>(pred))
+        : "memory");
+    return out != 0;
+}
+
 // ------------------------------------------------------------------------------- tcgen05
 // TMEM allocation: executed by one full warp.  The allocated column base is written to smem.
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols)
