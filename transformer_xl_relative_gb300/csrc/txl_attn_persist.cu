@@ -146,7 +146,9 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_persist_kernel(const __grid
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
+    pdl_launch_dependents();
     if ((smem_u32(smem) & 1023u) != 0) {
+        pdl_wait();
         if (tid == 0 && p.err_flag) atomicCAS(p.err_flag, 0, TXL_ERR_ALIGNMENT);
         return;
     }
@@ -183,6 +185,9 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_persist_kernel(const __grid
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // inputs (q, k, v, r, the memory) may come from the previous grid, which may also still read
+    // the output buffer: no global access before this point
+    pdl_wait();
     const uint32_t tmem = *tmem_holder;
     const WaitCtl wc{abort_flag, p.err_flag, kWaitTimeoutNs};
     const int C = p.C;
@@ -655,8 +660,7 @@ cudaError_t launch_attn_persist(const AttnTcParams& p, int sm_count, cudaStream_
     }
     const int64_t items = static_cast<int64_t>(p.n_qt) * p.H * p.B;
     const int grid = static_cast<int>(items < sm_count ? items : sm_count);
-    attn_persist_kernel<<<grid, kPThreads, PSmem::Size, s>>>(p);
-    return cudaGetLastError();
+    return launch_dependent(attn_persist_kernel, dim3(grid), dim3(kPThreads), PSmem::Size, s, p);
 }
 
 }  // namespace txl

@@ -10,6 +10,27 @@
 
 namespace txl {
 
+// Launch with programmatic stream serialization: the grid may start (and run its prologue) while
+// the previous grid of the stream finishes; the kernel itself calls pdl_wait before it touches
+// global memory.  Used for the kernels of one forward step (position table, fused attention,
+// memory push), which follow one another on a stream.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                             Args&&... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 constexpr int kMaxDModel = 4096;   // the bf16 path keeps d_model/2 frequencies in shared memory
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;   // 2 s: far above any healthy wait
 constexpr int kSchedCapacity = 4096;   // bytes of per-CTA item counts carried as kernel parameters

@@ -21,6 +21,8 @@ constexpr int kPushRows = 4;            // (b, t) rows per block pass: 4 loads i
 // M + L fit) and is done once per row, not per byte.
 __global__ void __launch_bounds__(kPushThreads) mem_push_vec16(MemPushParams p)
 {
+    pdl_launch_dependents();
+    pdl_wait();
     const int which = blockIdx.y;
     const int eb = p.elem_bytes;
     const int cpr = (p.D * eb) >> 4;                       // 16-byte chunks per head row
@@ -112,7 +114,7 @@ cudaError_t launch_mem_push(const MemPushParams& p, cudaStream_t s)
         const int64_t rows = static_cast<int64_t>(p.B) * p.n_t;
         int64_t blocks = (rows + kPushRows - 1) / kPushRows;
         if (blocks > cap / 2) blocks = cap / 2;
-        mem_push_vec16<<<dim3(static_cast<unsigned>(blocks), 2), kPushThreads, 0, s>>>(p);
+        return launch_dependent(mem_push_vec16, dim3(static_cast<unsigned>(blocks), 2), dim3(kPushThreads), 0, s, p);
     } else {
         int64_t blocks = (work + kPushThreads - 1) / kPushThreads;
         if (blocks > cap) blocks = cap;

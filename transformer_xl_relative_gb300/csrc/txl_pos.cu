@@ -193,7 +193,9 @@ __global__ void __launch_bounds__(kPosThreads, 1) pos_gen_tc_kernel(const __grid
     float2* freq2 = reinterpret_cast<float2*>(smem + PosSmem::Freq);
     float4* step4 = reinterpret_cast<float4*>(smem + PosSmem::Step);
 
+    pdl_launch_dependents();
     if ((smem_u32(smem) & 1023u) != 0) {        // the swizzled layout needs a 1 KB aligned base
+        pdl_wait();
         if (tid == 0 && p.err_flag) atomicCAS(p.err_flag, 0, TXL_ERR_ALIGNMENT);
         return;
     }
@@ -223,6 +225,7 @@ __global__ void __launch_bounds__(kPosThreads, 1) pos_gen_tc_kernel(const __grid
         // ------------------------------------------------ TMA producer: W_R tiles
         if (lane == 0) {
             tma_prefetch_desc(&p.tm_w);
+            pdl_wait();                                  // W_R may come from the previous grid
             int issued = 0;
             int s = 0;
             uint32_t par = 0;
@@ -358,6 +361,7 @@ __global__ void __launch_bounds__(kPosThreads, 1) pos_gen_tc_kernel(const __grid
             }
         }
         if (ok) ok = warp_wait(acc_full, 0, wc, 7);
+        pdl_wait();                                      // the previous grid may still read r
         // every generator warp reaches the staging barrier of the dense epilogue, or none does
         ok = named_bar_and(1, kPosGenThreads, ok);
         if (ok) {
@@ -400,8 +404,7 @@ cudaError_t launch_pos_gen_tc(const PosGenTcParams& p, cudaStream_t s)
         attr_done = true;
     }
     dim3 grid((p.n_rows + 127) / 128, (p.H * p.D + 127) / 128);
-    pos_gen_tc_kernel<<<grid, kPosThreads, PosSmem::Size, s>>>(p);
-    return cudaGetLastError();
+    return launch_dependent(pos_gen_tc_kernel, grid, dim3(kPosThreads), PosSmem::Size, s, p);
 }
 
 }  // namespace txl

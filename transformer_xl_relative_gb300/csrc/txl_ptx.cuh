@@ -142,6 +142,15 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
     return ok;
 }
 
+// ------------------------------------------------------------------------------- dependent launch
+// A grid launched with programmatic stream serialization may begin while the previous grid of
+// the stream is still running.  pdl_wait blocks until that grid has completed and its memory
+// operations are visible; a thread must call it before touching global memory the previous grid
+// may read or write (a no-op in a grid launched without the attribute).  pdl_launch_dependents
+// lets the next such grid of the stream begin launching; it does not release its pdl_wait.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map)
 {
