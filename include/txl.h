@@ -208,6 +208,53 @@ txl_status txl_rel_attn_decode_noalloc(int B, int L, int H, int D, int clamp_len
 txl_status txl_mem_push(txl_mem* mem, const txl_view* k_new, const txl_view* v_new, int L,
                         void* stream);
 
+/*
+ * txl_linear -- Y = X W: bf16 inputs, fp32 accumulation on the tensor cores, one rounding of each
+ * output to bf16.  The content projections of the attention layer: q_proj, k_proj, v_proj and
+ * o_proj of "TransformerXL 相对位置编码" §3.1 (linear maps without bias); Q = h W_q, K = h~ W_k,
+ * V = h~ W_v of "Transformer-XL 和相对位置编码" §2.3.1.
+ *   X : device [m][ld_x], columns 0..k-1 are read;  W : device [k][ld_w], columns 0..n-1 are read;
+ *   Y : device [m][ld_y], columns 0..n-1 are written and nothing else.
+ * Limits: m, n >= 0 (either 0: nothing to do), k >= 1; ld_x >= k, ld_w >= n, ld_y >= n; X and W
+ * 16-byte aligned with ld_x, ld_w multiples of 8 (TXL_ERR_ALIGNMENT otherwise).  bf16 only
+ * (TXL_ERR_UNSUPPORTED for TXL_F32).  err_flag: as txl_rel_attn_fwd.
+ */
+txl_status txl_linear(int m, int n, int k, const void* X, int64_t ld_x, const void* W, int64_t ld_w,
+                      void* Y, int64_t ld_y, txl_dtype dtype, int* err_flag, void* stream);
+
+/*
+ * txl_rel_attn_layer -- one attention-layer step of Transformer-XL over hidden states:
+ *   Q = h W_q and K = h~ W_k, V = h~ W_v over h~ = [SG(h_mem) o h], the memory-extended states
+ *   ("Transformer-XL 和相对位置编码" §2.3.1); the relative attention of txl_rel_attn_fwd with the
+ *   memory's keys first; y = concat_heads(attention) W_o ("TransformerXL 相对位置编码" §3.1); then
+ *   the segment enters the memory (the FIFO of txl_mem_push; mem->wp and mem->valid advance).
+ * The memory caches the projected keys and values of its positions (h_mem W_k, h_mem W_v) rather
+ * than h_mem: with the weights fixed this is the same function (a row's projection does not depend
+ * on when it is taken), and each position is projected once, when it enters the memory, instead of
+ * once for every segment that attends to it.
+ *   h      : device bf16 [B*L][ld_h], row b*L + t = position t of batch entry b, d_model columns.
+ *   mem    : K/V memory as for txl_rel_attn_fwd (bf16, B, H, D matching), or NULL / M = 0.
+ *   W_qkv  : device bf16 [d_model][3*H*D], columns [0,HD) = W_q, [HD,2HD) = W_k, [2HD,3HD) = W_v.
+ *   W_o    : device bf16 [H*D][d_model].
+ *   u, v_bias, r, ld_r, n_rows, clamp_len, scale : as txl_rel_attn_fwd (r from txl_rel_pos_gen).
+ *   y      : device bf16 [B*L][ld_y], d_model columns written.
+ *   workspace : device, >= txl_rel_attn_layer_workspace_size(B, L, H, D) bytes, 16-byte aligned
+ *            (TXL_ERR_WORKSPACE if missing or smaller): the segment's q|k|v [B*L][3*H*D] and the
+ *            attention output [B*L][H*D], bf16.  Its contents after the call are unspecified.
+ * Limits: H*D and d_model multiples of 8; the limits of txl_linear and txl_rel_attn_fwd.  bf16
+ * only.  Enqueues four launches on `stream` (projection, attention, output projection, push).
+ */
+txl_status txl_rel_attn_layer(int B, int L, int H, int D, int d_model, int clamp_len,
+                              const void* h, int64_t ld_h, txl_mem* mem,
+                              const void* W_qkv, const void* W_o,
+                              const float* u, const float* v_bias,
+                              const void* r, int64_t ld_r, int n_rows, float scale,
+                              void* y, int64_t ld_y, void* workspace, size_t workspace_bytes,
+                              int* err_flag, void* stream);
+
+/* Bytes of device workspace txl_rel_attn_layer needs: B*L*H*D*8 (0 for an empty shape). */
+size_t txl_rel_attn_layer_workspace_size(int B, int L, int H, int D);
+
 /* Self-test of the bounded waits used by every kernel: launches one CTA that waits on an
  * mbarrier nothing will signal, gives up after timeout_us microseconds (1 .. 10^7), writes
  * TXL_ERR_TIMEOUT to the device int err_flag and returns.  The context stays usable. */

@@ -15,4 +15,8 @@ from .oracle import (  # noqa: F401
     ring_push,
     ring_logical,
     attn_flops,
+    linear,
+    rel_layer,
+    stream_layer,
+    layer_flops,
 )

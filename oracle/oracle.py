@@ -184,6 +184,64 @@ def ring_logical(ring: np.ndarray, wp: int, valid: int) -> np.ndarray:
     return out
 
 
+def linear(X, W) -> np.ndarray:
+    """Y = X W in fp64 (a library matmul as the step): q_proj / k_proj / v_proj / o_proj of
+    "TransformerXL 相对位置编码" §3.1, linear maps without bias."""
+    return _f64(X) @ _f64(W)
+
+
+def rel_layer(h_mem, h, W_q, W_k, W_v, W_o, u, vb, W_R, H: int, D: int, mem_valid: int,
+              clamp_len: int, scale=None, threads=None, rows=None) -> np.ndarray:
+    """One attention-layer step with a memory of hidden states, in the order
+    "Transformer-XL 和相对位置编码" §2.3.1 gives it: the memory-extended states
+    h~ = [SG(h_mem) o h] (memory first, along the sequence), Q = h W_q, K = h~ W_k, V = h~ W_v,
+    then the relative attention (``rel_attn``) and the output projection over the concatenated
+    heads, y = attn W_o ("TransformerXL 相对位置编码" §3.1).  Stop-gradient has no effect on the
+    forward values.
+
+    h_mem [B, M, d_model] (logical order, oldest first; the first M - mem_valid rows are not
+    valid), h [B, L, d_model]; W_q, W_k, W_v [d_model, H*D]; W_o [H*D, d_model].  Returns
+    y [B, L, d_model] (rows not selected by ``rows`` = (b, h, i) triples come back NaN).
+    """
+    h_mem, h = _f64(h_mem), _f64(h)
+    B, L, dm = h.shape
+    M = h_mem.shape[1]
+    h_ext = np.concatenate([h_mem, h], axis=1)                   # [B, M+L, d_model]
+    q = linear(h, W_q).reshape(B, L, H, D)
+    k = linear(h_ext, W_k).reshape(B, M + L, H, D)
+    v = linear(h_ext, W_v).reshape(B, M + L, H, D)
+    a = rel_attn(q, k, v, u, vb, W_R, M, mem_valid, clamp_len, scale=scale, threads=threads, rows=rows)
+    return linear(a.reshape(B, L, H * D), W_o)
+
+
+def stream_layer(h_all, W_q, W_k, W_v, W_o, u, vb, W_R, H: int, D: int, L: int, M: int,
+                 clamp_len: int, scale=None, threads=None) -> np.ndarray:
+    """The layer over S consecutive segments of h_all [B, S*L, d_model]: segment s attends to
+    the hidden states of the M positions before it (fewer at the start of the sequence, the rest
+    of the memory not valid), re-projected at every step, as the recurrence of
+    "Transformer-XL 和相对位置编码" §2.3.1 defines it."""
+    h_all = _f64(h_all)
+    B, T, dm = h_all.shape
+    assert T % L == 0
+    out = np.empty((B, T, _f64(W_o).shape[1]), dtype=np.float64)
+    for s in range(T // L):
+        t0 = s * L
+        valid = min(t0, M)
+        h_mem = np.zeros((B, M, dm), dtype=np.float64)
+        if valid:
+            h_mem[:, M - valid:] = h_all[:, t0 - valid:t0]
+        out[:, t0:t0 + L] = rel_layer(h_mem, h_all[:, t0:t0 + L], W_q, W_k, W_v, W_o, u, vb, W_R, H, D,
+                                      valid, clamp_len, scale=scale, threads=threads)
+    return out
+
+
+def layer_flops(B: int, H: int, D: int, L: int, M: int, d_model: int, mem_valid: int | None = None) -> int:
+    """Algorithmic flops of one layer step: the projections of the segment (q, k, v: 2*d_model*3HD
+    per position; output: 2*HD*d_model per position) plus the attention (``attn_flops``).  The
+    memory's keys and values are projected when they enter the memory, once per position."""
+    return 2 * B * L * d_model * 4 * H * D + attn_flops(B, H, D, L, M, mem_valid)
+
+
 def attn_flops(B: int, H: int, D: int, L: int, M: int, mem_valid: int | None = None) -> int:
     """Algorithmic flops of one call: 6*D per visible (query, key) pair (AC 2D, BD 2D, PV 2D)."""
     if mem_valid is None:

@@ -142,6 +142,29 @@ def test_rejections_before_any_launch(native):
     assert lib.txl_rel_attn_decode_noalloc(64, 16, 16, 64, 1000, ctypes.byref(q), ctypes.byref(mem),
                                            ctypes.byref(q), ctypes.byref(q), FAKE, FAKE, FAKE, 64, 4112,
                                            0.0, ctypes.byref(q), 1, None) == native.TXL_ERR_WORKSPACE
+    # projections: fp32 is not provided, K must be positive, rows must hold their columns, X and W
+    # need 16-byte rows; an empty product is a no-op
+    assert lib.txl_linear(8, 8, 8, FAKE, 8, FAKE, 8, FAKE, 8, 0, None, None) == native.TXL_ERR_UNSUPPORTED
+    assert lib.txl_linear(8, 8, 0, FAKE, 8, FAKE, 8, FAKE, 8, 1, None, None) == native.TXL_ERR_INVALID_ARG
+    assert lib.txl_linear(8, 16, 8, FAKE, 8, FAKE, 8, FAKE, 16, 1, None, None) == native.TXL_ERR_INVALID_ARG
+    assert lib.txl_linear(8, 8, 8, FAKE + 2, 8, FAKE, 8, FAKE, 8, 1, None, None) == native.TXL_ERR_ALIGNMENT
+    assert lib.txl_linear(8, 8, 12, FAKE, 12, FAKE, 8, FAKE, 8, 1, None, None) == native.TXL_ERR_ALIGNMENT
+    assert lib.txl_linear(0, 8, 8, FAKE, 8, FAKE, 8, FAKE, 8, 1, None, None) == native.TXL_OK
+    # layer step: workspace formula, a missing or short workspace, H*D or d_model not a multiple
+    # of 8, a memory of another shape; all rejected before any launch and the memory unchanged
+    assert lib.txl_rel_attn_layer_workspace_size(2, 3, 4, 64) == 2 * 3 * 4 * 64 * 8
+    assert lib.txl_rel_attn_layer_workspace_size(0, 3, 4, 64) == 0
+    mem = native.TxlMem(FAKE, FAKE, 64, 8, 8, 2, 8, 4, 64, 1, 0, 0)
+    lay = lambda B, H, D, dm, ws, n: lib.txl_rel_attn_layer(  # noqa: E731
+        B, 8, H, D, dm, 16, FAKE, dm, ctypes.byref(mem), FAKE, FAKE, FAKE, FAKE, FAKE, D, 16, 0.0, FAKE, dm,
+        ws, n, None, None)
+    assert lay(2, 4, 64, 128, None, 0) == native.TXL_ERR_WORKSPACE
+    assert lay(2, 4, 64, 128, FAKE, 16) == native.TXL_ERR_WORKSPACE
+    assert lay(2, 4, 6, 128, FAKE, 1 << 30) == native.TXL_ERR_INVALID_ARG    # D differs from the memory's
+    assert lay(2, 1, 6, 128, FAKE, 1 << 30) == native.TXL_ERR_INVALID_ARG
+    assert lay(2, 4, 64, 100, FAKE, 1 << 30) == native.TXL_ERR_ALIGNMENT
+    assert lay(3, 4, 64, 128, FAKE, 1 << 30) == native.TXL_ERR_INVALID_ARG   # memory of B = 2
+    assert (mem.wp, mem.valid) == (0, 0)
     # self-test limits
     assert lib.txl_selftest_wait_timeout(FAKE, 0, None) == native.TXL_ERR_INVALID_ARG
     assert lib.txl_selftest_wait_timeout(None, 10, None) == native.TXL_ERR_INVALID_ARG

@@ -182,6 +182,68 @@ def mem_push(mem: Memory, k_new: torch.Tensor, v_new: torch.Tensor, stream=None)
     return mem
 
 
+def _rows2d(t: torch.Tensor, what: str):
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError("%s must be a 2-D tensor with unit column stride" % what)
+    return t.data_ptr(), t.stride(0)
+
+
+def linear(X: torch.Tensor, W: torch.Tensor, Y: torch.Tensor | None = None,
+           err_flag: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Y = X W for bf16 X [m, k] and W [k, n] (txl_linear); Y [m, n] is allocated if not given."""
+    m, k = X.shape
+    k2, n = W.shape
+    if k2 != k:
+        raise ValueError("inner dimensions differ")
+    if Y is None:
+        Y = torch.empty(m, n, dtype=X.dtype, device=X.device)
+    px, ldx = _rows2d(X, "X")
+    pw, ldw = _rows2d(W, "W")
+    py, ldy = _rows2d(Y, "Y")
+    st = _lib().txl_linear(m, n, k, px, ldx, pw, ldw, py, ldy, dtype_code(X),
+                           err_flag.data_ptr() if err_flag is not None else None, _stream(stream))
+    check(st, "txl_linear")
+    return Y
+
+
+def rel_attn_layer_workspace_size(B: int, L: int, H: int, D: int) -> int:
+    """Bytes of workspace rel_attn_layer needs (txl_rel_attn_layer_workspace_size)."""
+    return int(_lib().txl_rel_attn_layer_workspace_size(B, L, H, D))
+
+
+def rel_attn_layer(h: torch.Tensor, mem: Memory | None, W_qkv: torch.Tensor, W_o: torch.Tensor,
+                   u: torch.Tensor, v_bias: torch.Tensor, r: torch.Tensor, n_rows: int, clamp_len: int,
+                   n_head: int, d_head: int, y: torch.Tensor | None = None, scale: float = 0.0,
+                   workspace: torch.Tensor | None = None, err_flag: torch.Tensor | None = None,
+                   stream=None) -> torch.Tensor:
+    """One attention-layer step over hidden states h [B, L, d_model] (txl_rel_attn_layer): the
+    projections, the relative attention over [memory ++ segment], the output projection, and the
+    push of the segment's keys and values into `mem`.  Returns y [B, L, d_model]."""
+    B, L, d_model = h.shape
+    if h.stride(2) != 1 or (B > 1 and h.stride(0) != L * h.stride(1)):
+        raise ValueError("h must be [B, L, d_model] with rows b*L + t evenly spaced")
+    if u.dtype != torch.float32 or v_bias.dtype != torch.float32:
+        raise TypeError("u and v_bias are fp32 [H, D]")
+    if not (u.is_contiguous() and v_bias.is_contiguous() and W_qkv.is_contiguous() and W_o.is_contiguous()):
+        raise ValueError("u, v_bias, W_qkv and W_o must be contiguous")
+    if y is None:
+        y = torch.empty(B, L, d_model, dtype=h.dtype, device=h.device)
+    if y.stride(2) != 1 or (B > 1 and y.stride(0) != L * y.stride(1)):
+        raise ValueError("y must be [B, L, d_model] with rows b*L + t evenly spaced")
+    need = rel_attn_layer_workspace_size(B, L, n_head, d_head)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=h.device)
+    nbytes = workspace.numel() * workspace.element_size()
+    memc = ctypes.byref(mem.c_struct) if mem is not None else None
+    st = _lib().txl_rel_attn_layer(
+        B, L, n_head, d_head, d_model, int(clamp_len), h.data_ptr(), h.stride(1), memc, W_qkv.data_ptr(),
+        W_o.data_ptr(), u.data_ptr(), v_bias.data_ptr(), r.data_ptr(), r.stride(1), int(n_rows), float(scale),
+        y.data_ptr(), y.stride(1), workspace.data_ptr(), nbytes,
+        err_flag.data_ptr() if err_flag is not None else None, _stream(stream))
+    check(st, "txl_rel_attn_layer")
+    return y
+
+
 def selftest_wait_timeout(err_flag: torch.Tensor, timeout_us: int, stream=None) -> None:
     st = _lib().txl_selftest_wait_timeout(err_flag.data_ptr(), int(timeout_us), _stream(stream))
     check(st, "txl_selftest_wait_timeout")

@@ -6,6 +6,7 @@
 #include <algorithm>
 #include <mutex>
 
+#include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
 #include "txl_internal.h"
@@ -435,6 +436,100 @@ txl_status txl_mem_push(txl_mem* mem, const txl_view* k_new, const txl_view* v_n
     if (launch_mem_push(p, static_cast<cudaStream_t>(stream)) != cudaSuccess) return TXL_ERR_CUDA;
     mem->wp = static_cast<int>((static_cast<int64_t>(mem->wp) + L) % mem->M);
     mem->valid = std::min(mem->valid + L, mem->M);
+    return TXL_OK;
+}
+
+namespace {
+
+// 2D bf16 tensor map over a row-major [rows][ld] matrix, columns 0..cols-1, box (64, box_rows).
+bool encode_rows(CUtensorMap* map, const void* ptr, int64_t cols, int64_t rows, int64_t ld, unsigned box_rows)
+{
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * 2)};
+    const cuuint32_t box[2] = {64, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+txl_status txl_linear(int m, int n, int k, const void* X, int64_t ld_x, const void* W, int64_t ld_w, void* Y,
+                      int64_t ld_y, txl_dtype dtype, int* err_flag, void* stream)
+{
+    if (m < 0 || n < 0 || k <= 0 || !X || !W || !Y) return TXL_ERR_INVALID_ARG;
+    if (ld_x < k || ld_w < n || ld_y < n) return TXL_ERR_INVALID_ARG;
+    if (dtype == TXL_F32) return TXL_ERR_UNSUPPORTED;
+    if (dtype != TXL_BF16) return TXL_ERR_INVALID_ARG;
+    if (m == 0 || n == 0) return TXL_OK;
+    if (!a16(X) || !a16(W) || !s16(ld_x, 2) || !s16(ld_w, 2)) return TXL_ERR_ALIGNMENT;
+    if (static_cast<int64_t>(m) + 127 > INT32_MAX || static_cast<int64_t>(n) + 255 > INT32_MAX) return TXL_ERR_INVALID_ARG;
+    if (!encoder_ready()) return TXL_ERR_CUDA;
+    LinearParams p;
+    std::memset(&p, 0, sizeof(p));
+    if (!encode_rows(&p.tm_x, X, k, m, ld_x, 128) || !encode_rows(&p.tm_w, W, n, k, ld_w, 64)) return TXL_ERR_CUDA;
+    p.y = Y;
+    p.ld_y = ld_y;
+    p.m = m;
+    p.n = n;
+    p.k = k;
+    p.tiles_n = (n + 255) / 256;
+    const int64_t tiles = static_cast<int64_t>((m + 127) / 128) * p.tiles_n;
+    if (tiles > INT32_MAX) return TXL_ERR_INVALID_ARG;
+    p.n_tiles = static_cast<int>(tiles);
+    p.k_tiles = (k + 63) / 64;
+    p.vec = (a16(Y) && s16(ld_y, 2)) ? 1 : 0;
+    p.err_flag = err_flag;
+    const int sms = sm_count();
+    if (sms <= 0) return TXL_ERR_CUDA;
+    return launch_linear(p, sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? TXL_OK : TXL_ERR_CUDA;
+}
+
+size_t txl_rel_attn_layer_workspace_size(int B, int L, int H, int D)
+{
+    if (B <= 0 || L <= 0 || H <= 0 || D <= 0) return 0;
+    // q|k|v of the segment [B*L][3*H*D] and the attention output [B*L][H*D], bf16
+    return static_cast<size_t>(B) * L * H * D * 4 * 2;
+}
+
+txl_status txl_rel_attn_layer(int B, int L, int H, int D, int d_model, int clamp_len, const void* h, int64_t ld_h,
+                              txl_mem* mem, const void* W_qkv, const void* W_o, const float* u, const float* v_bias,
+                              const void* r, int64_t ld_r, int n_rows, float scale, void* y, int64_t ld_y,
+                              void* workspace, size_t workspace_bytes, int* err_flag, void* stream)
+{
+    if (B < 0 || L < 0 || H <= 0 || D <= 0 || d_model <= 0 || clamp_len < 0) return TXL_ERR_INVALID_ARG;
+    if (!h || !W_qkv || !W_o || !u || !v_bias || !r || !y) return TXL_ERR_INVALID_ARG;
+    if (ld_h < d_model || ld_y < d_model) return TXL_ERR_INVALID_ARG;
+    if (mem && mem->M > 0 && (mem->B != B || mem->H != H || mem->D != D || mem->dtype != TXL_BF16))
+        return TXL_ERR_INVALID_ARG;
+    const int64_t HD = static_cast<int64_t>(H) * D;
+    if ((HD & 7) || (d_model & 7)) return TXL_ERR_ALIGNMENT;      // 16-byte rows of q|k|v, attn, y
+    if (B == 0 || L == 0) return TXL_OK;
+    const size_t need = txl_rel_attn_layer_workspace_size(B, L, H, D);
+    if (!workspace || workspace_bytes < need) return TXL_ERR_WORKSPACE;
+    if (!a16(workspace)) return TXL_ERR_ALIGNMENT;
+    const int rows = B * L;
+    if (static_cast<int64_t>(B) * L > INT32_MAX) return TXL_ERR_INVALID_ARG;
+    __nv_bfloat16* qkv = static_cast<__nv_bfloat16*>(workspace);
+    __nv_bfloat16* attn = qkv + static_cast<int64_t>(rows) * 3 * HD;
+    // Q = h W_q and the segment's K = h W_k, V = h W_v in one product with [W_q W_k W_v]
+    txl_status st = txl_linear(rows, static_cast<int>(3 * HD), d_model, h, ld_h, W_qkv, 3 * HD, qkv, 3 * HD,
+                               TXL_BF16, err_flag, stream);
+    if (st != TXL_OK) return st;
+    // the attention over [memory ++ segment]: the memory holds the K, V of earlier positions
+    const txl_view q{qkv, L * 3 * HD, 3 * HD, D};
+    const txl_view kc{qkv + HD, L * 3 * HD, 3 * HD, D};
+    const txl_view vc{qkv + 2 * HD, L * 3 * HD, 3 * HD, D};
+    const txl_view out{attn, L * HD, HD, D};
+    st = txl_rel_attn_fwd(B, L, H, D, clamp_len, &q, mem, &kc, &vc, u, v_bias, r, ld_r, n_rows, scale, &out,
+                          TXL_BF16, nullptr, 0, err_flag, stream);
+    if (st != TXL_OK) return st;
+    // y = concat_h(attn) W_o
+    st = txl_linear(rows, d_model, static_cast<int>(HD), attn, HD, W_o, d_model, y, ld_y, TXL_BF16, err_flag, stream);
+    if (st != TXL_OK) return st;
+    // the segment's K, V enter the memory (FIFO)
+    if (mem && mem->M > 0) return txl_mem_push(mem, &kc, &vc, L, stream);
     return TXL_OK;
 }
 

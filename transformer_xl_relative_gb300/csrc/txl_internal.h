@@ -107,6 +107,22 @@ cudaError_t launch_attn_tc(const AttnTcParams& p, cudaStream_t s);
 // d_head <= 64: one persistent CTA per SM (at most sm_count CTAs) over all query tiles
 cudaError_t launch_attn_persist(const AttnTcParams& p, int sm_count, cudaStream_t s);
 
+// ---------------------------------------------------------------- projections (tcgen05 GEMM)
+struct LinearParams {
+    CUtensorMap tm_x;    // X as 2D (k, m): box 64 x 128, 128-byte swizzle
+    CUtensorMap tm_w;    // W as 2D (n, k): box 64 x 64, 128-byte swizzle
+    void* y;             // bf16 [m][ld_y]
+    int64_t ld_y;
+    int m, n, k;
+    int tiles_n;         // ceil(n / 256)
+    int n_tiles;         // ceil(m / 128) * tiles_n
+    int k_tiles;         // ceil(k / 64)
+    int vec;             // Y 16-byte aligned and ld_y a multiple of 8: 16-byte stores
+    int* err_flag;
+};
+
+cudaError_t launch_linear(const LinearParams& p, int sm_count, cudaStream_t s);
+
 // ---------------------------------------------------------------- decode (few queries, split keys)
 constexpr int kDecodeChunk = 256;   // keys per CTA
 constexpr int kDecodeMaxL = 16;     // queries per (b, h) the decode path takes

@@ -19,7 +19,7 @@ EXPORTS = (
     "txl_status_str", "txl_version", "txl_rel_pos_gen", "txl_rel_attn_fwd",
     "txl_rel_attn_workspace_size", "txl_rel_attn_path", "txl_rel_attn_decode",
     "txl_rel_attn_decode_workspace_size", "txl_rel_attn_decode_noalloc", "txl_mem_push",
-    "txl_selftest_wait_timeout",
+    "txl_selftest_wait_timeout", "txl_linear", "txl_rel_attn_layer", "txl_rel_attn_layer_workspace_size",
 )
 
 
@@ -82,6 +82,13 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.txl_mem_push.restype = i
     lib.txl_selftest_wait_timeout.argtypes = [vp, ctypes.c_uint, vp]
     lib.txl_selftest_wait_timeout.restype = i
+    lib.txl_linear.argtypes = [i, i, i, vp, i64, vp, i64, vp, i64, i, vp, vp]
+    lib.txl_linear.restype = i
+    lib.txl_rel_attn_layer.argtypes = [i, i, i, i, i, i, vp, i64, Mp, vp, vp, vp, vp, vp, i64, i, fp,
+                                       vp, i64, vp, ctypes.c_size_t, vp, vp]
+    lib.txl_rel_attn_layer.restype = i
+    lib.txl_rel_attn_layer_workspace_size.argtypes = [i, i, i, i]
+    lib.txl_rel_attn_layer_workspace_size.restype = ctypes.c_size_t
     _lib = lib
     return lib
 

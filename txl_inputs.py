@@ -7,6 +7,8 @@ Distributions (the pages give no dataset for this path; these stand in for one):
   q, k, v  ~ N(0, 1)                     (projected activations)
   u, v_bias ~ N(0, 0.02^2)               ("TransformerXL 相对位置编码" §3.1 and §4.5: randn * 0.02)
   W_R      ~ N(0, 1/d_model) (variance)  (reading of "N(0, 1/d_model)": std d_model^-1/2)
+  layer    : hidden states h ~ N(0, 1); W_q, W_k, W_v ~ N(0, 1/d_model) and W_o ~ N(0, 1/(H*D))
+             (variance), so q, k, v and y come out with unit variance like the inputs above
 Values are drawn on the CPU with ``torch.Generator().manual_seed(seed)`` in fp32 and then cast
 to the compute dtype, so every consumer sees identical bits.
 """
@@ -122,3 +124,23 @@ def make_segment(cfg: Config, s: int):
 def custom(name="custom", B=1, H=2, D=16, d_model=32, L=16, M=16, clamp_len=1000, dtype="bf16",
            seed=7, segments=1, head_stride=0, ld_w=0) -> Config:
     return Config(name, B, H, D, d_model, L, M, clamp_len, dtype, seed, segments, head_stride, ld_w)
+
+
+def make_layer(cfg: Config, segments: int = 1, seed: int | None = None):
+    """Inputs of the attention-layer step: hidden states h [B, segments*L, d_model] and the
+    weights W_qkv [d_model, 3*H*D] (columns W_q | W_k | W_v) and W_o [H*D, d_model], in the
+    compute dtype, plus u, v_bias and W_R as make_params draws them."""
+    gen = torch.Generator().manual_seed(cfg.seed + 20_000 if seed is None else seed)
+    HD = cfg.H * cfg.D
+    h = _randn(gen, (cfg.B, segments * cfg.L, cfg.d_model))
+    W_qkv = _randn(gen, (cfg.d_model, 3 * HD), cfg.d_model ** -0.5)
+    W_o = _randn(gen, (HD, cfg.d_model), HD ** -0.5)
+    u, vb, W_R = make_params(cfg, cfg.seed + 10_000 if seed is None else seed + 1)
+    dt = cfg.torch_dtype
+    return dict(h=h.to(dt), W_qkv=W_qkv.to(dt), W_o=W_o.to(dt), u=u, vb=vb, W_R=W_R)
+
+
+def make_matrix(rows: int, cols: int, seed: int, std: float = 1.0, dtype=torch.bfloat16) -> torch.Tensor:
+    """A [rows, cols] N(0, std^2) matrix in `dtype` (operands of the projection products)."""
+    gen = torch.Generator().manual_seed(seed)
+    return _randn(gen, (rows, cols), std).to(dtype)
