@@ -264,6 +264,77 @@ def bench_decode(txl, device, stream, rank, args):
             "gpu_launches_per_call": 2}
 
 
+def bench_layer(txl, device, stream, rank, args):
+    """The attention-layer step over hidden states (txl_rel_attn_layer) on the large workload:
+    q|k|v projection of the segment (6144 x 3072 x 1024), the fused attention over [memory ++
+    segment], the output projection (6144 x 1024 x 1024) and the push of the segment's K/V, plus
+    the position table, per step.  Eight hidden-state sets (100 MB) rotate with the 25 MB K/V ring,
+    the 50 MB workspace and 8 MB of weights, so a step does not find its inputs L2-warm.  The
+    q|k|v product is also timed alone (same rotation) against the measured bf16 peak."""
+    import torch
+    B, H, D, L, M, C, dm = 16, 16, 64, 384, 384, 1000, 1024
+    HD = H * D
+    dt = torch.bfloat16
+    g = torch.Generator(device=device).manual_seed(rank_seed(777, rank))
+    n_rows = min(M + L, C + 1)
+    W_R = (torch.randn(dm, HD, generator=g, device=device) * dm ** -0.5).to(dt)
+    W_qkv = (torch.randn(dm, 3 * HD, generator=g, device=device) * dm ** -0.5).to(dt)
+    W_o = (torch.randn(HD, dm, generator=g, device=device) * HD ** -0.5).to(dt)
+    u = (0.02 * torch.randn(H, D, generator=g, device=device)).float()
+    vb = (0.02 * torch.randn(H, D, generator=g, device=device)).float()
+    r = torch.empty(n_rows, H, D, dtype=dt, device=device)
+    nsets = 8
+    hs = [torch.randn(B, L, dm, generator=g, device=device).to(dt) for _ in range(nsets)]
+    ys = [torch.empty(B, L, dm, dtype=dt, device=device) for _ in range(2)]
+    mem = txl.Memory.empty(B, M, H, D, device=device)
+    ws = torch.empty(txl.rel_attn_layer_workspace_size(B, L, H, D), dtype=torch.uint8, device=device)
+    qkv = ws[: B * L * 3 * HD * 2].view(dt).view(B * L, 3 * HD)
+
+    def step(i):
+        txl.rel_pos_gen(W_R, r, n_rows, dm, H, D)
+        txl.rel_attn_layer(hs[i], mem, W_qkv, W_o, u, vb, r, n_rows, C, H, D, ys[i & 1], workspace=ws)
+
+    def proj(i):
+        txl.linear(hs[i].view(B * L, dm), W_qkv, qkv)
+
+    def timed(fn, reps=10):
+        with torch.cuda.stream(stream):
+            for i in range(2 * nsets):
+                fn(i % nsets)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for i in range(nsets):
+                fn(i)
+        with torch.cuda.stream(stream):
+            graph.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(reps):
+                graph.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / (nsets * reps)
+
+    t_step = timed(step)
+    t_proj = timed(proj)
+    # every position of the memory is valid once the warm-up has pushed two segments
+    attn = 6 * D * B * H * (L * M + L * (L + 1) // 2)
+    flops = 2 * B * L * dm * 4 * HD + attn + 2 * n_rows * dm * HD
+    pflops = 2.0 * B * L * dm * 3 * HD
+    peak, _, _, kind = _peaks()
+    achieved = pflops / (t_proj * 1e-6) / 1e12
+    return {"workload": "layer: B16 L384 M384 H16 D64 d_model1024 clamp1000 bf16 (hidden states in, y out)",
+            "us_per_step": t_step, "tflops": flops / (t_step * 1e-6) / 1e12,
+            "algorithmic_flops_per_step": flops, "gpu_launches_per_step": 5,
+            "roofline": {"kernel": "txl_linear (linear_kernel, q|k|v 6144x3072x1024)", "bound": "tensor",
+                         "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                         "peak_source": "%s bf16 burst" % kind, "us_per_launch": t_proj,
+                         "algorithmic_flops_per_launch": pflops}}
+
+
 def run_txl(args):
     import torch
 
@@ -418,6 +489,7 @@ def run_txl(args):
     d2h = ho.numel() * ho.element_size()
 
     decode = bench_decode(txl, device, stream, rank, args)
+    layer = bench_layer(txl, device, stream, rank, args)
 
     attn_flops, pos_flops = _flops(cfg)
     step_flops = attn_flops + pos_flops
@@ -453,6 +525,7 @@ def run_txl(args):
                 "ms_per_step": t_e2e_ms},
         "gpu_launches": 3 * steps,
         "decode": decode,
+        "layer": layer,
         "roofline": {"kernel": "txl_rel_attn_fwd (attn_persist_kernel)", "bound": "tensor",
                      "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "peak_source": "%s bf16 burst (MEASURED_PEAKS.json)" % peak_kind

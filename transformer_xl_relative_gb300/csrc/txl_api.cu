@@ -475,11 +475,13 @@ txl_status txl_linear(int m, int n, int k, const void* X, int64_t ld_x, const vo
     p.n = n;
     p.k = k;
     p.tiles_n = (n + 255) / 256;
-    const int64_t tiles = static_cast<int64_t>((m + 127) / 128) * p.tiles_n;
+    p.m_tiles = (m + 127) / 128;
+    const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.tiles_n;
     if (tiles > INT32_MAX) return TXL_ERR_INVALID_ARG;
     p.n_tiles = static_cast<int>(tiles);
     p.k_tiles = (k + 63) / 64;
     p.vec = (a16(Y) && s16(ld_y, 2)) ? 1 : 0;
+    p.tma_store = (p.vec && encode_rows(&p.tm_y, Y, n, m, ld_y, 32)) ? 1 : 0;
     p.err_flag = err_flag;
     const int sms = sm_count();
     if (sms <= 0) return TXL_ERR_CUDA;

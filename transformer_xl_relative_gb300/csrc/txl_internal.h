@@ -111,13 +111,16 @@ cudaError_t launch_attn_persist(const AttnTcParams& p, int sm_count, cudaStream_
 struct LinearParams {
     CUtensorMap tm_x;    // X as 2D (k, m): box 64 x 128, 128-byte swizzle
     CUtensorMap tm_w;    // W as 2D (n, k): box 64 x 64, 128-byte swizzle
+    CUtensorMap tm_y;    // Y as 2D (n, m): box 64 x 32, 128-byte swizzle (when tma_store)
     void* y;             // bf16 [m][ld_y]
     int64_t ld_y;
     int m, n, k;
     int tiles_n;         // ceil(n / 256)
-    int n_tiles;         // ceil(m / 128) * tiles_n
+    int m_tiles;         // ceil(m / 128)
+    int n_tiles;         // m_tiles * tiles_n
     int k_tiles;         // ceil(k / 64)
     int vec;             // Y 16-byte aligned and ld_y a multiple of 8: 16-byte stores
+    int tma_store;       // the same, and tm_y encoded: the epilogue stores tiles by TMA
     int* err_flag;
 };
 
