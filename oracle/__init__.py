@@ -19,4 +19,5 @@ from .oracle import (  # noqa: F401
     rel_layer,
     stream_layer,
     layer_flops,
+    rel_attn_bwd,
 )

@@ -184,6 +184,69 @@ def ring_logical(ring: np.ndarray, wp: int, valid: int) -> np.ndarray:
     return out
 
 
+def rel_attn_bwd(q, k, v, u, vb, W_R, M: int, mem_valid: int, clamp_len: int, dO, scale=None,
+                 bh=None) -> dict:
+    """Gradients of one call of ``rel_attn`` with respect to q, k, v, u, v_bias, the position
+    rows r and W_R, for an upstream gradient dO [B, L, H, D] (chain rule through the four-term
+    score of "Transformer-XL 和相对位置编码" §2.3.2 and the softmax; no gradient is formed for
+    anything the pages put behind stop-gradient: that is the caller's choice of which slices of
+    dk, dv to use).  Plain fp64 linear algebra per (b, h): scores S = scale (q' K^T + BD) with
+    q' = q + u, q'' = q + v_bias and BD[i, j] = q''_i . r[min(M + i - j, C)]; P = softmax over the
+    visible keys; dP = dO V^T; dS = P (dP - rowsum(P dP)) * scale; then
+
+        dq_i = sum_j dS_ij (k_j + r[delta_ij]),   dk_j = sum_i dS_ij q'_i,   dv_j = sum_i P_ij dO_i,
+        du   = sum_{b,i,j} dS_ij k_j,              dv_bias = sum_{b,i,j} dS_ij r[delta_ij],
+        dr[delta] = sum_{b,(i,j): delta_ij = delta} dS_ij q''_i,   dW_R = sum_delta R_delta^T dr[delta].
+
+    The position term is handled through E[i, delta] = sum over keys j with clamped distance delta
+    of dS_ij, a scatter written out with np.add.at.  ``bh``: optional list of (b, h) pairs to
+    evaluate (dq, dk, dv of the others come back NaN; du, dv_bias, dr, dW_R then cover only them).
+    Returns float64 arrays: dq [B,L,H,D], dk, dv [B,M+L,H,D], du, dvb [H,D], dr [n_rows,H,D],
+    dW_R [d_model, H*D]."""
+    q, k, v, u, vb, W, dO = (_f64(x) for x in (q, k, v, u, vb, W_R, dO))
+    B, L, H, D = q.shape
+    T = M + L
+    d_model = W.shape[0]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    n_rows = min(T, clamp_len + 1)
+    r = rel_table(n_rows, d_model, H, D, W)                       # [n_rows, H, D]
+    i_idx = np.arange(L)[:, None]
+    j_idx = np.arange(T)[None, :]
+    delta = M + i_idx - j_idx
+    vis = (j_idx >= M - mem_valid) & (delta >= 0)
+    dcl = np.clip(np.minimum(delta, clamp_len), 0, n_rows - 1)
+    out = {"dq": np.full((B, L, H, D), np.nan), "dk": np.full((B, T, H, D), np.nan),
+           "dv": np.full((B, T, H, D), np.nan), "du": np.zeros((H, D)), "dvb": np.zeros((H, D)),
+           "dr": np.zeros((n_rows, H, D))}
+    pairs = bh if bh is not None else [(b, h) for b in range(B) for h in range(H)]
+    for b, h in pairs:
+        qp = q[b, :, h] + u[h]
+        qpp = q[b, :, h] + vb[h]
+        K, V, rh, g = k[b, :, h], v[b, :, h], r[:, h], dO[b, :, h]
+        G = qpp @ rh.T                                              # [L, n_rows]
+        S = scale * (qp @ K.T + np.take_along_axis(G, dcl, axis=1))
+        S = np.where(vis, S, -np.inf)
+        P = np.exp(S - S.max(axis=1, keepdims=True))
+        P /= P.sum(axis=1, keepdims=True)
+        dP = g @ V.T
+        dS = scale * P * (dP - (P * dP).sum(axis=1, keepdims=True))
+        dS = np.where(vis, dS, 0.0)
+        E = np.zeros((L, n_rows))
+        np.add.at(E, (np.broadcast_to(i_idx, dcl.shape), dcl), dS)
+        dq_ac = dS @ K
+        dq_bd = E @ rh
+        out["dq"][b, :, h] = dq_ac + dq_bd
+        out["dk"][b, :, h] = dS.T @ qp
+        out["dv"][b, :, h] = P.T @ g
+        out["du"][h] += dq_ac.sum(axis=0)
+        out["dvb"][h] += dq_bd.sum(axis=0)
+        out["dr"][:, h] += E.T @ qpp
+    Rm = np.stack([sinusoid(float(dd), d_model) for dd in range(n_rows)])     # [n_rows, d_model]
+    out["dW_R"] = Rm.T @ out["dr"].reshape(n_rows, H * D)
+    return out
+
+
 def linear(X, W) -> np.ndarray:
     """Y = X W in fp64 (a library matmul as the step): q_proj / k_proj / v_proj / o_proj of
     "TransformerXL 相对位置编码" §3.1, linear maps without bias."""
