@@ -255,6 +255,45 @@ txl_status txl_rel_attn_layer(int B, int L, int H, int D, int d_model, int clamp
 /* Bytes of device workspace txl_rel_attn_layer needs: B*L*H*D*8 (0 for an empty shape). */
 size_t txl_rel_attn_layer_workspace_size(int B, int L, int H, int D);
 
+/*
+ * txl_rel_attn_bwd -- gradients of one txl_rel_attn_fwd call for an upstream gradient d_out,
+ * by the chain rule through the four-term score ("Transformer-XL 和相对位置编码" §2.3.2) and the
+ * softmax: with q' = q + u, q'' = q + v_bias, P the attention weights and dS_ij =
+ * scale P_ij (d_out_i . v_j - d_out_i . out_i),
+ *   dq_i  = sum_j dS_ij (k_j + r[delta_ij])        dk_j = sum_i dS_ij q'_i      dv_j = sum_i P_ij d_out_i
+ *   du    = sum dS_ij k_j     dv_bias = sum dS_ij r[delta_ij]     dr[delta] = sum_{delta_ij = delta} dS_ij q''_i
+ * The memory's keys and values get no gradient: the memory is the stop-gradient part of the
+ * extended sequence ("Transformer-XL 和相对位置编码" §2.3.1); dk_cur, dv_cur cover the current
+ * segment's keys.  Arguments as txl_rel_attn_fwd, plus
+ *   out    : the forward call's output (view, dtype);  d_out : upstream gradient (view, dtype).
+ *   dq, dk_cur, dv_cur : device fp32 [B][L][H][D] (dense);  du, dv_bias : device fp32 [H][D];
+ *   dr     : device fp32 [n_rows][H][D], every row written (rows no pair reaches are zero).
+ *   workspace : device, >= txl_rel_attn_bwd_workspace_size(B, L, H, D) bytes, 16-byte aligned.
+ * All arithmetic in fp32 (scores recomputed, P never stored).  Enqueues several launches.
+ */
+txl_status txl_rel_attn_bwd(int B, int L, int H, int D, int clamp_len,
+                            const txl_view* q, const txl_mem* mem,
+                            const txl_view* k_cur, const txl_view* v_cur,
+                            const float* u, const float* v_bias,
+                            const void* r, int64_t ld_r, int n_rows, float scale,
+                            const txl_view* out, const txl_view* d_out,
+                            float* dq, float* dk_cur, float* dv_cur, float* du, float* dv_bias,
+                            float* dr, txl_dtype dtype, void* workspace, size_t workspace_bytes,
+                            void* stream);
+
+/* Bytes of device workspace txl_rel_attn_bwd needs: B*L*H*(2 + 2*D)*4 (0 for an empty shape). */
+size_t txl_rel_attn_bwd_workspace_size(int B, int L, int H, int D);
+
+/*
+ * txl_rel_pos_bwd -- gradient of W_R from the gradient of the position rows:
+ *   dW_R[m][h*d_head + d] = sum_delta R_delta[m] * dr[delta][h][d]
+ * with R_delta the interleaved sinusoid of txl_rel_pos_gen (evaluated in double precision and
+ * rounded to fp32).  dr: device fp32 [n_rows][H][D] (as txl_rel_attn_bwd writes it);
+ * dW_R: device fp32 [d_model][ld_dw], columns 0..H*D-1 written.  d_model even, ld_dw >= H*D.
+ */
+txl_status txl_rel_pos_bwd(int n_rows, int d_model, int n_head, int d_head, const float* dr,
+                           float* dW_R, int64_t ld_dw, void* stream);
+
 /* Self-test of the bounded waits used by every kernel: launches one CTA that waits on an
  * mbarrier nothing will signal, gives up after timeout_us microseconds (1 .. 10^7), writes
  * TXL_ERR_TIMEOUT to the device int err_flag and returns.  The context stays usable. */

@@ -1,0 +1,99 @@
+"""GPU parity of the backward (txl_rel_attn_bwd, txl_rel_pos_bwd) against the fp64 backward oracle
+(itself pinned against finite differences of the forward oracle).
+
+The GPU recomputes the scores in fp32 from the same inputs and takes D_i = d_out_i . out_i from
+the forward output it is given (here the library's own forward, rounded to the compute dtype),
+while the oracle uses the exact fp64 attention.  The rounding of out (half an ulp: 2^-9 relative in
+bf16, 2^-24 in fp32) enters every dS_ij of the row through D_i, so gradients are compared with a
+tolerance relative to their largest entry: 2e-2 for bf16 inputs, 1e-4 for fp32."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import txl_inputs
+from gpu_common import ld_r_for, to_dev
+
+pytestmark = pytest.mark.gpu
+RTOL = {"bf16": 2e-2, "f32": 1e-4}
+
+
+@pytest.fixture(scope="module")
+def txl():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    import transformer_xl_relative_gb300 as m
+    return m
+
+
+def _close(got, ref, tol, what):
+    got = np.asarray(got, dtype=np.float64)
+    scale = max(np.max(np.abs(ref)), 1e-30)
+    err = np.max(np.abs(got - ref)) if ref.size else 0.0
+    assert np.isfinite(got).all(), what
+    assert err <= tol * scale, (what, err, scale)
+
+
+BWD = [
+    # B, H, D, d_model, L, M, valid, wp, C, dtype, head_stride
+    (1, 2, 16, 32, 8, 8, 8, 0, 1000, "f32", 0),          # tiny fp32, full memory
+    (2, 2, 64, 128, 64, 64, 40, 0, 1000, "bf16", 0),     # partly valid memory
+    (1, 2, 32, 64, 40, 30, 30, 7, 20, "bf16", 0),        # ring with an unaligned write pointer, clamp inside
+    (2, 3, 41, 82, 24, 0, 0, 0, 10, "bf16", 48),         # no memory, clamp, padded heads
+    (2, 4, 64, 128, 128, 128, 128, 0, 1000, "bf16", 0),  # a full 128-key tile on each side
+]
+
+
+@pytest.mark.parametrize("shape", BWD, ids=["B%dH%dD%d_L%dM%dv%dwp%dC%d_%s" % (s[0], s[1], s[2], s[4], s[5], s[6], s[7], s[8], s[9])
+                                            for s in BWD])
+def test_backward_matches_oracle(txl, shape):
+    B, H, D, dm, L, M, valid, wp, C, dtype, hs = shape
+    cfg = txl_inputs.custom(B=B, H=H, D=D, d_model=dm, L=L, M=M, clamp_len=C, dtype=dtype, seed=500 + L + M, head_stride=hs)
+    case = txl_inputs.make_case(cfg)
+    dO = txl_inputs.make_qkv(cfg, seed=900 + L, L=L, T=1)[0]                    # [B, L, H, D] upstream gradient
+    q, k, v = (to_dev(case[n], cfg.hs) for n in ("q", "k", "v"))
+    g_dev = to_dev(dO, cfg.hs)
+    dt = cfg.torch_dtype
+    n_rows = min(M + L, C + 1)
+    r = torch.empty(n_rows, H, ld_r_for(D), dtype=dt, device="cuda")
+    txl.rel_pos_gen(case["W_R"].cuda(), r, n_rows, dm, H, D)
+    mem = None
+    if M > 0:
+        store_k = to_dev(torch.zeros_like(case["k"][:, :M]), cfg.hs)
+        store_v = to_dev(torch.zeros_like(case["v"][:, :M]), cfg.hs)
+        slots = (wp + torch.arange(M)) % M
+        store_k[:, slots] = k[:, :M]
+        store_v[:, slots] = v[:, :M]
+        mem = txl.Memory(store_k, store_v, wp, valid)
+    u, vb = case["u"].cuda(), case["vb"].cuda()
+    out = to_dev(torch.zeros_like(case["q"]), cfg.hs)
+    txl.rel_attn_fwd(q, mem, k[:, M:], v[:, M:], u, vb, r, n_rows, C, out)
+    g = txl.rel_attn_bwd(q, mem, k[:, M:], v[:, M:], u, vb, r, n_rows, C, out, g_dev)
+    dW = txl.rel_pos_bwd(g["dr"], dm)
+    torch.cuda.synchronize()
+    ref = oracle.rel_attn_bwd(case["q"], case["k"], case["v"], case["u"], case["vb"], case["W_R"][:, :H * D], M, valid,
+                              C, dO)
+    tol = RTOL[dtype]
+    _close(g["dq"].cpu().numpy(), ref["dq"], tol, "dq")
+    _close(g["dk_cur"].cpu().numpy(), ref["dk"][:, M:], tol, "dk")
+    _close(g["dv_cur"].cpu().numpy(), ref["dv"][:, M:], tol, "dv")
+    _close(g["du"].cpu().numpy(), ref["du"], tol, "du")
+    _close(g["dv_bias"].cpu().numpy(), ref["dvb"], tol, "dv_bias")
+    _close(g["dr"].cpu().numpy(), ref["dr"], tol, "dr")
+    _close(dW.cpu().numpy(), ref["dW_R"], tol, "dW_R")
+
+
+def test_pos_backward_closed_form(txl):
+    """dW_R for a one-hot dr: row delta of dr selects the sinusoid R_delta (column h*D + d)."""
+    n_rows, dm, H, D = 50, 64, 2, 8
+    dr = torch.zeros(n_rows, H, D, dtype=torch.float32, device="cuda")
+    dr[37, 1, 5] = 1.0
+    dr[3, 0, 0] = -2.0
+    dW = txl.rel_pos_bwd(dr, dm)
+    torch.cuda.synchronize()
+    ref = np.zeros((dm, H * D))
+    ref[:, 1 * D + 5] = oracle.sinusoid(37.0, dm)
+    ref[:, 0] = -2.0 * oracle.sinusoid(3.0, dm)
+    assert np.max(np.abs(dW.cpu().numpy() - ref)) <= 1e-6

@@ -9,12 +9,14 @@ from .api import (  # noqa: F401
     Memory,
     linear,
     mem_push,
+    rel_attn_bwd,
     rel_attn_decode,
     rel_attn_decode_workspace_size,
     rel_attn_fwd,
     rel_attn_layer,
     rel_attn_layer_workspace_size,
     rel_attn_path,
+    rel_pos_bwd,
     rel_pos_gen,
     selftest_wait_timeout,
     version,

@@ -244,6 +244,46 @@ def rel_attn_layer(h: torch.Tensor, mem: Memory | None, W_qkv: torch.Tensor, W_o
     return y
 
 
+def rel_attn_bwd(q: torch.Tensor, mem: Memory | None, k_cur: torch.Tensor, v_cur: torch.Tensor,
+                 u: torch.Tensor, v_bias: torch.Tensor, r: torch.Tensor, n_rows: int, clamp_len: int,
+                 out: torch.Tensor, d_out: torch.Tensor, scale: float = 0.0,
+                 workspace: torch.Tensor | None = None, stream=None) -> dict:
+    """Gradients of one rel_attn_fwd call for the upstream gradient d_out (txl_rel_attn_bwd).
+    Returns fp32 tensors dq, dk_cur, dv_cur [B, L, H, D], du, dv_bias [H, D], dr [n_rows, H, D]."""
+    (B, L, H, D), memc, vq, vk, vv, vo = _attn_args(q, mem, k_cur, v_cur, r, out)
+    vg = view(d_out)
+    if u.dtype != torch.float32 or v_bias.dtype != torch.float32:
+        raise TypeError("u and v_bias are fp32 [H, D]")
+    f32 = dict(dtype=torch.float32, device=q.device)
+    g = {"dq": torch.empty(B, L, H, D, **f32), "dk_cur": torch.empty(B, L, H, D, **f32),
+         "dv_cur": torch.empty(B, L, H, D, **f32), "du": torch.empty(H, D, **f32),
+         "dv_bias": torch.empty(H, D, **f32), "dr": torch.empty(n_rows, H, D, **f32)}
+    need = int(_lib().txl_rel_attn_bwd_workspace_size(B, L, H, D))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    st = _lib().txl_rel_attn_bwd(
+        B, L, H, D, int(clamp_len), ctypes.byref(vq), memc, ctypes.byref(vk), ctypes.byref(vv),
+        u.data_ptr(), v_bias.data_ptr(), r.data_ptr(), r.stride(1), int(n_rows), float(scale),
+        ctypes.byref(vo), ctypes.byref(vg), g["dq"].data_ptr(), g["dk_cur"].data_ptr(), g["dv_cur"].data_ptr(),
+        g["du"].data_ptr(), g["dv_bias"].data_ptr(), g["dr"].data_ptr(), dtype_code(q), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    check(st, "txl_rel_attn_bwd")
+    return g
+
+
+def rel_pos_bwd(dr: torch.Tensor, d_model: int, dW_R: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """dW_R [d_model, H*D] = sum_delta R_delta^T dr[delta] for fp32 dr [n_rows, H, D] (txl_rel_pos_bwd)."""
+    n_rows, H, D = dr.shape
+    if not dr.is_contiguous() or dr.dtype != torch.float32:
+        raise ValueError("dr must be a contiguous fp32 [n_rows, H, D] tensor")
+    if dW_R is None:
+        dW_R = torch.empty(d_model, H * D, dtype=torch.float32, device=dr.device)
+    st = _lib().txl_rel_pos_bwd(n_rows, d_model, H, D, dr.data_ptr(), dW_R.data_ptr(), dW_R.stride(0),
+                                _stream(stream))
+    check(st, "txl_rel_pos_bwd")
+    return dW_R
+
+
 def selftest_wait_timeout(err_flag: torch.Tensor, timeout_us: int, stream=None) -> None:
     st = _lib().txl_selftest_wait_timeout(err_flag.data_ptr(), int(timeout_us), _stream(stream))
     check(st, "txl_selftest_wait_timeout")

@@ -535,6 +535,76 @@ txl_status txl_rel_attn_layer(int B, int L, int H, int D, int d_model, int clamp
     return TXL_OK;
 }
 
+size_t txl_rel_attn_bwd_workspace_size(int B, int L, int H, int D)
+{
+    if (B <= 0 || L <= 0 || H <= 0 || D <= 0) return 0;
+    const size_t rows = static_cast<size_t>(B) * L * H;
+    return rows * 2 * sizeof(float) + rows * D * 2 * sizeof(float);
+}
+
+txl_status txl_rel_attn_bwd(int B, int L, int H, int D, int clamp_len, const txl_view* q, const txl_mem* mem,
+                            const txl_view* k_cur, const txl_view* v_cur, const float* u, const float* v_bias,
+                            const void* r, int64_t ld_r, int n_rows, float scale, const txl_view* out,
+                            const txl_view* d_out, float* dq, float* dk_cur, float* dv_cur, float* du,
+                            float* dv_bias, float* dr, txl_dtype dtype, void* workspace, size_t workspace_bytes,
+                            void* stream)
+{
+    txl_status st = check_attn(B, L, H, D, q, mem, k_cur, v_cur, r, ld_r, out, dtype);
+    if (st != TXL_OK) return st;
+    if (clamp_len < 0 || !u || !v_bias || !view_ok(d_out)) return TXL_ERR_INVALID_ARG;
+    if (!dq || !dk_cur || !dv_cur || !du || !dv_bias || !dr) return TXL_ERR_INVALID_ARG;
+    const int M = (mem && mem->M > 0) ? mem->M : 0;
+    const int valid = M > 0 ? mem->valid : 0;
+    const int need_rows = std::min(M + L, clamp_len + 1);
+    if (n_rows < need_rows) return TXL_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (B == 0 || L == 0) {
+        // no query: every gradient is zero
+        const size_t hd = static_cast<size_t>(H) * D * sizeof(float);
+        if (cudaMemsetAsync(du, 0, hd, s) != cudaSuccess || cudaMemsetAsync(dv_bias, 0, hd, s) != cudaSuccess ||
+            cudaMemsetAsync(dr, 0, hd * n_rows, s) != cudaSuccess)
+            return TXL_ERR_CUDA;
+        return TXL_OK;
+    }
+    const size_t need = txl_rel_attn_bwd_workspace_size(B, L, H, D);
+    if (!workspace || workspace_bytes < need) return TXL_ERR_WORKSPACE;
+    if (!a16(workspace)) return TXL_ERR_ALIGNMENT;
+    if (scale <= 0.f) scale = 1.0f / std::sqrt(static_cast<float>(D));
+    BwdParams p;
+    std::memset(&p, 0, sizeof(p));
+    AttnSimtParams& a = p.a;
+    a.q = q->ptr; a.q_sb = q->stride_b; a.q_st = q->stride_t; a.q_sh = q->stride_h;
+    if (M > 0) {
+        a.kmem = mem->k; a.vmem = mem->v;
+        a.m_sb = mem->stride_b; a.m_st = mem->stride_t; a.m_sh = mem->stride_h;
+    }
+    a.kcur = k_cur->ptr; a.kc_sb = k_cur->stride_b; a.kc_st = k_cur->stride_t; a.kc_sh = k_cur->stride_h;
+    a.vcur = v_cur->ptr; a.vc_sb = v_cur->stride_b; a.vc_st = v_cur->stride_t; a.vc_sh = v_cur->stride_h;
+    a.out = out->ptr; a.o_sb = out->stride_b; a.o_st = out->stride_t; a.o_sh = out->stride_h;
+    a.u = u; a.vb = v_bias;
+    a.r = r; a.r_row = static_cast<int64_t>(H) * ld_r; a.r_head = ld_r;
+    a.B = B; a.L = L; a.H = H; a.D = D; a.M = M; a.lo = M - valid; a.wp = M > 0 ? mem->wp : 0; a.C = clamp_len;
+    a.scale = scale;
+    p.dout = d_out->ptr; p.g_sb = d_out->stride_b; p.g_st = d_out->stride_t; p.g_sh = d_out->stride_h;
+    p.dq = dq; p.dk = dk_cur; p.dv = dv_cur; p.du = du; p.dvb = dv_bias; p.dr = dr; p.n_rows = n_rows;
+    const size_t rows = static_cast<size_t>(B) * L * H;
+    float* ws = static_cast<float*>(workspace);
+    p.lse = ws;
+    p.dd = ws + rows;
+    p.pac = ws + 2 * rows;
+    p.pbd = ws + 2 * rows + rows * D;
+    return launch_rel_attn_bwd(p, dtype, s) == cudaSuccess ? TXL_OK : TXL_ERR_CUDA;
+}
+
+txl_status txl_rel_pos_bwd(int n_rows, int d_model, int n_head, int d_head, const float* dr, float* dW_R,
+                           int64_t ld_dw, void* stream)
+{
+    if (n_rows < 0 || d_model < 2 || (d_model & 1) || n_head <= 0 || d_head <= 0) return TXL_ERR_INVALID_ARG;
+    if (!dW_R || (n_rows > 0 && !dr) || ld_dw < static_cast<int64_t>(n_head) * d_head) return TXL_ERR_INVALID_ARG;
+    PosBwdParams p{dr, dW_R, ld_dw, n_rows, d_model, n_head, d_head};
+    return launch_pos_bwd(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? TXL_OK : TXL_ERR_CUDA;
+}
+
 txl_status txl_selftest_wait_timeout(int* err_flag, unsigned timeout_us, void* stream)
 {
     if (!err_flag || timeout_us == 0 || timeout_us > 10000000u) return TXL_ERR_INVALID_ARG;

@@ -107,6 +107,26 @@ cudaError_t launch_attn_tc(const AttnTcParams& p, cudaStream_t s);
 // d_head <= 64: one persistent CTA per SM (at most sm_count CTAs) over all query tiles
 cudaError_t launch_attn_persist(const AttnTcParams& p, int sm_count, cudaStream_t s);
 
+// ---------------------------------------------------------------- backward (SIMT)
+struct BwdParams {
+    AttnSimtParams a;                           // the forward call's inputs and its output (a.out)
+    const void* dout; int64_t g_sb, g_st, g_sh; // upstream gradient, the inputs' dtype
+    float* dq; float* dk; float* dv;            // [B][L][H][D] (dk, dv: the current segment's keys)
+    float* du; float* dvb;                      // [H][D]
+    float* dr; int n_rows;                      // [n_rows][H][D]
+    float* lse; float* dd;                      // workspace [B][L][H]: log-sum-exp, dO . out
+    float* pac; float* pbd;                     // workspace [B][L][H][D]: per-query parts of du, dv_bias
+};
+
+struct PosBwdParams {
+    const float* dr;                            // [n_rows][H*D]
+    float* dW; int64_t ld_dw;                   // [d_model][ld_dw]
+    int n_rows, d_model, H, D;
+};
+
+cudaError_t launch_rel_attn_bwd(const BwdParams& p, txl_dtype dtype, cudaStream_t s);
+cudaError_t launch_pos_bwd(const PosBwdParams& p, cudaStream_t s);
+
 // ---------------------------------------------------------------- projections (tcgen05 GEMM)
 struct LinearParams {
     CUtensorMap tm_x;    // X as 2D (k, m): box 64 x 128, 128-byte swizzle
