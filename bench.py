@@ -335,6 +335,65 @@ def bench_layer(txl, device, stream, rank, args):
                          "algorithmic_flops_per_launch": pflops}}
 
 
+def bench_backward(txl, device, stream, rank, args):
+    """Gradients of one fused-attention call on the large workload (txl_rel_attn_bwd + the position
+    table's txl_rel_pos_bwd): every score recomputed in fp32 on the CUDA cores.  Algorithmic flops
+    per visible (query, key) pair: 16 D (scores 4 D, dP 2 D, dq 4 D, dk 2 D, dv 2 D, dr 2 D), plus
+    2 n_rows d_model H D for dW_R; reported against the fp32 FMA peak of the SMs (152 SMs x 128
+    lanes x 2 flops x the measured maximum SM clock)."""
+    import torch
+    B, H, D, L, M, C, dm = 16, 16, 64, 384, 384, 1000, 1024
+    dt = torch.bfloat16
+    g = torch.Generator(device=device).manual_seed(rank_seed(31337, rank))
+    n_rows = min(M + L, C + 1)
+    W = (torch.randn(dm, H * D, generator=g, device=device) * dm ** -0.5).to(dt)
+    r = torch.empty(n_rows, H, D, dtype=dt, device=device)
+    txl.rel_pos_gen(W, r, n_rows, dm, H, D)
+    u = (0.02 * torch.randn(H, D, generator=g, device=device)).float()
+    vb = (0.02 * torch.randn(H, D, generator=g, device=device)).float()
+    q = torch.randn(B, L, H, D, generator=g, device=device).to(dt)
+    k = torch.randn(B, M + L, H, D, generator=g, device=device).to(dt)
+    v = torch.randn(B, M + L, H, D, generator=g, device=device).to(dt)
+    dO = torch.randn(B, L, H, D, generator=g, device=device).to(dt)
+    out = torch.empty(B, L, H, D, dtype=dt, device=device)
+    mem = txl.Memory(k[:, :M], v[:, :M], 0, M)
+    txl.rel_attn_fwd(q, mem, k[:, M:], v[:, M:], u, vb, r, n_rows, C, out)
+    ws = torch.empty(16 * 1024 * 1024 * 8, dtype=torch.uint8, device=device)
+    res = {}
+
+    def call():
+        res["g"] = txl.rel_attn_bwd(q, mem, k[:, M:], v[:, M:], u, vb, r, n_rows, C, out, dO, workspace=ws)
+        res["dW"] = txl.rel_pos_bwd(res["g"]["dr"], dm)
+
+    with torch.cuda.stream(stream):
+        call()
+    torch.cuda.synchronize()
+    reps = 3
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            call()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    t_us = e0.elapsed_time(e1) * 1e3 / reps
+    pairs = B * H * (L * M + L * (L + 1) // 2)
+    flops = 16 * D * pairs + 2 * n_rows * dm * H * D
+    sm_mhz = 2070.0
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            sm_mhz = float(json.load(f).get("sm_max_mhz", sm_mhz))
+    except Exception:
+        pass
+    fp32_peak = 152 * 128 * 2 * sm_mhz * 1e6 / 1e12
+    achieved = flops / (t_us * 1e-6) / 1e12
+    return {"workload": "backward: B16 H16 D64 d_model1024 L384 M384 clamp1000, bf16 inputs, fp32 gradients",
+            "us_per_call": t_us, "algorithmic_flops_per_call": flops,
+            "roofline": {"bound": "alu", "achieved": achieved, "peak": fp32_peak, "unit": "TFLOP/s",
+                         "frac": achieved / fp32_peak,
+                         "peak_source": "fp32 FMA: 152 SMs x 128 lanes x 2 flops x %.0f MHz" % sm_mhz}}
+
+
 def run_txl(args):
     import torch
 
@@ -490,6 +549,7 @@ def run_txl(args):
 
     decode = bench_decode(txl, device, stream, rank, args)
     layer = bench_layer(txl, device, stream, rank, args)
+    backward = bench_backward(txl, device, stream, rank, args)
 
     attn_flops, pos_flops = _flops(cfg)
     step_flops = attn_flops + pos_flops
@@ -526,6 +586,7 @@ def run_txl(args):
         "gpu_launches": 3 * steps,
         "decode": decode,
         "layer": layer,
+        "backward": backward,
         "roofline": {"kernel": "txl_rel_attn_fwd (attn_persist_kernel)", "bound": "tensor",
                      "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "peak_source": "%s bf16 burst (MEASURED_PEAKS.json)" % peak_kind
