@@ -43,6 +43,7 @@ BWD = [
     (1, 2, 32, 64, 40, 30, 30, 7, 20, "bf16", 0),        # ring with an unaligned write pointer, clamp inside
     (2, 3, 41, 82, 24, 0, 0, 0, 10, "bf16", 48),         # no memory, clamp, padded heads
     (2, 4, 64, 128, 128, 128, 128, 0, 1000, "bf16", 0),  # a full 128-key tile on each side
+    (1, 2, 128, 128, 30, 33, 20, 5, 40, "bf16", 0),      # D = 128, ring, clamp, L not a multiple of 4
 ]
 
 

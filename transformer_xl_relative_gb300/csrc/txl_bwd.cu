@@ -28,6 +28,7 @@ namespace txl {
 namespace {
 
 constexpr int kBwdWarps = 4;
+constexpr int kG = 4;          // queries, keys or distances per warp: neighbours share operand rows
 
 template <typename T> __device__ __forceinline__ float ldf(const T* p);
 template <> __device__ __forceinline__ float ldf<float>(const float* p) { return __ldg(p); }
@@ -40,12 +41,46 @@ __device__ __forceinline__ float warp_sum(float x)
     return x;
 }
 
+// Warp-wide sums of 2^LOG values at once, left in every lane.  A transposing butterfly halves the
+// values each lane carries per exchange (xor 16, 8, ... : lane l ends with value index taken from
+// its high bits), plain exchanges finish the sums, and one shuffle per value broadcasts it:
+// for 8 values 4 + 2 + 1 + 2 + 8 = 17 shuffles instead of 8 x 5 = 40.
+template <int LOG>
+__device__ __forceinline__ void warp_sums(float* v, int lane)
+{
+    constexpr int N = 1 << LOG;
+    float w[N];
+#pragma unroll
+    for (int k = 0; k < N; ++k) w[k] = v[k];
+    int n = N;
+#pragma unroll
+    for (int r = 0; r < LOG; ++r) {
+        const int bit = 16 >> r;                       // lane bit of this exchange
+        const bool hi = lane & bit;
+        n >>= 1;
+#pragma unroll
+        for (int m = 0; m < N / 2; ++m) {
+            if (m < n) {
+                const float keep = hi ? w[m + n] : w[m];
+                const float send = hi ? w[m] : w[m + n];
+                w[m] = keep + __shfl_xor_sync(0xffffffffu, send, bit);
+            }
+        }
+    }
+#pragma unroll
+    for (int bit = 16 >> LOG; bit > 0; bit >>= 1) w[0] += __shfl_xor_sync(0xffffffffu, w[0], bit);
+    // lane l now holds the sum of value k = (l >> (5 - LOG)); broadcast each
+#pragma unroll
+    for (int k = 0; k < N; ++k) v[k] = __shfl_sync(0xffffffffu, w[0], k << (5 - LOG));
+}
+
 // Key j (logical, 0 <= j < M + L) of (b, h): the memory ring for j < M, the current segment after.
 template <typename T>
 __device__ __forceinline__ void key_ptrs(const AttnSimtParams& a, int b, int h, int j, const T*& kp, const T*& vp)
 {
     if (j < a.M) {
-        const int slot = static_cast<int>((static_cast<int64_t>(a.wp) + j) % a.M);
+        int slot = a.wp + j;                              // wp < M and j < M: one subtraction wraps it
+        if (slot >= a.M) slot -= a.M;
         const int64_t off = b * a.m_sb + slot * a.m_st + h * a.m_sh;
         kp = static_cast<const T*>(a.kmem) + off;
         vp = static_cast<const T*>(a.vmem) + off;
@@ -56,13 +91,23 @@ __device__ __forceinline__ void key_ptrs(const AttnSimtParams& a, int b, int h, 
     }
 }
 
+template <typename T, int DC>
+__device__ __forceinline__ void load_vec(const T* p, int D, int lane, float* x)
+{
+#pragma unroll
+    for (int c = 0; c < DC; ++c) {
+        const int d = lane + 32 * c;
+        x[c] = d < D ? ldf(p + d) : 0.f;
+    }
+}
+
 // Query i of (b, h): q' = q + u and q'' = q + v_bias in the lane's dimensions.
-template <typename T>
+template <typename T, int DC>
 __device__ __forceinline__ void load_query(const AttnSimtParams& a, int b, int h, int i, int lane, float* qu, float* qv)
 {
     const T* q = static_cast<const T*>(a.q) + b * a.q_sb + i * a.q_st + h * a.q_sh;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < DC; ++c) {
         const int d = lane + 32 * c;
         float x = 0.f, uu = 0.f, vv = 0.f;
         if (d < a.D) {
@@ -76,200 +121,427 @@ __device__ __forceinline__ void load_query(const AttnSimtParams& a, int b, int h
 }
 
 template <typename T>
-__device__ __forceinline__ void load_vec(const T* p, int D, int lane, float* x)
-{
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        const int d = lane + 32 * c;
-        x[c] = d < D ? ldf(p + d) : 0.f;
-    }
-}
-
-// scale * (q' . k + q'' . r) for the (query, key) pair, reduced over the warp.
-template <typename T>
-__device__ __forceinline__ float score(const AttnSimtParams& a, const float* qu, const float* qv, const T* kp,
-                                       const T* rp, int lane, float* kx, float* rx)
-{
-    float part = 0.f;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        const int d = lane + 32 * c;
-        kx[c] = d < a.D ? ldf(kp + d) : 0.f;
-        rx[c] = d < a.D ? ldf(rp + d) : 0.f;
-        part = fmaf(qu[c], kx[c], fmaf(qv[c], rx[c], part));
-    }
-    return warp_sum(part) * a.scale;
-}
-
-template <typename T>
 __device__ __forceinline__ const T* rrow(const AttnSimtParams& a, int h, int delta)
 {
-    const int dc = delta < a.C ? delta : a.C;
+    const int dc = delta < 0 ? 0 : (delta < a.C ? delta : a.C);       // negative: a masked pair
     return static_cast<const T*>(a.r) + dc * a.r_row + h * a.r_head;
 }
 
-// ---------------------------------------------------------------------------- rows: dq, lse, D
 template <typename T>
+__device__ __forceinline__ const T* gout(const BwdParams& p, int b, int h, int i)
+{
+    return static_cast<const T*>(p.dout) + b * p.g_sb + i * p.g_st + h * p.g_sh;
+}
+
+__device__ __forceinline__ int64_t qrow(const AttnSimtParams& a, int b, int i, int h)
+{
+    return (static_cast<int64_t>(b) * a.L + i) * a.H + h;                // [B][L][H] row
+}
+
+// ---------------------------------------------------------------------------- rows: dq, lse, D
+// Warp = kG consecutive queries i0 + g of one (b, h).  Keys are visited in increasing order; the
+// position row of query g at key j + 1 is the row query g - 1 used at key j, so each key costs
+// one new r row (for g = 0), its k row, and (second pass) its v row.
+template <typename T, int DC>
 __global__ void __launch_bounds__(32 * kBwdWarps) bwd_rows_kernel(const BwdParams p)
 {
     const AttnSimtParams& a = p.a;
     const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
-    if (gw >= static_cast<int64_t>(a.B) * a.H * a.L) return;
-    const int i = static_cast<int>(gw % a.L);
-    const int h = static_cast<int>((gw / a.L) % a.H);
-    const int b = static_cast<int>(gw / (static_cast<int64_t>(a.L) * a.H));
-    float qu[4], qv[4], g[4], o[4], kx[4], rx[4], vx[4];
-    load_query<T>(a, b, h, i, lane, qu, qv);
-    load_vec(static_cast<const T*>(p.dout) + b * p.g_sb + i * p.g_st + h * p.g_sh, a.D, lane, g);
-    load_vec(static_cast<const T*>(a.out) + b * a.o_sb + i * a.o_st + h * a.o_sh, a.D, lane, o);
-    float dd = 0.f;
+    const int nq = (a.L + kG - 1) / kG;
+    if (gw >= static_cast<int64_t>(a.B) * a.H * nq) return;
+    const int i0 = static_cast<int>(gw % nq) * kG;
+    const int h = static_cast<int>((gw / nq) % a.H);
+    const int b = static_cast<int>(gw / (static_cast<int64_t>(nq) * a.H));
+    float qu[kG][DC], qv[kG][DC], go[kG][DC], dd[kG];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) dd = fmaf(g[c], o[c], dd);
-    dd = warp_sum(dd);
-    const int qpos = a.M + i;
-    // pass 1: log-sum-exp of the visible scores (online)
-    float m = -INFINITY, l = 0.f;
-    for (int j = a.lo; j <= qpos; ++j) {
-        const T *kp, *vp;
-        key_ptrs<T>(a, b, h, j, kp, vp);
-        const float s = score<T>(a, qu, qv, kp, rrow<T>(a, h, qpos - j), lane, kx, rx);
-        const float mn = fmaxf(m, s);
-        l = l * expf(m - mn) + expf(s - mn);
-        m = mn;
+    for (int g = 0; g < kG; ++g) {
+        const int i = min(i0 + g, a.L - 1);               // rows past L repeat the last (not stored)
+        load_query<T, DC>(a, b, h, i, lane, qu[g], qv[g]);
+        float o[DC];
+        load_vec<T, DC>(gout<T>(p, b, h, i), a.D, lane, go[g]);
+        load_vec<T, DC>(static_cast<const T*>(a.out) + b * a.o_sb + i * a.o_st + h * a.o_sh, a.D, lane, o);
+        float x = 0.f;
+#pragma unroll
+        for (int c = 0; c < DC; ++c) x = fmaf(go[g][c], o[c], x);
+        dd[g] = warp_sum(x);
     }
-    const float lse = m + logf(l);
-    // pass 2: dS and dq
-    float dac[4] = {0.f, 0.f, 0.f, 0.f}, dbd[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int j = a.lo; j <= qpos; ++j) {
-        const T *kp, *vp;
-        key_ptrs<T>(a, b, h, j, kp, vp);
-        const float s = score<T>(a, qu, qv, kp, rrow<T>(a, h, qpos - j), lane, kx, rx);
-        load_vec(vp, a.D, lane, vx);
-        float dp = 0.f;
+    const int j_end = a.M + min(i0 + kG - 1, a.L - 1);  // the last query's diagonal
+    float lse[kG];
+    {
+        float m[kG], l[kG], rx[kG][DC];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) dp = fmaf(g[c], vx[c], dp);
-        dp = warp_sum(dp);
-        const float ds = a.scale * expf(s - lse) * (dp - dd);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            dac[c] = fmaf(ds, kx[c], dac[c]);
-            dbd[c] = fmaf(ds, rx[c], dbd[c]);
+        for (int g = 0; g < kG; ++g) {
+            m[g] = -INFINITY;
+            l[g] = 0.f;
+            load_vec<T, DC>(rrow<T>(a, h, a.M + i0 + g - a.lo), a.D, lane, rx[g]);
         }
-    }
-    const int64_t row = (static_cast<int64_t>(b) * a.L + i) * a.H + h;     // [B][L][H] row of D
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        const int d = lane + 32 * c;
-        if (d < a.D) {
-            p.dq[row * a.D + d] = dac[c] + dbd[c];
-            p.pac[row * a.D + d] = dac[c];
-            p.pbd[row * a.D + d] = dbd[c];
+        // software pipeline: the next key's k row and the next r row are requested before the
+        // current key's arithmetic
+        float kn[DC], rn[DC];
+        {
+            const T *kp, *vp;
+            key_ptrs<T>(a, b, h, a.lo, kp, vp);
+            load_vec<T, DC>(kp, a.D, lane, kn);
         }
+        for (int j = a.lo; j <= j_end; ++j) {
+            float kx[DC];
+#pragma unroll
+            for (int c = 0; c < DC; ++c) kx[c] = kn[c];
+            if (j < j_end) {
+                const T *kp, *vp;
+                key_ptrs<T>(a, b, h, j + 1, kp, vp);
+                load_vec<T, DC>(kp, a.D, lane, kn);
+            }
+            load_vec<T, DC>(rrow<T>(a, h, a.M + i0 - j - 1), a.D, lane, rn);
+            float part[kG];
+#pragma unroll
+            for (int g = 0; g < kG; ++g) {
+                float x = 0.f;
+#pragma unroll
+                for (int c = 0; c < DC; ++c) x = fmaf(qu[g][c], kx[c], fmaf(qv[g][c], rx[g][c], x));
+                part[g] = x;
+            }
+            warp_sums<2>(part, lane);
+#pragma unroll
+            for (int g = 0; g < kG; ++g) {
+                if (j <= a.M + i0 + g) {                  // visible to query g
+                    const float s = part[g] * a.scale;
+                    const float mn = fmaxf(m[g], s);
+                    l[g] = l[g] * __expf(m[g] - mn) + __expf(s - mn);
+                    m[g] = mn;
+                }
+            }
+            // next key: query g takes query g-1's row, query 0 its next (smaller) distance
+#pragma unroll
+            for (int g = kG - 1; g > 0; --g)
+#pragma unroll
+                for (int c = 0; c < DC; ++c) rx[g][c] = rx[g - 1][c];
+#pragma unroll
+            for (int c = 0; c < DC; ++c) rx[0][c] = rn[c];
+        }
+#pragma unroll
+        for (int g = 0; g < kG; ++g) lse[g] = m[g] + __logf(l[g]);
     }
-    if (lane == 0) {
-        p.lse[row] = lse;
-        p.dd[row] = dd;
+    float dac[kG][DC], dbd[kG][DC], rx[kG][DC];
+#pragma unroll
+    for (int g = 0; g < kG; ++g) {
+#pragma unroll
+        for (int c = 0; c < DC; ++c) dac[g][c] = dbd[g][c] = 0.f;
+        load_vec<T, DC>(rrow<T>(a, h, a.M + i0 + g - a.lo), a.D, lane, rx[g]);
+    }
+    float kn[DC], vn[DC], rn[DC];
+    {
+        const T *kp, *vp;
+        key_ptrs<T>(a, b, h, a.lo, kp, vp);
+        load_vec<T, DC>(kp, a.D, lane, kn);
+        load_vec<T, DC>(vp, a.D, lane, vn);
+    }
+    for (int j = a.lo; j <= j_end; ++j) {
+        float kx[DC], vx[DC];
+#pragma unroll
+        for (int c = 0; c < DC; ++c) {
+            kx[c] = kn[c];
+            vx[c] = vn[c];
+        }
+        if (j < j_end) {
+            const T *kp, *vp;
+            key_ptrs<T>(a, b, h, j + 1, kp, vp);
+            load_vec<T, DC>(kp, a.D, lane, kn);
+            load_vec<T, DC>(vp, a.D, lane, vn);
+        }
+        load_vec<T, DC>(rrow<T>(a, h, a.M + i0 - j - 1), a.D, lane, rn);
+        float part[kG], dp[kG];
+#pragma unroll
+        for (int g = 0; g < kG; ++g) {
+            float x = 0.f, y = 0.f;
+#pragma unroll
+            for (int c = 0; c < DC; ++c) {
+                x = fmaf(qu[g][c], kx[c], fmaf(qv[g][c], rx[g][c], x));
+                y = fmaf(go[g][c], vx[c], y);
+            }
+            part[g] = x;
+            dp[g] = y;
+        }
+        {
+            float both[2 * kG];
+#pragma unroll
+            for (int g = 0; g < kG; ++g) {
+                both[g] = part[g];
+                both[kG + g] = dp[g];
+            }
+            warp_sums<3>(both, lane);
+#pragma unroll
+            for (int g = 0; g < kG; ++g) {
+                part[g] = both[g];
+                dp[g] = both[kG + g];
+            }
+        }
+#pragma unroll
+        for (int g = 0; g < kG; ++g) {
+            const float ds = (j <= a.M + i0 + g) ? a.scale * __expf(part[g] * a.scale - lse[g]) * (dp[g] - dd[g]) : 0.f;
+#pragma unroll
+            for (int c = 0; c < DC; ++c) {
+                dac[g][c] = fmaf(ds, kx[c], dac[g][c]);
+                dbd[g][c] = fmaf(ds, rx[g][c], dbd[g][c]);
+            }
+        }
+#pragma unroll
+        for (int g = kG - 1; g > 0; --g)
+#pragma unroll
+            for (int c = 0; c < DC; ++c) rx[g][c] = rx[g - 1][c];
+#pragma unroll
+        for (int c = 0; c < DC; ++c) rx[0][c] = rn[c];
+    }
+#pragma unroll
+    for (int g = 0; g < kG; ++g) {
+        const int i = i0 + g;
+        if (i >= a.L) break;
+        const int64_t row = qrow(a, b, i, h);
+#pragma unroll
+        for (int c = 0; c < DC; ++c) {
+            const int d = lane + 32 * c;
+            if (d < a.D) {
+                p.dq[row * a.D + d] = dac[g][c] + dbd[g][c];
+                p.pac[row * a.D + d] = dac[g][c];
+                p.pbd[row * a.D + d] = dbd[g][c];
+            }
+        }
+        if (lane == 0) {
+            p.lse[row] = lse[g];
+            p.dd[row] = dd[g];
+        }
     }
 }
 
 // ---------------------------------------------------------------------------- keys: dk, dv
-template <typename T>
+// Warp = kG consecutive keys jc0 + g of the current segment of one (b, h).  Queries are visited
+// in increasing order (query i sees key jc iff i >= jc); key g's position row at query i + 1 is
+// key g - 1's row at query i, so each query costs its q and dO rows and one new r row.
+template <typename T, int DC>
 __global__ void __launch_bounds__(32 * kBwdWarps) bwd_keys_kernel(const BwdParams p)
 {
     const AttnSimtParams& a = p.a;
     const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
-    if (gw >= static_cast<int64_t>(a.B) * a.H * a.L) return;
-    const int jc = static_cast<int>(gw % a.L);                 // key of the current segment
-    const int h = static_cast<int>((gw / a.L) % a.H);
-    const int b = static_cast<int>(gw / (static_cast<int64_t>(a.L) * a.H));
-    const T *kp, *vp;
-    key_ptrs<T>(a, b, h, a.M + jc, kp, vp);
-    float kx[4], vx[4], qu[4], qv[4], g[4], rx[4];
-    load_vec(kp, a.D, lane, kx);
-    load_vec(vp, a.D, lane, vx);
-    float dk[4] = {0.f, 0.f, 0.f, 0.f}, dv[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int i = jc; i < a.L; ++i) {                            // queries that see key M + jc
-        load_query<T>(a, b, h, i, lane, qu, qv);
-        load_vec(static_cast<const T*>(p.dout) + b * p.g_sb + i * p.g_st + h * p.g_sh, a.D, lane, g);
-        load_vec(rrow<T>(a, h, i - jc), a.D, lane, rx);
-        float part = 0.f, dp = 0.f;
+    const int nk = (a.L + kG - 1) / kG;
+    if (gw >= static_cast<int64_t>(a.B) * a.H * nk) return;
+    const int jc0 = static_cast<int>(gw % nk) * kG;
+    const int h = static_cast<int>((gw / nk) % a.H);
+    const int b = static_cast<int>(gw / (static_cast<int64_t>(nk) * a.H));
+    float kx[kG][DC], vx[kG][DC], dk[kG][DC], dv[kG][DC], rx[kG][DC];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            part = fmaf(qu[c], kx[c], fmaf(qv[c], rx[c], part));
-            dp = fmaf(g[c], vx[c], dp);
+    for (int g = 0; g < kG; ++g) {
+        const T *kp, *vp;
+        key_ptrs<T>(a, b, h, a.M + min(jc0 + g, a.L - 1), kp, vp);
+        load_vec<T, DC>(kp, a.D, lane, kx[g]);
+        load_vec<T, DC>(vp, a.D, lane, vx[g]);
+#pragma unroll
+        for (int c = 0; c < DC; ++c) dk[g][c] = dv[g][c] = 0.f;
+        load_vec<T, DC>(rrow<T>(a, h, -g), a.D, lane, rx[g]);        // distance at query jc0
+    }
+    // software pipeline: the next query's rows and r row are requested before this query's arithmetic
+    float qun[DC], qvn[DC], gon[DC], rn[DC], lsen, ddn;
+    load_query<T, DC>(a, b, h, jc0, lane, qun, qvn);
+    load_vec<T, DC>(gout<T>(p, b, h, jc0), a.D, lane, gon);
+    lsen = p.lse[qrow(a, b, jc0, h)];
+    ddn = p.dd[qrow(a, b, jc0, h)];
+    for (int i = jc0; i < a.L; ++i) {
+        float qu[DC], qv[DC], go[DC];
+#pragma unroll
+        for (int c = 0; c < DC; ++c) {
+            qu[c] = qun[c];
+            qv[c] = qvn[c];
+            go[c] = gon[c];
         }
-        part = warp_sum(part);
-        dp = warp_sum(dp);
-        const int64_t row = (static_cast<int64_t>(b) * a.L + i) * a.H + h;
-        const float pr = expf(part * a.scale - p.lse[row]);
-        const float ds = a.scale * pr * (dp - p.dd[row]);
+        const float lse = lsen, ddi = ddn;
+        if (i + 1 < a.L) {
+            load_query<T, DC>(a, b, h, i + 1, lane, qun, qvn);
+            load_vec<T, DC>(gout<T>(p, b, h, i + 1), a.D, lane, gon);
+            lsen = p.lse[qrow(a, b, i + 1, h)];
+            ddn = p.dd[qrow(a, b, i + 1, h)];
+        }
+        load_vec<T, DC>(rrow<T>(a, h, i + 1 - jc0), a.D, lane, rn);
+        float part[kG], dp[kG];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            dk[c] = fmaf(ds, qu[c], dk[c]);
-            dv[c] = fmaf(pr, g[c], dv[c]);
+        for (int g = 0; g < kG; ++g) {
+            float x = 0.f, y = 0.f;
+#pragma unroll
+            for (int c = 0; c < DC; ++c) {
+                x = fmaf(qu[c], kx[g][c], fmaf(qv[c], rx[g][c], x));
+                y = fmaf(go[c], vx[g][c], y);
+            }
+            part[g] = x;
+            dp[g] = y;
+        }
+        {
+            float both[2 * kG];
+#pragma unroll
+            for (int g = 0; g < kG; ++g) {
+                both[g] = part[g];
+                both[kG + g] = dp[g];
+            }
+            warp_sums<3>(both, lane);
+#pragma unroll
+            for (int g = 0; g < kG; ++g) {
+                part[g] = both[g];
+                dp[g] = both[kG + g];
+            }
+        }
+#pragma unroll
+        for (int g = 0; g < kG; ++g) {
+            const bool vis = i >= jc0 + g;
+            const float pr = vis ? __expf(part[g] * a.scale - lse) : 0.f;
+            const float ds = a.scale * pr * (dp[g] - ddi);
+#pragma unroll
+            for (int c = 0; c < DC; ++c) {
+                dk[g][c] = fmaf(ds, qu[c], dk[g][c]);
+                dv[g][c] = fmaf(pr, go[c], dv[g][c]);
+            }
+        }
+#pragma unroll
+        for (int g = kG - 1; g > 0; --g)
+#pragma unroll
+            for (int c = 0; c < DC; ++c) rx[g][c] = rx[g - 1][c];
+#pragma unroll
+        for (int c = 0; c < DC; ++c) rx[0][c] = rn[c];
+    }
+#pragma unroll
+    for (int g = 0; g < kG; ++g) {
+        const int jc = jc0 + g;
+        if (jc >= a.L) break;
+        const int64_t row = qrow(a, b, jc, h);
+#pragma unroll
+        for (int c = 0; c < DC; ++c) {
+            const int d = lane + 32 * c;
+            if (d < a.D) {
+                p.dk[row * a.D + d] = dk[g][c];
+                p.dv[row * a.D + d] = dv[g][c];
+            }
         }
     }
-    const int64_t row = (static_cast<int64_t>(b) * a.L + jc) * a.H + h;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        const int d = lane + 32 * c;
-        if (d < a.D) {
-            p.dk[row * a.D + d] = dk[c];
-            p.dv[row * a.D + d] = dv[c];
-        }
-    }
-}
-
-// dS_ij of one visible (query, key) pair, with q''_i of the query left in qv.
-template <typename T>
-__device__ __forceinline__ float pair_ds(const BwdParams& p, int b, int h, int i, int j, int lane, float* qv)
-{
-    const AttnSimtParams& a = p.a;
-    float qu[4], g[4], kx[4], rx[4], vx[4];
-    load_query<T>(a, b, h, i, lane, qu, qv);
-    const T *kp, *vp;
-    key_ptrs<T>(a, b, h, j, kp, vp);
-    const float s = score<T>(a, qu, qv, kp, rrow<T>(a, h, a.M + i - j), lane, kx, rx);
-    load_vec(static_cast<const T*>(p.dout) + b * p.g_sb + i * p.g_st + h * p.g_sh, a.D, lane, g);
-    load_vec(vp, a.D, lane, vx);
-    float dp = 0.f;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) dp = fmaf(g[c], vx[c], dp);
-    dp = warp_sum(dp);
-    const int64_t row = (static_cast<int64_t>(b) * a.L + i) * a.H + h;
-    return a.scale * expf(s - p.lse[row]) * (dp - p.dd[row]);
 }
 
 // ---------------------------------------------------------------------------- distances below the clamp
-template <typename T>
+// Warp = kG consecutive distances delta0 + g of one head; over every (b, i), distance g pairs query
+// i with key M + i - delta0 - g.  Key g at query i + 1 is key g - 1 at query i, so each query costs
+// its q and dO rows and one new k, v row.
+template <typename T, int DC>
 __global__ void __launch_bounds__(32 * kBwdWarps) bwd_dist_kernel(const BwdParams p, int n_exact)
 {
     const AttnSimtParams& a = p.a;
     const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
-    if (gw >= static_cast<int64_t>(a.H) * n_exact) return;
-    const int delta = static_cast<int>(gw % n_exact);
-    const int h = static_cast<int>(gw / n_exact);
-    float acc[4] = {0.f, 0.f, 0.f, 0.f}, qv[4];
-    for (int b = 0; b < a.B; ++b)
-        for (int i = 0; i < a.L; ++i) {
-            const int j = a.M + i - delta;
-            if (j < a.lo) continue;                       // before the valid memory (or the sequence)
-            const float ds = pair_ds<T>(p, b, h, i, j, lane, qv);
+    const int nd = (n_exact + kG - 1) / kG;
+    if (gw >= static_cast<int64_t>(a.H) * nd) return;
+    const int d0 = static_cast<int>(gw % nd) * kG;
+    const int h = static_cast<int>(gw / nd);
+    float rx[kG][DC], acc[kG][DC];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) acc[c] = fmaf(ds, qv[c], acc[c]);
+    for (int g = 0; g < kG; ++g) {
+        load_vec<T, DC>(rrow<T>(a, h, min(d0 + g, n_exact - 1)), a.D, lane, rx[g]);
+#pragma unroll
+        for (int c = 0; c < DC; ++c) acc[g][c] = 0.f;
+    }
+    // queries with at least one of the warp's keys visible: M + i - d0 >= lo
+    const int i_start = max(0, a.lo + d0 - a.M);
+    for (int b = 0; b < a.B; ++b) {
+        float kx[kG][DC], vx[kG][DC];
+#pragma unroll
+        for (int g = 0; g < kG; ++g) {
+            const int j = a.M + i_start - d0 - g;
+            const T *kp, *vp;
+            key_ptrs<T>(a, b, h, max(j, 0), kp, vp);
+            load_vec<T, DC>(kp, a.D, lane, kx[g]);
+            load_vec<T, DC>(vp, a.D, lane, vx[g]);
         }
+        if (i_start >= a.L) continue;
+        float qun[DC], qvn[DC], gon[DC], knx[DC], vnx[DC], lsen, ddn;
+        load_query<T, DC>(a, b, h, i_start, lane, qun, qvn);
+        load_vec<T, DC>(gout<T>(p, b, h, i_start), a.D, lane, gon);
+        lsen = p.lse[qrow(a, b, i_start, h)];
+        ddn = p.dd[qrow(a, b, i_start, h)];
+        for (int i = i_start; i < a.L; ++i) {
+            float qu[DC], qv[DC], go[DC];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        const int d = lane + 32 * c;
-        if (d < a.D) p.dr[(static_cast<int64_t>(delta) * a.H + h) * a.D + d] = acc[c];
+            for (int c = 0; c < DC; ++c) {
+                qu[c] = qun[c];
+                qv[c] = qvn[c];
+                go[c] = gon[c];
+            }
+            const float lse = lsen, ddi = ddn;
+            if (i + 1 < a.L) {                               // the next query's rows and its new key
+                load_query<T, DC>(a, b, h, i + 1, lane, qun, qvn);
+                load_vec<T, DC>(gout<T>(p, b, h, i + 1), a.D, lane, gon);
+                lsen = p.lse[qrow(a, b, i + 1, h)];
+                ddn = p.dd[qrow(a, b, i + 1, h)];
+                const T *kp, *vp;
+                key_ptrs<T>(a, b, h, max(a.M + i + 1 - d0, 0), kp, vp);
+                load_vec<T, DC>(kp, a.D, lane, knx);
+                load_vec<T, DC>(vp, a.D, lane, vnx);
+            }
+            float part[kG], dp[kG];
+#pragma unroll
+            for (int g = 0; g < kG; ++g) {
+                float x = 0.f, y = 0.f;
+#pragma unroll
+                for (int c = 0; c < DC; ++c) {
+                    x = fmaf(qu[c], kx[g][c], fmaf(qv[c], rx[g][c], x));
+                    y = fmaf(go[c], vx[g][c], y);
+                }
+                part[g] = x;
+                dp[g] = y;
+            }
+            {
+                float both[2 * kG];
+#pragma unroll
+                for (int g = 0; g < kG; ++g) {
+                    both[g] = part[g];
+                    both[kG + g] = dp[g];
+                }
+                warp_sums<3>(both, lane);
+#pragma unroll
+                for (int g = 0; g < kG; ++g) {
+                    part[g] = both[g];
+                    dp[g] = both[kG + g];
+                }
+            }
+#pragma unroll
+            for (int g = 0; g < kG; ++g) {
+                const bool vis = (d0 + g < n_exact) && (a.M + i - d0 - g >= a.lo);
+                const float ds = vis ? a.scale * __expf(part[g] * a.scale - lse) * (dp[g] - ddi) : 0.f;
+#pragma unroll
+                for (int c = 0; c < DC; ++c) acc[g][c] = fmaf(ds, qv[c], acc[g][c]);
+            }
+#pragma unroll
+            for (int g = kG - 1; g > 0; --g)
+#pragma unroll
+                for (int c = 0; c < DC; ++c) {
+                    kx[g][c] = kx[g - 1][c];
+                    vx[g][c] = vx[g - 1][c];
+                }
+#pragma unroll
+            for (int c = 0; c < DC; ++c) {
+                kx[0][c] = knx[c];
+                vx[0][c] = vnx[c];
+            }
+        }
+    }
+#pragma unroll
+    for (int g = 0; g < kG; ++g) {
+        const int delta = d0 + g;
+        if (delta >= n_exact) break;
+#pragma unroll
+        for (int c = 0; c < DC; ++c) {
+            const int d = lane + 32 * c;
+            if (d < a.D) p.dr[(static_cast<int64_t>(delta) * a.H + h) * a.D + d] = acc[g][c];
+        }
     }
 }
 
 // ---------------------------------------------------------------------------- distances at the clamp
-template <typename T>
+// Warp per (b, h, i): the keys j <= M + i - C all use r[C]; their dS q''_i is added into dr[C].
+template <typename T, int DC>
 __global__ void __launch_bounds__(32 * kBwdWarps) bwd_clamp_kernel(const BwdParams p)
 {
     const AttnSimtParams& a = p.a;
@@ -281,49 +553,88 @@ __global__ void __launch_bounds__(32 * kBwdWarps) bwd_clamp_kernel(const BwdPara
     const int b = static_cast<int>(gw / (static_cast<int64_t>(a.L) * a.H));
     const int j_hi = a.M + i - a.C;                       // keys at distance >= clamp_len
     if (j_hi < a.lo) return;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f}, qv[4];
-    for (int j = a.lo; j <= j_hi; ++j) {
-        const float ds = pair_ds<T>(p, b, h, i, j, lane, qv);
+    float qu[DC], qv[DC], go[DC], rx[DC], acc[DC];
+    load_query<T, DC>(a, b, h, i, lane, qu, qv);
+    load_vec<T, DC>(gout<T>(p, b, h, i), a.D, lane, go);
+    load_vec<T, DC>(rrow<T>(a, h, a.C), a.D, lane, rx);
+    const int64_t row = qrow(a, b, i, h);
+    const float lse = p.lse[row], ddi = p.dd[row];
+    float bd = 0.f;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) acc[c] = fmaf(ds, qv[c], acc[c]);
+    for (int c = 0; c < DC; ++c) {
+        bd = fmaf(qv[c], rx[c], bd);
+        acc[c] = 0.f;
+    }
+    bd = warp_sum(bd);                                    // the position term is the same for all these keys
+    float dssum = 0.f;
+    for (int j = a.lo; j <= j_hi; ++j) {
+        const T *kp, *vp;
+        key_ptrs<T>(a, b, h, j, kp, vp);
+        float kx[DC], vx[DC];
+        load_vec<T, DC>(kp, a.D, lane, kx);
+        load_vec<T, DC>(vp, a.D, lane, vx);
+        float x = 0.f, y = 0.f;
+#pragma unroll
+        for (int c = 0; c < DC; ++c) {
+            x = fmaf(qu[c], kx[c], x);
+            y = fmaf(go[c], vx[c], y);
+        }
+        x = warp_sum(x);
+        y = warp_sum(y);
+        dssum += a.scale * __expf((x + bd) * a.scale - lse) * (y - ddi);
     }
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < DC; ++c) {
         const int d = lane + 32 * c;
-        if (d < a.D) atomicAdd(p.dr + (static_cast<int64_t>(a.C) * a.H + h) * a.D + d, acc[c]);
+        if (d < a.D) atomicAdd(p.dr + (static_cast<int64_t>(a.C) * a.H + h) * a.D + d, dssum * qv[c]);
     }
 }
 
 // ---------------------------------------------------------------------------- du, dv_bias
-__global__ void bwd_bias_kernel(const BwdParams p)
+// Grid (column blocks of 128 (h, d), row chunks): each thread sums its column over one chunk of the
+// B*L per-query rows and adds the partial sums into du, dv_bias (zeroed before).
+constexpr int kBiasRowsPerChunk = 96;
+
+__global__ void bwd_bias_kernel(const BwdParams p, int64_t chunk)
 {
     const AttnSimtParams& a = p.a;
     const int hd = blockIdx.x * blockDim.x + threadIdx.x;
     const int HD = a.H * a.D;
     if (hd >= HD) return;
-    float su = 0.f, sv = 0.f;
     const int64_t rows = static_cast<int64_t>(a.B) * a.L;
-    for (int64_t r = 0; r < rows; ++r) {
+    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * chunk;
+    const int64_t r1 = r0 + chunk < rows ? r0 + chunk : rows;
+    float su = 0.f, sv = 0.f;
+    for (int64_t r = r0; r < r1; ++r) {
         su += p.pac[r * HD + hd];
         sv += p.pbd[r * HD + hd];
     }
-    p.du[hd] = su;
-    p.dvb[hd] = sv;
+    atomicAdd(p.du + hd, su);
+    atomicAdd(p.dvb + hd, sv);
 }
 
 // ---------------------------------------------------------------------------- dW_R = R^T dr
-// Block (64 model columns m, 64 columns n = h*D + d); the sinusoid rows R_delta[m] of a chunk of
-// 32 distances are evaluated in double precision and rounded to fp32 (as the fp32 forward does).
+// Block (64 model columns m, 64 columns n = h*D + d), 256 threads with 4 x 4 outputs each.  The
+// block's 64 frequencies are computed once in double precision; an element R_delta[m] reduces the
+// angle delta * w modulo 2 pi in double precision and evaluates the fp32 sine or cosine of the
+// reduced angle (within an ulp or two of the double-precision value rounded to fp32).
 constexpr int kPosBwdT = 64, kPosBwdChunk = 32;
 
 __global__ void __launch_bounds__(256) pos_bwd_kernel(PosBwdParams p)
 {
     __shared__ float Rs[kPosBwdChunk][kPosBwdT + 1];
     __shared__ float Gs[kPosBwdChunk][kPosBwdT + 1];
+    __shared__ double Ws[kPosBwdT];
     const int m0 = blockIdx.y * kPosBwdT, n0 = blockIdx.x * kPosBwdT;
     const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;      // 16 x 16 threads, 4 x 4 outputs each
+    if (threadIdx.x < kPosBwdT) {
+        const int k = (m0 + threadIdx.x) >> 1;
+        Ws[threadIdx.x] = pow(10000.0, -(2.0 * k) / static_cast<double>(p.d_model));
+    }
+    __syncthreads();
     float acc[4][4] = {};
     const int HD = p.H * p.D;
+    constexpr double kTwoPi = 6.283185307179586476925;
     for (int d0 = 0; d0 < p.n_rows; d0 += kPosBwdChunk) {
         for (int e = threadIdx.x; e < kPosBwdChunk * kPosBwdT; e += blockDim.x) {
             const int rr = e / kPosBwdT, cc = e % kPosBwdT;
@@ -331,10 +642,9 @@ __global__ void __launch_bounds__(256) pos_bwd_kernel(PosBwdParams p)
             float rv = 0.f, gv = 0.f;
             if (delta < p.n_rows) {
                 if (m < p.d_model) {
-                    const int k = m >> 1;
-                    const double w = pow(10000.0, -(2.0 * k) / static_cast<double>(p.d_model));
-                    const double x = static_cast<double>(delta) * w;
-                    rv = static_cast<float>((m & 1) ? cos(x) : sin(x));
+                    const double x = static_cast<double>(delta) * Ws[cc];
+                    const float red = static_cast<float>(x - rint(x / kTwoPi) * kTwoPi);
+                    rv = (m & 1) ? cosf(red) : sinf(red);
                 }
                 if (n < HD) gv = p.dr[static_cast<int64_t>(delta) * HD + n];
             }
@@ -366,27 +676,41 @@ __global__ void __launch_bounds__(256) pos_bwd_kernel(PosBwdParams p)
         }
 }
 
-template <typename T>
+template <typename T, int DC>
 cudaError_t launch_all(const BwdParams& p, cudaStream_t s)
 {
     const AttnSimtParams& a = p.a;
-    const int64_t row_warps = static_cast<int64_t>(a.B) * a.H * a.L;
-    const int64_t row_blocks = (row_warps + kBwdWarps - 1) / kBwdWarps;
-    if (row_blocks > 0x7fffffffll) return cudaErrorInvalidValue;
     const int thr = 32 * kBwdWarps;
+    auto blocks = [](int64_t warps) { return (warps + kBwdWarps - 1) / kBwdWarps; };
+    const int64_t grp = static_cast<int64_t>(a.B) * a.H * ((a.L + kG - 1) / kG);
+    const int64_t row_warps = static_cast<int64_t>(a.B) * a.H * a.L;
+    if (blocks(row_warps) > 0x7fffffffll) return cudaErrorInvalidValue;
     const int n_need = (a.M + a.L < a.C + 1) ? a.M + a.L : a.C + 1;
     const bool clamped = a.C < a.M + a.L - 1;
     const int n_exact = clamped ? a.C : n_need;
     cudaError_t e = cudaMemsetAsync(p.dr, 0, static_cast<size_t>(p.n_rows) * a.H * a.D * sizeof(float), s);
     if (e != cudaSuccess) return e;
-    bwd_rows_kernel<T><<<static_cast<unsigned>(row_blocks), thr, 0, s>>>(p);
-    bwd_keys_kernel<T><<<static_cast<unsigned>(row_blocks), thr, 0, s>>>(p);
-    const int64_t dist_blocks = (static_cast<int64_t>(a.H) * n_exact + kBwdWarps - 1) / kBwdWarps;
-    if (dist_blocks > 0) bwd_dist_kernel<T><<<static_cast<unsigned>(dist_blocks), thr, 0, s>>>(p, n_exact);
-    if (clamped) bwd_clamp_kernel<T><<<static_cast<unsigned>(row_blocks), thr, 0, s>>>(p);
+    bwd_rows_kernel<T, DC><<<static_cast<unsigned>(blocks(grp)), thr, 0, s>>>(p);
+    bwd_keys_kernel<T, DC><<<static_cast<unsigned>(blocks(grp)), thr, 0, s>>>(p);
+    const int64_t dist_warps = static_cast<int64_t>(a.H) * ((n_exact + kG - 1) / kG);
+    if (n_exact > 0) bwd_dist_kernel<T, DC><<<static_cast<unsigned>(blocks(dist_warps)), thr, 0, s>>>(p, n_exact);
+    if (clamped) bwd_clamp_kernel<T, DC><<<static_cast<unsigned>(blocks(row_warps)), thr, 0, s>>>(p);
     const int HD = a.H * a.D;
-    bwd_bias_kernel<<<(HD + 127) / 128, 128, 0, s>>>(p);
+    const int64_t rows = static_cast<int64_t>(a.B) * a.L;
+    int64_t chunk = kBiasRowsPerChunk;
+    if ((rows + chunk - 1) / chunk > 65535) chunk = (rows + 65534) / 65535;
+    const int64_t chunks = (rows + chunk - 1) / chunk;
+    e = cudaMemsetAsync(p.du, 0, sizeof(float) * HD, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(p.dvb, 0, sizeof(float) * HD, s);
+    if (e != cudaSuccess) return e;
+    bwd_bias_kernel<<<dim3((HD + 127) / 128, static_cast<unsigned>(chunks)), 128, 0, s>>>(p, chunk);
     return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_t(const BwdParams& p, cudaStream_t s)
+{
+    return p.a.D <= 64 ? launch_all<T, 2>(p, s) : launch_all<T, 4>(p, s);
 }
 
 }  // namespace
@@ -394,7 +718,7 @@ cudaError_t launch_all(const BwdParams& p, cudaStream_t s)
 cudaError_t launch_rel_attn_bwd(const BwdParams& p, txl_dtype dtype, cudaStream_t s)
 {
     if (static_cast<int64_t>(p.a.B) * p.a.H * p.a.L == 0) return cudaSuccess;
-    return dtype == TXL_F32 ? launch_all<float>(p, s) : launch_all<__nv_bfloat16>(p, s);
+    return dtype == TXL_F32 ? launch_t<float>(p, s) : launch_t<__nv_bfloat16>(p, s);
 }
 
 cudaError_t launch_pos_bwd(const PosBwdParams& p, cudaStream_t s)
