@@ -20,4 +20,5 @@ from .oracle import (  # noqa: F401
     stream_layer,
     layer_flops,
     rel_attn_bwd,
+    table_attn,
 )

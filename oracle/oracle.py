@@ -247,6 +247,37 @@ def rel_attn_bwd(q, k, v, u, vb, W_R, M: int, mem_valid: int, clamp_len: int, dO
     return out
 
 
+def table_attn(q, k, v, u, vb, r_table, max_len: int, key_mask=None, scale=None) -> np.ndarray:
+    """The learned-table variant of "TransformerXL 相对位置编码" §3.1 (bidirectional, no memory):
+    the relative index rel(i, j) = clamp(i - j + max_len - 1, 0, 2 max_len - 2) selects a row of the
+    projected table r_table [2 max_len - 1, H, D] (pos_emb W_R: the projection commutes with the
+    lookup); the score is (a) scale q_i.k_j + (b) scale q_i.r_rel + (c) u.k_j + (d) v.r_rel, with the
+    scale on terms (a) and (b) only, as that page computes it; keys with key_mask[b, j] == 0 have
+    their score replaced by -1e9 before the softmax (so a row whose keys are all masked averages
+    every value uniformly); out = softmax . V.  q, k, v [B, L, H, D]; returns fp64 [B, L, H, D]."""
+    q, k, v, u, vb, rt = (_f64(x) for x in (q, k, v, u, vb, r_table))
+    B, L, H, D = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    pos = np.arange(L)
+    rel = np.clip(pos[:, None] - pos[None, :] + max_len - 1, 0, 2 * max_len - 2)     # [L, L]
+    out = np.empty((B, L, H, D), dtype=np.float64)
+    for b in range(B):
+        for h in range(H):
+            R = rt[rel, h]                                                       # [L, L, D]
+            a = scale * (q[b, :, h] @ k[b, :, h].T)
+            bt = scale * np.einsum("id,ijd->ij", q[b, :, h], R)
+            c = (k[b, :, h] @ u[h])[None, :]
+            d = R @ vb[h]
+            s = a + bt + c + d
+            if key_mask is not None:
+                s = np.where(np.asarray(key_mask)[b][None, :] == 0, -1e9, s)
+            p = np.exp(s - s.max(axis=1, keepdims=True))
+            p /= p.sum(axis=1, keepdims=True)
+            out[b, :, h] = p @ v[b, :, h]
+    return out
+
+
 def linear(X, W) -> np.ndarray:
     """Y = X W in fp64 (a library matmul as the step): q_proj / k_proj / v_proj / o_proj of
     "TransformerXL 相对位置编码" §3.1, linear maps without bias."""
