@@ -394,6 +394,56 @@ def bench_backward(txl, device, stream, rank, args):
                          "peak_source": "fp32 FMA: 152 SMs x 128 lanes x 2 flops x %.0f MHz" % sm_mhz}}
 
 
+def bench_table(txl, device, stream, rank, args):
+    """The learned-table variant (txl_rel_attn_table_fwd): bidirectional attention B16 L384 H16 D64,
+    max_len 512, bf16 inputs, every key visible.  fp32 arithmetic on the CUDA cores: algorithmic
+    flops 6 D per (query, key) pair (content 2 D, position 2 D, P.V 2 D) against the fp32 FMA peak."""
+    import torch
+    B, H, D, L, max_len = 16, 16, 64, 384, 512
+    dt = torch.bfloat16
+    g = torch.Generator(device=device).manual_seed(rank_seed(555, rank))
+    q, k, v = (torch.randn(B, L, H, D, generator=g, device=device).to(dt) for _ in range(3))
+    u = (0.02 * torch.randn(H, D, generator=g, device=device)).float()
+    vb = (0.02 * torch.randn(H, D, generator=g, device=device)).float()
+    rt = torch.randn(2 * max_len - 1, H, D, generator=g, device=device).to(dt)
+    out = torch.empty(B, L, H, D, dtype=dt, device=device)
+
+    def call():
+        txl.rel_attn_table_fwd(q, k, v, u, vb, rt, max_len, out)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            call()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        call()
+    reps = 20
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        graph.replay()
+        e0.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    t_us = e0.elapsed_time(e1) * 1e3 / reps
+    flops = 6 * D * B * H * L * L
+    sm_mhz = 2070.0
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            sm_mhz = float(json.load(f).get("sm_max_mhz", sm_mhz))
+    except Exception:
+        pass
+    fp32_peak = 152 * 128 * 2 * sm_mhz * 1e6 / 1e12
+    achieved = flops / (t_us * 1e-6) / 1e12
+    return {"workload": "table variant: B16 L384 H16 D64 max_len512 bf16, bidirectional, no mask",
+            "us_per_call": t_us, "algorithmic_flops_per_call": flops,
+            "roofline": {"bound": "alu", "achieved": achieved, "peak": fp32_peak, "unit": "TFLOP/s",
+                         "frac": achieved / fp32_peak,
+                         "peak_source": "fp32 FMA: 152 SMs x 128 lanes x 2 flops x %.0f MHz" % sm_mhz}}
+
+
 def run_txl(args):
     import torch
 
@@ -550,6 +600,7 @@ def run_txl(args):
     decode = bench_decode(txl, device, stream, rank, args)
     layer = bench_layer(txl, device, stream, rank, args)
     backward = bench_backward(txl, device, stream, rank, args)
+    table = bench_table(txl, device, stream, rank, args)
 
     attn_flops, pos_flops = _flops(cfg)
     step_flops = attn_flops + pos_flops
@@ -587,6 +638,7 @@ def run_txl(args):
         "decode": decode,
         "layer": layer,
         "backward": backward,
+        "table": table,
         "roofline": {"kernel": "txl_rel_attn_fwd (attn_persist_kernel)", "bound": "tensor",
                      "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "peak_source": "%s bf16 burst (MEASURED_PEAKS.json)" % peak_kind

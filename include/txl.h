@@ -294,6 +294,26 @@ size_t txl_rel_attn_bwd_workspace_size(int B, int L, int H, int D);
 txl_status txl_rel_pos_bwd(int n_rows, int d_model, int n_head, int d_head, const float* dr,
                            float* dW_R, int64_t ld_dw, void* stream);
 
+/*
+ * txl_rel_attn_table_fwd -- the learned-table variant of relative attention ("TransformerXL 相对位置编码"
+ * §3.1): bidirectional over one sequence of L positions (no memory, no causal mask).  The position
+ * vector of a pair is row rel = clamp(i - j + max_len - 1, 0, 2*max_len - 2) of the projected table
+ * r_table = pos_emb W_R (the distance shifted to a non-negative index and clamped, §2; project the
+ * learned pos_emb [2*max_len - 1][d_model] with txl_linear, the projection commutes with the lookup):
+ *   s_ij = scale*q_i.k_j + scale*q_i.r_rel + u_h.k_j + v_h.r_rel
+ * (the scale on the first two terms only, as that page computes it), keys with key_mask[b][j] == 0
+ * scored -1e9 (a row whose keys are all masked averages every value), out_i = softmax_j(s_ij) v_j.
+ *   q, k, v, out : views of [B][L][H][D] (device, dtype).  u, v_bias : device fp32 [H][D].
+ *   r_table : device [2*max_len - 1][H][ld_r], dtype.  key_mask : device uint8 [B][L] or NULL.
+ *   scale   : <= 0 selects 1/sqrt(D).
+ * Limits: 1 <= D <= 128, max_len >= 1.  fp32 arithmetic on the CUDA cores (one warp per four queries).
+ */
+txl_status txl_rel_attn_table_fwd(int B, int L, int H, int D, int max_len,
+                                  const txl_view* q, const txl_view* k, const txl_view* v,
+                                  const float* u, const float* v_bias,
+                                  const void* r_table, int64_t ld_r, const uint8_t* key_mask,
+                                  float scale, const txl_view* out, txl_dtype dtype, void* stream);
+
 /* Self-test of the bounded waits used by every kernel: launches one CTA that waits on an
  * mbarrier nothing will signal, gives up after timeout_us microseconds (1 .. 10^7), writes
  * TXL_ERR_TIMEOUT to the device int err_flag and returns.  The context stays usable. */

@@ -1,0 +1,72 @@
+"""GPU parity of the learned-table variant (txl_rel_attn_table_fwd, "TransformerXL 相对位置编码" §3.1)
+against the fp64 oracle (oracle.table_attn): bidirectional attention with the clamped
+non-negative relative index, the page's scaling of the four terms and its -1e9 key masking.
+Tolerances as for the main path: 1e-5 (fp32), 2e-2 (bf16 inputs, fp32 arithmetic)."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import txl_inputs
+from gpu_common import TOL, ld_r_for, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def txl():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    import transformer_xl_relative_gb300 as m
+    return m
+
+
+TABLE = [
+    # B, H, D, L, max_len, dtype, mask kind, head_stride
+    (2, 4, 32, 10, 512, "f32", "none", 0),      # the page's example sizes (d_model 128 = 4 x 32)
+    (2, 4, 64, 200, 64, "bf16", "random", 0),   # L > max_len: the index clamps at both ends
+    (3, 3, 41, 37, 16, "bf16", "one_empty", 48),  # padded heads; batch entry 1 has every key masked
+    (2, 2, 128, 33, 8, "f32", "random", 0),     # D = 128, L not a multiple of four
+]
+
+
+@pytest.mark.parametrize("shape", TABLE, ids=["B%dH%dD%d_L%d_max%d_%s_%s" % s[:7] for s in TABLE])
+def test_table_variant_matches_oracle(txl, shape):
+    B, H, D, L, max_len, dtype, mk, hs = shape
+    cfg = txl_inputs.custom(B=B, H=H, D=D, d_model=2 * D, L=L, M=0, dtype=dtype, seed=700 + L, head_stride=hs)
+    q, k, v = txl_inputs.make_qkv(cfg, seed=701 + L, L=L, T=L)
+    u, vb, _ = txl_inputs.make_params(cfg, seed=702 + L)
+    nt = 2 * max_len - 1
+    rt = txl_inputs.make_matrix(nt, H * D, seed=703 + L, dtype=cfg.torch_dtype).reshape(nt, H, D)
+    mask = None
+    if mk != "none":
+        gen = torch.Generator().manual_seed(704 + L)
+        mask = (torch.rand(B, L, generator=gen) > 0.25).to(torch.uint8)
+        if mk == "one_empty":
+            mask[1] = 0
+    r_dev = torch.zeros(nt, H, ld_r_for(D), dtype=cfg.torch_dtype, device="cuda")
+    r_dev[..., :D] = rt.cuda()
+    out = to_dev(torch.full_like(q, float("nan")), cfg.hs)
+    txl.rel_attn_table_fwd(to_dev(q, cfg.hs), to_dev(k, cfg.hs), to_dev(v, cfg.hs), u.cuda(), vb.cuda(), r_dev,
+                           max_len, out, key_mask=mask.cuda() if mask is not None else None)
+    torch.cuda.synchronize()
+    ref = oracle.table_attn(q, k, v, u, vb, rt, max_len, key_mask=mask.numpy() if mask is not None else None)
+    err = np.max(np.abs(out.double().cpu().numpy() - ref))
+    assert np.isfinite(err) and err <= TOL[dtype], err
+
+
+def test_table_from_a_projected_learned_table(txl):
+    """The page's composition: r_table = pos_emb W_R, projected with txl_linear, then the variant."""
+    B, H, D, L, max_len, dm = 2, 4, 64, 96, 64, 256
+    cfg = txl_inputs.custom(B=B, H=H, D=D, d_model=dm, L=L, M=0, dtype="bf16", seed=77)
+    q, k, v = txl_inputs.make_qkv(cfg, seed=78, L=L, T=L)
+    u, vb, W = txl_inputs.make_params(cfg, seed=79)
+    pos_emb = txl_inputs.make_matrix(2 * max_len - 1, dm, seed=80)
+    r = txl.linear(pos_emb.cuda(), W[:, :H * D].contiguous().cuda()).view(2 * max_len - 1, H, D)
+    out = torch.empty_like(q).cuda()
+    txl.rel_attn_table_fwd(q.cuda(), k.cuda(), v.cuda(), u.cuda(), vb.cuda(), r, max_len, out)
+    torch.cuda.synchronize()
+    ref = oracle.table_attn(q, k, v, u, vb, r.double().cpu().numpy(), max_len)
+    assert np.max(np.abs(out.double().cpu().numpy() - ref)) <= TOL["bf16"]

@@ -16,6 +16,7 @@ from .api import (  # noqa: F401
     rel_attn_layer,
     rel_attn_layer_workspace_size,
     rel_attn_path,
+    rel_attn_table_fwd,
     rel_pos_bwd,
     rel_pos_gen,
     selftest_wait_timeout,

@@ -284,6 +284,27 @@ def rel_pos_bwd(dr: torch.Tensor, d_model: int, dW_R: torch.Tensor | None = None
     return dW_R
 
 
+def rel_attn_table_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, u: torch.Tensor,
+                       v_bias: torch.Tensor, r_table: torch.Tensor, max_len: int, out: torch.Tensor,
+                       key_mask: torch.Tensor | None = None, scale: float = 0.0, stream=None) -> torch.Tensor:
+    """The learned-table variant (txl_rel_attn_table_fwd): bidirectional attention over q, k, v
+    [B, L, H, D] with the position vector of a pair read from r_table [2 max_len - 1, H, ld_r] at
+    clamp(i - j + max_len - 1); key_mask [B, L] uint8 (0 = masked) or None."""
+    B, L, H, D = q.shape
+    if u.dtype != torch.float32 or v_bias.dtype != torch.float32:
+        raise TypeError("u and v_bias are fp32 [H, D]")
+    if key_mask is not None and (key_mask.dtype != torch.uint8 or not key_mask.is_contiguous()):
+        raise TypeError("key_mask must be a contiguous uint8 [B, L] tensor")
+    vq, vk, vv, vo = view(q), view(k), view(v), view(out)
+    st = _lib().txl_rel_attn_table_fwd(
+        B, L, H, D, int(max_len), ctypes.byref(vq), ctypes.byref(vk), ctypes.byref(vv), u.data_ptr(),
+        v_bias.data_ptr(), r_table.data_ptr(), r_table.stride(1),
+        key_mask.data_ptr() if key_mask is not None else None, float(scale), ctypes.byref(vo), dtype_code(q),
+        _stream(stream))
+    check(st, "txl_rel_attn_table_fwd")
+    return out
+
+
 def selftest_wait_timeout(err_flag: torch.Tensor, timeout_us: int, stream=None) -> None:
     st = _lib().txl_selftest_wait_timeout(err_flag.data_ptr(), int(timeout_us), _stream(stream))
     check(st, "txl_selftest_wait_timeout")

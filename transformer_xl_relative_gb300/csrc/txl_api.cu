@@ -605,6 +605,33 @@ txl_status txl_rel_pos_bwd(int n_rows, int d_model, int n_head, int d_head, cons
     return launch_pos_bwd(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? TXL_OK : TXL_ERR_CUDA;
 }
 
+txl_status txl_rel_attn_table_fwd(int B, int L, int H, int D, int max_len, const txl_view* q, const txl_view* k,
+                                  const txl_view* v, const float* u, const float* v_bias, const void* r_table,
+                                  int64_t ld_r, const uint8_t* key_mask, float scale, const txl_view* out,
+                                  txl_dtype dtype, void* stream)
+{
+    if (B < 0 || L < 0 || H <= 0 || D <= 0 || max_len < 1) return TXL_ERR_INVALID_ARG;
+    if (D > 128) return TXL_ERR_UNSUPPORTED;
+    if (dtype != TXL_F32 && dtype != TXL_BF16) return TXL_ERR_INVALID_ARG;
+    if (!view_ok(q) || !view_ok(k) || !view_ok(v) || !view_ok(out) || !u || !v_bias || !r_table || ld_r < D)
+        return TXL_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(max_len) * 2 - 1 > INT32_MAX) return TXL_ERR_INVALID_ARG;
+    if (B == 0 || L == 0) return TXL_OK;
+    if (scale <= 0.f) scale = 1.0f / std::sqrt(static_cast<float>(D));
+    TableParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.q = q->ptr; p.q_sb = q->stride_b; p.q_st = q->stride_t; p.q_sh = q->stride_h;
+    p.k = k->ptr; p.k_sb = k->stride_b; p.k_st = k->stride_t; p.k_sh = k->stride_h;
+    p.v = v->ptr; p.v_sb = v->stride_b; p.v_st = v->stride_t; p.v_sh = v->stride_h;
+    p.out = out->ptr; p.o_sb = out->stride_b; p.o_st = out->stride_t; p.o_sh = out->stride_h;
+    p.u = u; p.vb = v_bias;
+    p.r = r_table; p.r_row = static_cast<int64_t>(H) * ld_r; p.r_head = ld_r;
+    p.mask = key_mask;
+    p.B = B; p.L = L; p.H = H; p.D = D; p.max_len = max_len;
+    p.scale = scale;
+    return launch_table_attn(p, dtype, static_cast<cudaStream_t>(stream)) == cudaSuccess ? TXL_OK : TXL_ERR_CUDA;
+}
+
 txl_status txl_selftest_wait_timeout(int* err_flag, unsigned timeout_us, void* stream)
 {
     if (!err_flag || timeout_us == 0 || timeout_us > 10000000u) return TXL_ERR_INVALID_ARG;

@@ -125,6 +125,21 @@ struct PosBwdParams {
 };
 
 cudaError_t launch_rel_attn_bwd(const BwdParams& p, txl_dtype dtype, cudaStream_t s);
+
+// ---------------------------------------------------------------- learned-table variant (SIMT)
+struct TableParams {
+    const void* q; int64_t q_sb, q_st, q_sh;
+    const void* k; int64_t k_sb, k_st, k_sh;
+    const void* v; int64_t v_sb, v_st, v_sh;
+    void* out; int64_t o_sb, o_st, o_sh;
+    const float* u; const float* vb;
+    const void* r; int64_t r_row, r_head;       // [2 max_len - 1][H][ld_r]
+    const uint8_t* mask;                        // [B][L], 0 = masked key; may be null
+    int B, L, H, D, max_len;
+    float scale;
+};
+
+cudaError_t launch_table_attn(const TableParams& p, txl_dtype dtype, cudaStream_t s);
 cudaError_t launch_pos_bwd(const PosBwdParams& p, cudaStream_t s);
 
 // ---------------------------------------------------------------- projections (tcgen05 GEMM)

@@ -20,7 +20,7 @@ EXPORTS = (
     "txl_rel_attn_workspace_size", "txl_rel_attn_path", "txl_rel_attn_decode",
     "txl_rel_attn_decode_workspace_size", "txl_rel_attn_decode_noalloc", "txl_mem_push",
     "txl_selftest_wait_timeout", "txl_linear", "txl_rel_attn_layer", "txl_rel_attn_layer_workspace_size",
-    "txl_rel_attn_bwd", "txl_rel_attn_bwd_workspace_size", "txl_rel_pos_bwd",
+    "txl_rel_attn_bwd", "txl_rel_attn_bwd_workspace_size", "txl_rel_pos_bwd", "txl_rel_attn_table_fwd",
 )
 
 
@@ -97,6 +97,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.txl_rel_attn_bwd_workspace_size.restype = ctypes.c_size_t
     lib.txl_rel_pos_bwd.argtypes = [i, i, i, i, vp, vp, i64, vp]
     lib.txl_rel_pos_bwd.restype = i
+    lib.txl_rel_attn_table_fwd.argtypes = [i, i, i, i, i, V, V, V, vp, vp, vp, i64, vp, fp, V, i, vp]
+    lib.txl_rel_attn_table_fwd.restype = i
     _lib = lib
     return lib
 
