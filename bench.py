@@ -174,6 +174,53 @@ def cpu_baseline(cfg, target_s: float = 12.0, threads=None):
                 nb, cfg.B, cfg.H, cfg.L, t_total)}
 
 
+def row_baselines(threads=None) -> dict:
+    """The oracle as it stands, timed on the host cores beside each of the next-row measurements,
+    on a bounded sample of its workload (a few seconds each), scaled to the sub-bench's unit."""
+    import numpy as np
+    import oracle
+    threads = threads or (os.cpu_count() or 1)
+    rng = np.random.default_rng(99)
+    res = {}
+    # decode: B8 H16 D64 L1 M4096 clamp 1000; sampled (b, h) pairs of the single query
+    B, H, D, L, M, C, dm = 8, 16, 64, 1, 4096, 1000, 1024
+    q = rng.standard_normal((1, L, H, D)); k = rng.standard_normal((1, M + L, H, D))
+    v = rng.standard_normal((1, M + L, H, D)); u = 0.02 * rng.standard_normal((H, D))
+    vb = 0.02 * rng.standard_normal((H, D)); W = rng.standard_normal((dm, H * D)) * dm ** -0.5
+    t0 = time.perf_counter()
+    oracle.rel_attn(q, k, v, u, vb, W, M, M, C, threads=threads, rows=[(0, h, 0) for h in range(H)])
+    t = time.perf_counter() - t0
+    res["decode"] = {"value": 1e6 * t * B, "unit": "us per call", "cores": threads, "kind": "oracle",
+                     "sample": "1 of 8 batch entries (16 heads, the position table included), fp64, %.1f s" % t}
+    # layer: B16 L384 M384 H16 D64 d_model 1024; one batch entry, every head and position
+    L, M, C = 384, 384, 1000
+    h_mem = rng.standard_normal((1, M, dm)); hh = rng.standard_normal((1, L, dm))
+    Wq, Wk, Wv = (rng.standard_normal((dm, H * D)) * dm ** -0.5 for _ in range(3))
+    Wo = rng.standard_normal((H * D, dm)) * (H * D) ** -0.5
+    t0 = time.perf_counter()
+    oracle.rel_layer(h_mem, hh, Wq, Wk, Wv, Wo, u, vb, W, H, D, M, C, threads=threads)
+    t = time.perf_counter() - t0
+    res["layer"] = {"value": oracle.layer_flops(1, H, D, L, M, dm) / t / 1e12, "unit": "TFLOP/s", "cores": threads,
+                    "kind": "oracle", "sample": "1 of 16 batch entries (every head and position), fp64, %.1f s" % t}
+    # backward: the large workload's call; two (b, h) pairs of one batch entry
+    q = rng.standard_normal((1, L, H, D)); k = rng.standard_normal((1, M + L, H, D))
+    v = rng.standard_normal((1, M + L, H, D)); dO = rng.standard_normal((1, L, H, D))
+    t0 = time.perf_counter()
+    oracle.rel_attn_bwd(q, k, v, u, vb, W, M, M, C, dO, bh=[(0, 0), (0, 1)])
+    t = time.perf_counter() - t0
+    pairs = 2 * (L * M + L * (L + 1) // 2)
+    res["backward"] = {"value": 16 * D * pairs / t / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                       "sample": "2 of 256 (b, h) pairs (numpy, the position table and dW_R included), fp64, %.1f s" % t}
+    # table variant: B16 L384 H16 D64 max_len 512; one batch entry, two heads
+    rt = rng.standard_normal((1023, 2, D))
+    t0 = time.perf_counter()
+    oracle.table_attn(q[:, :, :2], k[:, :L, :2], v[:, :L, :2], u[:2], vb[:2], rt, 512)
+    t = time.perf_counter() - t0
+    res["table"] = {"value": 6 * D * 2 * L * L / t / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                    "sample": "2 of 256 (b, h) pairs (numpy), fp64, %.1f s" % t}
+    return res
+
+
 def run_reference(args):
     world, rank, _ = _dist()
     if rank != 0:
@@ -648,6 +695,8 @@ def run_txl(args):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg)
+        for key, base in row_baselines().items():
+            line[key]["cpu_baseline"] = base
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
