@@ -601,7 +601,7 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_persist_kernel(const __grid
 
             // ---- epilogue: O / (l_0 + l_1) -> bf16 -> out[b, i0 + pi, h, :]; each half stores
             // half of the columns.  O is released to the next item's P.V as soon as it is read.
-            if (ok) ok = warp_wait(bar.o_full, n & 1, wc, 35);
+            if (ok) ok = warp_spin(bar.o_full, n & 1, wc, 35);
             xchg[2 * (it.n_t & 1) + hf] = l_half;
             pair_bar(li);
             uint32_t o[32];

@@ -151,6 +151,41 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Latency-first variants for waits on a critical path by threads with nothing else to issue:
+// the slow path polls test_wait without suspending (a suspended try_wait may resume up to its
+// suspend hint after the phase completed), checking the abort flag and deadline every 256 polls.
+static __device__ __noinline__ bool mbar_spin_slow(uint64_t* bar, uint32_t parity, WaitCtl w, int where)
+{
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 256; ++i)
+            if (mbar_test_wait(bar, parity)) return true;
+        if (*w.abort) return false;
+        if (global_timer_ns() - t0 > w.timeout_ns) {
+            wait_fail(w, where);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ bool mbar_spin(uint64_t* bar, uint32_t parity, const WaitCtl& w, int where)
+{
+    if (mbar_test_wait(bar, parity)) return true;
+    return mbar_spin_slow(bar, parity, w, where);
+}
+
+__device__ __forceinline__ bool warp_spin(uint64_t* bar, uint32_t parity, const WaitCtl& w, int where)
+{
+    if (__all_sync(0xffffffffu, mbar_test_wait(bar, parity))) return true;
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) ok = mbar_spin_slow(bar, parity, w, where);
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    if (ok) (void)mbar_test_wait(bar, parity);
+    __syncwarp();
+    return ok;
+}
+
 // ------------------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map)
 {
