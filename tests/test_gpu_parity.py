@@ -10,7 +10,7 @@ import torch
 
 import oracle
 import txl_inputs
-from gpu_common import TOL, ld_r_for, max_err, oracle_out, run_case
+from gpu_common import TOL, ld_r_for, max_err, oracle_out, run_case, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -107,3 +107,25 @@ def test_workload_full(txl, name):
     assert path == 1
     err = max_err(out, oracle_out(cfg, case))
     assert err <= TOL["bf16"], err
+
+
+# ---------------------------------------------------------------- output views without 16-byte rows
+@pytest.mark.parametrize("D", [64, 128])
+def test_out_view_unaligned(txl, D):
+    """An output view whose head stride is not a multiple of 16 bytes takes the scalar stores of
+    the fused kernels: the same values as a contiguous output, nothing written outside the view."""
+    cfg = txl_inputs.custom(B=2, H=3, D=D, d_model=2 * D, L=200, M=150, clamp_len=1000, dtype="bf16",
+                            seed=77 + D)
+    case = txl_inputs.make_case(cfg)
+    out, r, path = run_case(cfg, case, txl)
+    assert path == 1
+    q, k, v = (to_dev(case[n]) for n in ("q", "k", "v"))
+    M = cfg.M
+    mem = txl.Memory(k[:, :M], v[:, :M], 0, M)
+    store = torch.full((cfg.B, cfg.L, cfg.H, D + 1), 7.0, dtype=torch.bfloat16, device="cuda")
+    out2 = store[..., :D]
+    txl.rel_attn_fwd(q, mem, k[:, M:], v[:, M:], case["u"].cuda(), case["vb"].cuda(), r, r.shape[0],
+                     cfg.clamp_len, out2)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out2)
+    assert bool((store[..., D] == 7.0).all())

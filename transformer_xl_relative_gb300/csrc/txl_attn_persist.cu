@@ -551,21 +551,26 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_persist_kernel(const __grid
                         m_run = mt;
                         rescale_o = true;
                     }
+                    // P = 2^(s - m) is taken on bf16 pairs: P.V consumes bf16 P, so the pair is
+                    // rounded once before the exponential instead of after it, and one
+                    // special-function instruction serves two keys.  The row sum adds exactly the
+                    // bf16 values P.V multiplies.
                     const uint64_t negm = f2_pack(-m_run, -m_run);
-                    uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
+                    float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
                     uint32_t pw[32];
 #pragma unroll
                     for (int k = 0; k < 32; ++k) {
                         float y0, y1;
                         f2_unpack(f2_add(f2_pack(s[2 * k], s[2 * k + 1]), negm), y0, y1);
-                        const float p0 = ex2_approx(y0), p1 = ex2_approx(y1);
-                        if (k & 1) acc1 = f2_add(acc1, f2_pack(p0, p1));
-                        else acc0 = f2_add(acc0, f2_pack(p0, p1));
-                        pw[k] = pack_bf16x2(p0, p1);
+                        pw[k] = ex2_bf16x2(pack_bf16x2(y0, y1));
+                        if (k & 1) {
+                            b0 = add_bf16lo_f32(pw[k], b0);
+                            b1 = add_bf16hi_f32(pw[k], b1);
+                        } else {
+                            a0 = add_bf16lo_f32(pw[k], a0);
+                            a1 = add_bf16hi_f32(pw[k], a1);
+                        }
                     }
-                    float a0, a1, b0, b1;
-                    f2_unpack(acc0, a0, a1);
-                    f2_unpack(acc1, b0, b1);
                     l_half = fmaf(l_half, alpha, (a0 + a1) + (b0 + b1));
                     // P.V of the previous tile (of this item or the one before) must be complete
                     // before the P buffer, or O (rescale), is touched
@@ -599,42 +604,63 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_persist_kernel(const __grid
                 }
             }
 
-            // ---- epilogue: O / (l_0 + l_1) -> bf16 -> out[b, i0 + pi, h, :]; each half stores
-            // half of the columns.  O is released to the next item's P.V as soon as it is read.
+            // ---- epilogue: O / (l_0 + l_1) -> bf16 -> out[b, i0 + pi, h, :].  O is released to the
+            // next item's P.V as soon as it is read.  Each thread stages its normalised half row in
+            // the front of its (now dead) ring row; the pair of warps then writes its 32 rows as
+            // whole 128-byte lines, four rows per store instruction instead of 32 half lines.
             if (ok) ok = warp_spin(bar.o_full, n & 1, wc, 35);
             xchg[2 * (it.n_t & 1) + hf] = l_half;
             pair_bar(li);
-            uint32_t o[32];
+            const bool staged = p.out_vec != 0;
             if (ok) {
+                uint32_t o[32];
                 tc_fence_after();
                 tmem_ld32(tmem + lane_base + kColO + (NPV / 2) * hf, o);
                 tmem_ld_wait();
                 tc_fence_before();
                 __syncwarp();
                 mbar_arrive_if(bar.o_free, lane == 0);
-                const float l_row = l_half + xchg[2 * (it.n_t & 1) + (hf ^ 1)];
-                const int i = it.i0 + pi;
-                const float inv_l = 1.f / l_row;
-                const int d0 = (NPV / 2) * hf;
-                if (i < p.L) {
-                    __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + it.b * p.o_sb +
-                                          static_cast<int64_t>(i) * p.o_st + it.h * p.o_sh;
-                    if ((p.D % 8) == 0 && d0 + 32 <= p.D) {
+                const float inv_l = rcp_approx(l_half + xchg[2 * (it.n_t & 1) + (hf ^ 1)]);
+                if (staged) {
+                    uint4* st = reinterpret_cast<uint4*>(bdrow + 16 * hf);
 #pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            uint32_t w[4];
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        uint32_t w[4];
 #pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                w[e] = pack_bf16x2(__uint_as_float(o[8 * q4 + 2 * e]) * inv_l,
-                                                   __uint_as_float(o[8 * q4 + 2 * e + 1]) * inv_l);
-                            *reinterpret_cast<uint4*>(orow + d0 + 8 * q4) = make_uint4(w[0], w[1], w[2], w[3]);
-                        }
-                    } else {
+                        for (int e = 0; e < 4; ++e)
+                            w[e] = pack_bf16x2(__uint_as_float(o[8 * q4 + 2 * e]) * inv_l,
+                                               __uint_as_float(o[8 * q4 + 2 * e + 1]) * inv_l);
+                        st[q4] = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                } else {
+                    const int i = it.i0 + pi, d0 = (NPV / 2) * hf;
+                    if (i < p.L) {
+                        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + it.b * p.o_sb +
+                                              static_cast<int64_t>(i) * p.o_st + it.h * p.o_sh;
                         for (int k = 0; k < 32 && d0 + k < p.D; ++k)
                             orow[d0 + k] = __float2bfloat16_rn(__uint_as_float(o[k]) * inv_l);
                     }
                 }
             }
+            pair_bar(li);                                   // both halves of every row are staged
+            if (ok && staged) {
+                // this warp stores rows (li & ~31) + 16 hf + 0..15: lane -> row + lane / 8, chunk
+                // of 8 columns lane mod 8
+                const uint32_t* bd0 = reinterpret_cast<const uint32_t*>(smem + PSmem::BD);
+                const int c = lane & 7;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int r = (li & ~31) + 16 * hf + 4 * k + (lane >> 3);
+                    const int i = it.i0 + query_of_row(r);
+                    if (i < p.L && 8 * c < p.D) {
+                        const uint4 v = *reinterpret_cast<const uint4*>(bd0 + r * kBdPitchWords + 4 * c);
+                        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + it.b * p.o_sb +
+                                              static_cast<int64_t>(i) * p.o_st + it.h * p.o_sh;
+                        *reinterpret_cast<uint4*>(orow + 8 * c) = v;
+                    }
+                }
+            }
+            pair_bar(li);                                   // staged rows read before the ring reset
         }
     }
 

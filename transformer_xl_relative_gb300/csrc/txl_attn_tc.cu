@@ -603,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             const float inv_l = 1.f / l_row;
             __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + b * p.o_sb +
                                   static_cast<int64_t>(i) * p.o_st + h * p.o_sh;
-            const bool vec = (p.D % 8) == 0;
+            const bool vec = p.out_vec != 0;
 #pragma unroll 1
             for (int cb = 0; cb < NPV / 64; ++cb) {
                 uint32_t o[32];

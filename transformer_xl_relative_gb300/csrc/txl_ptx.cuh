@@ -515,4 +515,19 @@ __device__ __forceinline__ float ex2_approx(float x)
     return r;
 }
 
+// 2^x of both bf16 halves of w, one special-function instruction for the pair.
+__device__ __forceinline__ uint32_t ex2_bf16x2(uint32_t w)
+{
+    uint32_t r;
+    asm("ex2.approx.ftz.bf16x2 %0, %1;" : "=r"(r) : "r"(w));
+    return r;
+}
+
+__device__ __forceinline__ float rcp_approx(float x)
+{
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
 }  // namespace txl
