@@ -208,8 +208,9 @@ def row_baselines(threads=None) -> dict:
     t0 = time.perf_counter()
     oracle.rel_attn_bwd(q, k, v, u, vb, W, M, M, C, dO, bh=[(0, 0), (0, 1)])
     t = time.perf_counter() - t0
-    pairs = 2 * (L * M + L * (L + 1) // 2)
-    res["backward"] = {"value": 16 * D * pairs / t / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+    f_attn, _ = bwd_flops(1, 2, D, L, M, min(M + L, C + 1), dm)          # the two sampled (b, h)
+    _, f_pos = bwd_flops(1, H, D, L, M, min(M + L, C + 1), dm)           # dW_R is taken whole
+    res["backward"] = {"value": (f_attn + f_pos) / t / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
                        "sample": "2 of 256 (b, h) pairs (numpy, the position table and dW_R included), fp64, %.1f s" % t}
     # table variant: B16 L384 H16 D64 max_len 512; one batch entry, two heads
     rt = rng.standard_normal((1023, 2, D))
@@ -382,12 +383,20 @@ def bench_layer(txl, device, stream, rank, args):
                          "algorithmic_flops_per_launch": pflops}}
 
 
+def bwd_flops(B, H, D, L, M, n_rows, d_model):
+    """Algorithmic flops of the backward of one call: per visible (query, key) pair the two score
+    terms (4 D), dP (2 D), dq (4 D) and dr (2 D); per pair with a current-segment key also dk and
+    dv (4 D; the memory is stop-gradient); and dW_R = R^T dr (2 n_rows d_model H D)."""
+    pairs = B * H * (L * M + L * (L + 1) // 2)
+    pairs_cur = B * H * (L * (L + 1) // 2)
+    return 12 * D * pairs + 4 * D * pairs_cur, 2 * n_rows * d_model * H * D
+
+
 def bench_backward(txl, device, stream, rank, args):
-    """Gradients of one fused-attention call on the large workload (txl_rel_attn_bwd + the position
-    table's txl_rel_pos_bwd): every score recomputed in fp32 on the CUDA cores.  Algorithmic flops
-    per visible (query, key) pair: 16 D (scores 4 D, dP 2 D, dq 4 D, dk 2 D, dv 2 D, dr 2 D), plus
-    2 n_rows d_model H D for dW_R; reported against the fp32 FMA peak of the SMs (152 SMs x 128
-    lanes x 2 flops x the measured maximum SM clock)."""
+    """Gradients of one fused-attention call on the large workload: txl_rel_attn_bwd (on this
+    workload the tensor-core kernel: bf16 mma.sync products, fp32 accumulation and gradients)
+    and the position table's txl_rel_pos_bwd, timed together and each alone.  The attention
+    backward is reported against the measured bf16 tensor peak."""
     import torch
     B, H, D, L, M, C, dm = 16, 16, 64, 384, 384, 1000, 1024
     dt = torch.bfloat16
@@ -408,37 +417,42 @@ def bench_backward(txl, device, stream, rank, args):
     ws = torch.empty(16 * 1024 * 1024 * 8, dtype=torch.uint8, device=device)
     res = {}
 
-    def call():
+    def attn():
         res["g"] = txl.rel_attn_bwd(q, mem, k[:, M:], v[:, M:], u, vb, r, n_rows, C, out, dO, workspace=ws)
+
+    def pos():
         res["dW"] = txl.rel_pos_bwd(res["g"]["dr"], dm)
 
-    with torch.cuda.stream(stream):
-        call()
-    torch.cuda.synchronize()
-    reps = 3
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(reps):
-            call()
-        e1.record(stream)
-    torch.cuda.synchronize()
-    t_us = e0.elapsed_time(e1) * 1e3 / reps
-    pairs = B * H * (L * M + L * (L + 1) // 2)
-    flops = 16 * D * pairs + 2 * n_rows * dm * H * D
-    sm_mhz = 2070.0
-    try:
-        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            sm_mhz = float(json.load(f).get("sm_max_mhz", sm_mhz))
-    except Exception:
-        pass
-    fp32_peak = 152 * 128 * 2 * sm_mhz * 1e6 / 1e12
-    achieved = flops / (t_us * 1e-6) / 1e12
+    def both():
+        attn()
+        pos()
+
+    def timed(fn, reps=5):
+        with torch.cuda.stream(stream):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(reps):
+                fn()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / reps
+
+    t_us = timed(both)
+    t_attn = timed(attn)
+    t_pos = timed(pos)
+    f_attn, f_pos = bwd_flops(B, H, D, L, M, n_rows, dm)
+    bf16_peak, _, _, peak_src = _peaks()
+    achieved = f_attn / (t_attn * 1e-6) / 1e12
     return {"workload": "backward: B16 H16 D64 d_model1024 L384 M384 clamp1000, bf16 inputs, fp32 gradients",
-            "us_per_call": t_us, "algorithmic_flops_per_call": flops,
-            "roofline": {"bound": "alu", "achieved": achieved, "peak": fp32_peak, "unit": "TFLOP/s",
-                         "frac": achieved / fp32_peak,
-                         "peak_source": "fp32 FMA: 152 SMs x 128 lanes x 2 flops x %.0f MHz" % sm_mhz}}
+            "us_per_call": t_us, "us_attn_bwd": t_attn, "us_pos_bwd": t_pos,
+            "algorithmic_flops_per_call": f_attn + f_pos, "tflops": (f_attn + f_pos) / (t_us * 1e-6) / 1e12,
+            "roofline": {"kernel": "txl_rel_attn_bwd (bwd_tc_kernel, bf16 mma.sync, + bias reduction)",
+                         "bound": "tensor", "achieved": achieved, "peak": bf16_peak, "unit": "TFLOP/s",
+                         "frac": achieved / bf16_peak, "algorithmic_flops_per_launch": f_attn,
+                         "peak_source": peak_src + " bf16 burst"}}
 
 
 def bench_table(txl, device, stream, rank, args):

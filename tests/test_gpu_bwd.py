@@ -44,6 +44,16 @@ BWD = [
     (2, 3, 41, 82, 24, 0, 0, 0, 10, "bf16", 48),         # no memory, clamp, padded heads
     (2, 4, 64, 128, 128, 128, 128, 0, 1000, "bf16", 0),  # a full 128-key tile on each side
     (1, 2, 128, 128, 30, 33, 20, 5, 40, "bf16", 0),      # D = 128, ring, clamp, L not a multiple of 4
+    # d_head 64 with 16-byte rows takes the tensor-core kernel: ragged query tiles, ring write
+    # pointers, clamps inside a key tile's distance window, no memory, one query, the large
+    # workload's per-head shape; a 68-element head stride keeps d_head 64 on the SIMT kernels
+    (1, 2, 64, 128, 100, 70, 70, 13, 30, "bf16", 0),
+    (2, 2, 64, 128, 200, 0, 0, 0, 50, "bf16", 0),
+    (1, 1, 64, 64, 5, 3, 2, 1, 1000, "bf16", 0),
+    (1, 2, 64, 64, 1, 130, 130, 0, 1000, "bf16", 0),
+    (1, 2, 64, 128, 384, 384, 384, 0, 1000, "bf16", 0),
+    (1, 2, 64, 128, 70, 64, 64, 0, 40, "bf16", 0),
+    (1, 2, 64, 128, 40, 30, 30, 0, 1000, "bf16", 68),
 ]
 
 

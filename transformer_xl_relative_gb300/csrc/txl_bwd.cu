@@ -616,8 +616,9 @@ __global__ void bwd_bias_kernel(const BwdParams p, int64_t chunk)
 // ---------------------------------------------------------------------------- dW_R = R^T dr
 // Block (64 model columns m, 64 columns n = h*D + d), 256 threads with 4 x 4 outputs each.  The
 // block's 64 frequencies are computed once in double precision; an element R_delta[m] reduces the
-// angle delta * w modulo 2 pi in double precision and evaluates the fp32 sine or cosine of the
-// reduced angle (within an ulp or two of the double-precision value rounded to fp32).
+// angle delta * w modulo 2 pi in double precision (a multiply, a rounding and an fma: no double
+// division on the SMs' slow fp64 path) and evaluates the fp32 sine or cosine of the reduced angle
+// (within an ulp or two of the double-precision value rounded to fp32).
 constexpr int kPosBwdT = 64, kPosBwdChunk = 32;
 
 __global__ void __launch_bounds__(256) pos_bwd_kernel(PosBwdParams p)
@@ -635,6 +636,7 @@ __global__ void __launch_bounds__(256) pos_bwd_kernel(PosBwdParams p)
     float acc[4][4] = {};
     const int HD = p.H * p.D;
     constexpr double kTwoPi = 6.283185307179586476925;
+    constexpr double kInvTwoPi = 0.159154943091895335768884;   // the quotient only picks the multiple of 2 pi
     for (int d0 = 0; d0 < p.n_rows; d0 += kPosBwdChunk) {
         for (int e = threadIdx.x; e < kPosBwdChunk * kPosBwdT; e += blockDim.x) {
             const int rr = e / kPosBwdT, cc = e % kPosBwdT;
@@ -643,7 +645,7 @@ __global__ void __launch_bounds__(256) pos_bwd_kernel(PosBwdParams p)
             if (delta < p.n_rows) {
                 if (m < p.d_model) {
                     const double x = static_cast<double>(delta) * Ws[cc];
-                    const float red = static_cast<float>(x - rint(x / kTwoPi) * kTwoPi);
+                    const float red = static_cast<float>(fma(-rint(x * kInvTwoPi), kTwoPi, x));
                     rv = (m & 1) ? cosf(red) : sinf(red);
                 }
                 if (n < HD) gv = p.dr[static_cast<int64_t>(delta) * HD + n];
@@ -676,6 +678,22 @@ __global__ void __launch_bounds__(256) pos_bwd_kernel(PosBwdParams p)
         }
 }
 
+// The bias reduction: du and dv_bias from the per-query parts in the workspace.
+cudaError_t launch_bias(const BwdParams& p, cudaStream_t s)
+{
+    const AttnSimtParams& a = p.a;
+    const int HD = a.H * a.D;
+    const int64_t rows = static_cast<int64_t>(a.B) * a.L;
+    int64_t chunk = kBiasRowsPerChunk;
+    if ((rows + chunk - 1) / chunk > 65535) chunk = (rows + 65534) / 65535;
+    const int64_t chunks = (rows + chunk - 1) / chunk;
+    cudaError_t e = cudaMemsetAsync(p.du, 0, sizeof(float) * HD, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(p.dvb, 0, sizeof(float) * HD, s);
+    if (e != cudaSuccess) return e;
+    bwd_bias_kernel<<<dim3((HD + 127) / 128, static_cast<unsigned>(chunks)), 128, 0, s>>>(p, chunk);
+    return cudaGetLastError();
+}
+
 template <typename T, int DC>
 cudaError_t launch_all(const BwdParams& p, cudaStream_t s)
 {
@@ -695,16 +713,7 @@ cudaError_t launch_all(const BwdParams& p, cudaStream_t s)
     const int64_t dist_warps = static_cast<int64_t>(a.H) * ((n_exact + kG - 1) / kG);
     if (n_exact > 0) bwd_dist_kernel<T, DC><<<static_cast<unsigned>(blocks(dist_warps)), thr, 0, s>>>(p, n_exact);
     if (clamped) bwd_clamp_kernel<T, DC><<<static_cast<unsigned>(blocks(row_warps)), thr, 0, s>>>(p);
-    const int HD = a.H * a.D;
-    const int64_t rows = static_cast<int64_t>(a.B) * a.L;
-    int64_t chunk = kBiasRowsPerChunk;
-    if ((rows + chunk - 1) / chunk > 65535) chunk = (rows + 65534) / 65535;
-    const int64_t chunks = (rows + chunk - 1) / chunk;
-    e = cudaMemsetAsync(p.du, 0, sizeof(float) * HD, s);
-    if (e == cudaSuccess) e = cudaMemsetAsync(p.dvb, 0, sizeof(float) * HD, s);
-    if (e != cudaSuccess) return e;
-    bwd_bias_kernel<<<dim3((HD + 127) / 128, static_cast<unsigned>(chunks)), 128, 0, s>>>(p, chunk);
-    return cudaGetLastError();
+    return launch_bias(p, s);
 }
 
 template <typename T>
@@ -718,6 +727,16 @@ cudaError_t launch_t(const BwdParams& p, cudaStream_t s)
 cudaError_t launch_rel_attn_bwd(const BwdParams& p, txl_dtype dtype, cudaStream_t s)
 {
     if (static_cast<int64_t>(p.a.B) * p.a.H * p.a.L == 0) return cudaSuccess;
+    if (bwd_tc_eligible(p, dtype)) {
+        const AttnSimtParams& a = p.a;
+        const size_t cur = static_cast<size_t>(a.B) * a.L * a.H * a.D * sizeof(float);
+        cudaError_t e = cudaMemsetAsync(p.dr, 0, static_cast<size_t>(p.n_rows) * a.H * a.D * sizeof(float), s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(p.dk, 0, cur, s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(p.dv, 0, cur, s);
+        if (e == cudaSuccess) e = launch_bwd_tc(p, s);
+        if (e == cudaSuccess) e = launch_bias(p, s);
+        return e;
+    }
     return dtype == TXL_F32 ? launch_t<float>(p, s) : launch_t<__nv_bfloat16>(p, s);
 }
 

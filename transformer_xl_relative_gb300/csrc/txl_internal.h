@@ -126,6 +126,10 @@ struct PosBwdParams {
 };
 
 cudaError_t launch_rel_attn_bwd(const BwdParams& p, txl_dtype dtype, cudaStream_t s);
+// tensor-core backward (bf16, D = 64, 16-byte aligned rows): eligibility and the gradient kernel
+// (dq, pac, pbd written; dk, dv, dr accumulated atomically into zeroed buffers)
+bool bwd_tc_eligible(const BwdParams& p, txl_dtype dtype);
+cudaError_t launch_bwd_tc(const BwdParams& p, cudaStream_t s);
 
 // ---------------------------------------------------------------- learned-table variant (SIMT)
 struct TableParams {
