@@ -29,6 +29,14 @@ TABLE = [
     (2, 4, 64, 200, 64, "bf16", "random", 0),   # L > max_len: the index clamps at both ends
     (3, 3, 41, 37, 16, "bf16", "one_empty", 48),  # padded heads; batch entry 1 has every key masked
     (2, 2, 128, 33, 8, "f32", "random", 0),     # D = 128, L not a multiple of four
+    # bf16 with d_head 64 and 16-byte rows takes the tensor-core kernel: one position, a ragged
+    # key tile with a fully masked batch entry, the bench's per-head shape, a table of five rows
+    # (nearly every pair clamped); a 68-element head stride keeps d_head 64 on the SIMT kernel
+    (1, 2, 64, 1, 4, "bf16", "none", 0),
+    (2, 2, 64, 130, 512, "bf16", "one_empty", 0),
+    (1, 3, 64, 384, 512, "bf16", "none", 0),
+    (1, 2, 64, 70, 3, "bf16", "random", 0),
+    (1, 2, 64, 50, 16, "bf16", "none", 68),
 ]
 
 

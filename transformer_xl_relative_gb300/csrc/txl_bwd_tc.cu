@@ -25,10 +25,13 @@
 #include <cuda_bf16.h>
 
 #include "txl_internal.h"
+#include "txl_mma.cuh"
 
 namespace txl {
 
 namespace {
+
+using namespace mma;
 
 constexpr int kBT = 128;                 // threads: four warps
 constexpr int kQT = 64;                  // queries per CTA
@@ -53,85 +56,6 @@ struct BSmem {
     static constexpr int Size = BD + kQT * kBdPitch * 2;
 };
 
-__device__ __forceinline__ uint32_t swz64(int row, int col)        // byte offset, 64-wide rows
-{
-    return static_cast<uint32_t>(row * 128 + ((((col >> 3) ^ row) & 7) << 4) + (col & 7) * 2);
-}
-__device__ __forceinline__ uint32_t swz128(int row, int col)       // byte offset, 128-wide rows
-{
-    const int c = col >> 3;
-    return static_cast<uint32_t>(row * 256 + (((c & 8) | ((c ^ row) & 7)) << 4) + (col & 7) * 2);
-}
-
-__device__ __forceinline__ uint32_t cvta_smem(const void* p)
-{
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3)
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3)
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
-}
-
-// D += A B: m16n8k16, A row-major bf16, B column-major bf16, fp32 accumulators.
-__device__ __forceinline__ void mma16816(float* c, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1)
-{
-    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-                 "{%8, %9}, {%0, %1, %2, %3};"
-                 : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ uint32_t pack2(float lo, float hi)
-{
-    uint32_t r;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-
-__device__ __forceinline__ float ex2(float x)
-{
-    float r;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
-    return r;
-}
-
-// Fragment addresses (lane l) for ldmatrix.x4, see the fragment layouts of mma.m16n8k16:
-//  A 16x16 at (r0, c0) of a row-major [m][k] tile (non-transposed load)
-__device__ __forceinline__ void a_rc(int lane, int r0, int c0, int& r, int& c)
-{
-    r = r0 + (lane & 7) + ((lane >> 3) & 1) * 8;
-    c = c0 + (lane >> 4) * 8;
-}
-//  B of two n-tiles (n0 .. n0+15) x k16 (k0 ..) from an [n][k] tile (non-transposed load)
-__device__ __forceinline__ void b_nk(int lane, int n0, int k0, int& r, int& c)
-{
-    r = n0 + (lane & 7) + (lane >> 4) * 8;
-    c = k0 + ((lane >> 3) & 1) * 8;
-}
-//  B of two n-tiles from a [k][n] tile (transposed load)
-__device__ __forceinline__ void b_kn(int lane, int k0, int n0, int& r, int& c)
-{
-    r = k0 + (lane & 7) + ((lane >> 3) & 1) * 8;
-    c = n0 + (lane >> 4) * 8;
-}
-//  A 16x16 at (m0, k0) from a [k][m] tile (transposed load)
-__device__ __forceinline__ void a_km(int lane, int m0, int k0, int& r, int& c)
-{
-    r = k0 + (lane & 7) + (lane >> 4) * 8;
-    c = m0 + ((lane >> 3) & 1) * 8;
-}
-
 // Key j of (b, h): memory ring slot for 0 <= j < M, current segment for M <= j < M + L, else null.
 __device__ __forceinline__ void key_rows(const AttnSimtParams& a, int b, int h, int j, const __nv_bfloat16*& kp,
                                          const __nv_bfloat16*& vp)
@@ -150,15 +74,6 @@ __device__ __forceinline__ void key_rows(const AttnSimtParams& a, int b, int h, 
         vp = static_cast<const __nv_bfloat16*>(a.vcur) + b * a.vc_sb + static_cast<int64_t>(t) * a.vc_st + h * a.vc_sh;
     }
 }
-
-// 16-byte asynchronous copy into shared memory; src_bytes = 0 fills the 16 bytes with zeros.
-__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes)
-{
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(cvta_smem(dst)), "l"(src), "r"(src_bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 // Issue the copies of the key tile (and the value tile) starting at key j0 and of the position
 // window whose row 0 is distance tb (rows clamped into [0, min(C, n_rows - 1)]: rows outside pair

@@ -143,6 +143,9 @@ struct TableParams {
     int B, L, H, D, max_len;
     float scale;
 };
+// tensor-core table variant (bf16, D = 64, 16-byte aligned rows)
+bool table_tc_eligible(const TableParams& p, txl_dtype dtype);
+cudaError_t launch_table_tc(const TableParams& p, cudaStream_t s);
 
 cudaError_t launch_table_attn(const TableParams& p, txl_dtype dtype, cudaStream_t s);
 cudaError_t launch_pos_bwd(const PosBwdParams& p, cudaStream_t s);

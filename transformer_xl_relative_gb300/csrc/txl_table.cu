@@ -161,6 +161,7 @@ cudaError_t launch_t(const TableParams& p, cudaStream_t s)
 cudaError_t launch_table_attn(const TableParams& p, txl_dtype dtype, cudaStream_t s)
 {
     if (static_cast<int64_t>(p.B) * p.H * p.L == 0) return cudaSuccess;
+    if (table_tc_eligible(p, dtype)) return launch_table_tc(p, s);
     return dtype == TXL_F32 ? launch_t<float>(p, s) : launch_t<__nv_bfloat16>(p, s);
 }
 
