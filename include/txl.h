@@ -290,9 +290,12 @@ size_t txl_rel_attn_bwd_workspace_size(int B, int L, int H, int D);
 /*
  * txl_rel_pos_bwd -- gradient of W_R from the gradient of the position rows:
  *   dW_R[m][h*d_head + d] = sum_delta R_delta[m] * dr[delta][h][d]
- * with R_delta the interleaved sinusoid of txl_rel_pos_gen (frequencies and the angle reduced
- * modulo 2 pi in double precision, then the fp32 sine or cosine).  dr: device fp32 [n_rows][H][D] (as txl_rel_attn_bwd writes it);
- * dW_R: device fp32 [d_model][ld_dw], columns 0..H*D-1 written.  d_model even, ld_dw >= H*D.
+ * with R_delta the interleaved sinusoid of txl_rel_pos_gen (frequencies in double precision; the
+ * angle of every fourth distance reduced modulo 2 pi in double precision, the other three offset from
+ * it in fp32; then the fp32 sine or cosine: entries within 6e-7 of the exact sinusoid).  dr: device fp32 [n_rows][H][D] (as txl_rel_attn_bwd writes it);
+ * dW_R: device fp32 [d_model][ld_dw], columns 0..H*D-1 written (zeroed, then partial sums over
+ * ranges of distances added atomically: the fp32 summation order may differ from call to call).
+ * d_model even, ld_dw >= H*D.
  */
 txl_status txl_rel_pos_bwd(int n_rows, int d_model, int n_head, int d_head, const float* dr,
                            float* dW_R, int64_t ld_dw, void* stream);

@@ -615,10 +615,11 @@ __global__ void bwd_bias_kernel(const BwdParams p, int64_t chunk)
 
 // ---------------------------------------------------------------------------- dW_R = R^T dr
 // Block (64 model columns m, 64 columns n = h*D + d), 256 threads with 4 x 4 outputs each.  The
-// block's 64 frequencies are computed once in double precision; an element R_delta[m] reduces the
-// angle delta * w modulo 2 pi in double precision (a multiply, a rounding and an fma: no double
-// division on the SMs' slow fp64 path) and evaluates the fp32 sine or cosine of the reduced angle
-// (within an ulp or two of the double-precision value rounded to fp32).
+// block's 64 frequencies are computed once in double precision.  For every fourth distance d4 the
+// angle d4 * w of each column is reduced modulo 2 pi in double precision (a multiply, a rounding and
+// an fma; the SMs' fp64 path is slow, so once per four rows); an element d4 + e (e < 4) takes its
+// angle as that base plus e * w in fp32 (|angle| < pi + 3: absolute error below 6e-7) and the fp32
+// sine or cosine of it.
 constexpr int kPosBwdT = 64, kPosBwdChunk = 32;
 
 __global__ void __launch_bounds__(256) pos_bwd_kernel(PosBwdParams p)
@@ -626,27 +627,39 @@ __global__ void __launch_bounds__(256) pos_bwd_kernel(PosBwdParams p)
     __shared__ float Rs[kPosBwdChunk][kPosBwdT + 1];
     __shared__ float Gs[kPosBwdChunk][kPosBwdT + 1];
     __shared__ double Ws[kPosBwdT];
+    __shared__ float Wf[kPosBwdT];                     // fp32 frequencies
+    __shared__ float Bs[kPosBwdChunk / 4][kPosBwdT];   // reduced angles of every fourth distance
     const int m0 = blockIdx.y * kPosBwdT, n0 = blockIdx.x * kPosBwdT;
     const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;      // 16 x 16 threads, 4 x 4 outputs each
     if (threadIdx.x < kPosBwdT) {
         const int k = (m0 + threadIdx.x) >> 1;
         Ws[threadIdx.x] = pow(10000.0, -(2.0 * k) / static_cast<double>(p.d_model));
+        Wf[threadIdx.x] = static_cast<float>(Ws[threadIdx.x]);
     }
     __syncthreads();
     float acc[4][4] = {};
     const int HD = p.H * p.D;
     constexpr double kTwoPi = 6.283185307179586476925;
     constexpr double kInvTwoPi = 0.159154943091895335768884;   // the quotient only picks the multiple of 2 pi
-    for (int d0 = 0; d0 < p.n_rows; d0 += kPosBwdChunk) {
+    // this block's share of the distances (blockIdx.z of gridDim.z, whole chunks); the shares add
+    // into the zeroed dW
+    const int per = (p.n_rows + kPosBwdChunk * gridDim.z - 1) / (kPosBwdChunk * gridDim.z) * kPosBwdChunk;
+    const int d_lo = blockIdx.z * per, d_hi = min(p.n_rows, d_lo + per);
+    for (int d0 = d_lo; d0 < d_hi; d0 += kPosBwdChunk) {
+        for (int e = threadIdx.x; e < (kPosBwdChunk / 4) * kPosBwdT; e += blockDim.x) {
+            const int q4 = e / kPosBwdT, cc = e % kPosBwdT;
+            const double x = static_cast<double>(d0 + 4 * q4) * Ws[cc];
+            Bs[q4][cc] = static_cast<float>(fma(-rint(x * kInvTwoPi), kTwoPi, x));
+        }
+        __syncthreads();
         for (int e = threadIdx.x; e < kPosBwdChunk * kPosBwdT; e += blockDim.x) {
             const int rr = e / kPosBwdT, cc = e % kPosBwdT;
             const int delta = d0 + rr, m = m0 + cc, n = n0 + cc;
             float rv = 0.f, gv = 0.f;
-            if (delta < p.n_rows) {
+            if (delta < d_hi) {
                 if (m < p.d_model) {
-                    const double x = static_cast<double>(delta) * Ws[cc];
-                    const float red = static_cast<float>(fma(-rint(x * kInvTwoPi), kTwoPi, x));
-                    rv = (m & 1) ? cosf(red) : sinf(red);
+                    const float ang = fmaf(static_cast<float>(rr & 3), Wf[cc], Bs[rr >> 2][cc]);
+                    rv = (m & 1) ? cosf(ang) : sinf(ang);
                 }
                 if (n < HD) gv = p.dr[static_cast<int64_t>(delta) * HD + n];
             }
@@ -674,7 +687,7 @@ __global__ void __launch_bounds__(256) pos_bwd_kernel(PosBwdParams p)
 #pragma unroll
         for (int f = 0; f < 4; ++f) {
             const int m = m0 + ty + 16 * e, n = n0 + tx + 16 * f;
-            if (m < p.d_model && n < HD) p.dW[static_cast<int64_t>(m) * p.ld_dw + n] = acc[e][f];
+            if (m < p.d_model && n < HD) atomicAdd(p.dW + static_cast<int64_t>(m) * p.ld_dw + n, acc[e][f]);
         }
 }
 
@@ -746,7 +759,12 @@ cudaError_t launch_pos_bwd(const PosBwdParams& p, cudaStream_t s)
     if (p.n_rows == 0)
         return cudaMemset2DAsync(p.dW, static_cast<size_t>(p.ld_dw) * sizeof(float), 0,
                                  sizeof(float) * p.H * p.D, p.d_model, s);
-    dim3 grid((p.H * p.D + kPosBwdT - 1) / kPosBwdT, (p.d_model + kPosBwdT - 1) / kPosBwdT);
+    const cudaError_t e = cudaMemset2DAsync(p.dW, static_cast<size_t>(p.ld_dw) * sizeof(float), 0,
+                                            sizeof(float) * p.H * p.D, p.d_model, s);
+    if (e != cudaSuccess) return e;
+    // the distances split over up to four blocks per output tile (enough blocks for every SM)
+    const int splits = p.n_rows >= 4 * kPosBwdChunk ? 4 : 1;
+    dim3 grid((p.H * p.D + kPosBwdT - 1) / kPosBwdT, (p.d_model + kPosBwdT - 1) / kPosBwdT, splits);
     pos_bwd_kernel<<<grid, 256, 0, s>>>(p);
     return cudaGetLastError();
 }
