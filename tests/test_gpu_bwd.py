@@ -108,3 +108,31 @@ def test_pos_backward_closed_form(txl):
     ref[:, 1 * D + 5] = oracle.sinusoid(37.0, dm)
     ref[:, 0] = -2.0 * oracle.sinusoid(3.0, dm)
     assert np.max(np.abs(dW.cpu().numpy() - ref)) <= 1e-6
+
+
+def test_backward_large_workload_sampled(txl):
+    """The bench's backward workload at full size (B16 H16 D64 L384 M384 clamp 1000, bf16: the
+    tensor-core kernel, in the launch the bench times): dq, dk and dv of sampled (b, h) pairs against
+    the oracle evaluated on those pairs alone (the pairs are independent; du, dv_bias and dr sum over
+    every pair and are covered by the smaller cases)."""
+    B, H, D, dm, L, M, C = 16, 16, 64, 1024, 384, 384, 1000
+    cfg = txl_inputs.custom(B=B, H=H, D=D, d_model=dm, L=L, M=M, clamp_len=C, dtype="bf16", seed=4242)
+    case = txl_inputs.make_case(cfg)
+    dO = txl_inputs.make_qkv(cfg, seed=4243, L=L, T=1)[0]
+    q, k, v = (to_dev(case[n]) for n in ("q", "k", "v"))
+    n_rows = min(M + L, C + 1)
+    r = torch.empty(n_rows, H, D, dtype=torch.bfloat16, device="cuda")
+    txl.rel_pos_gen(case["W_R"].cuda(), r, n_rows, dm, H, D)
+    mem = txl.Memory(k[:, :M], v[:, :M], 0, M)
+    u, vb = case["u"].cuda(), case["vb"].cuda()
+    out = torch.empty_like(q)
+    txl.rel_attn_fwd(q, mem, k[:, M:], v[:, M:], u, vb, r, n_rows, C, out)
+    g = txl.rel_attn_bwd(q, mem, k[:, M:], v[:, M:], u, vb, r, n_rows, C, out, to_dev(dO))
+    torch.cuda.synchronize()
+    pairs = [(0, 0), (7, 11), (15, 15)]
+    ref = oracle.rel_attn_bwd(case["q"], case["k"], case["v"], case["u"], case["vb"], case["W_R"][:, :H * D], M, M,
+                              C, dO, bh=pairs)
+    for b, h in pairs:
+        _close(g["dq"][b, :, h].cpu().numpy(), ref["dq"][b, :, h], RTOL["bf16"], "dq %d %d" % (b, h))
+        _close(g["dk_cur"][b, :, h].cpu().numpy(), ref["dk"][b, M:, h], RTOL["bf16"], "dk %d %d" % (b, h))
+        _close(g["dv_cur"][b, :, h].cpu().numpy(), ref["dv"][b, M:, h], RTOL["bf16"], "dv %d %d" % (b, h))

@@ -78,3 +78,22 @@ def test_table_from_a_projected_learned_table(txl):
     torch.cuda.synchronize()
     ref = oracle.table_attn(q, k, v, u, vb, r.double().cpu().numpy(), max_len)
     assert np.max(np.abs(out.double().cpu().numpy() - ref)) <= TOL["bf16"]
+
+
+def test_table_large_workload_sampled(txl):
+    """The bench's table-variant workload at full size (B16 L384 H16 D64 max_len 512, bf16: the
+    tensor-core kernel): sampled (b, h) pairs against the oracle on those slices."""
+    B, H, D, L, max_len = 16, 16, 64, 384, 512
+    cfg = txl_inputs.custom(B=B, H=H, D=D, d_model=2 * D, L=L, M=0, dtype="bf16", seed=5151)
+    q, k, v = txl_inputs.make_qkv(cfg, seed=5152, L=L, T=L)
+    u, vb, _ = txl_inputs.make_params(cfg, seed=5153)
+    nt = 2 * max_len - 1
+    rt = txl_inputs.make_matrix(nt, H * D, seed=5154, dtype=torch.bfloat16).reshape(nt, H, D)
+    out = torch.empty_like(q).cuda()
+    txl.rel_attn_table_fwd(q.cuda(), k.cuda(), v.cuda(), u.cuda(), vb.cuda(), rt.cuda(), max_len, out)
+    torch.cuda.synchronize()
+    for b, h in [(0, 0), (9, 4), (15, 15)]:
+        sl = (slice(b, b + 1), slice(None), slice(h, h + 1))
+        ref = oracle.table_attn(q[sl], k[sl], v[sl], u[h:h + 1], vb[h:h + 1], rt[:, h:h + 1], max_len)
+        err = np.max(np.abs(out[sl].double().cpu().numpy() - ref))
+        assert err <= TOL["bf16"], (b, h, err)
