@@ -189,7 +189,9 @@ __global__ void __launch_bounds__(kBT) bwd_tc_kernel(const BwdParams p)
     const AttnSimtParams& a = p.a;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, tg = lane & 3;
-    const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    // grid (H, B, query tiles) with the query tile slowest and reversed: the CTAs with the most key
+    // tiles are dispatched first, the short ones fill the last wave
+    const int h = blockIdx.x, b = blockIdx.y, qt = gridDim.z - 1 - blockIdx.z;
     const int i0 = kQT * qt;
     const uint32_t sbase = cvta_smem(sm);
     const float c = a.scale * 1.4426950408889634f;
@@ -552,7 +554,7 @@ cudaError_t launch_bwd_tc(const BwdParams& p, cudaStream_t s)
         if (e != cudaSuccess) return e;
         attr_done = true;
     }
-    const dim3 grid((p.a.L + kQT - 1) / kQT, p.a.H, p.a.B);
+    const dim3 grid(p.a.H, p.a.B, (p.a.L + kQT - 1) / kQT);
     bwd_tc_kernel<<<grid, kBT, BSmem::Size, s>>>(p);
     return cudaGetLastError();
 }
