@@ -38,6 +38,10 @@ def _peaks():
         return 1900.0, 1700.0, 6800.0, "fallback"
 
 
+METRIC = "rel-attn TFLOP/s (L384 M384 H16 D64 bf16), whole step: pos-gen + fused attention + memory push"
+WORKLOAD_NAME = "large: B16 H16 D64 d_model1024 L384 M384 clamp1000 (per GPU)"
+
+
 def _flops(cfg):
     import oracle
     attn = oracle.attn_flops(cfg.B, cfg.H, cfg.D, cfg.L, cfg.M)
@@ -160,14 +164,17 @@ def cpu_baseline(cfg, target_s: float = 12.0, threads=None):
     from oracle.oracle import _f64
     q, k, v, u, vb = (_f64(case[n]) for n in ("q", "k", "v", "u", "vb"))
     W = _f64(case["W_R"][:, : cfg.H * cfg.D])
-    done_flops, t_total, nb = 0, 0.0, 0
+    t_total, nb = 0.0, 0
     while nb < cfg.B and t_total < target_s:
         rows = [(nb, h, i) for h in range(cfg.H) for i in range(cfg.L)]
         t0 = time.perf_counter()
         oracle.rel_attn(q, k, v, u, vb, W, cfg.M, cfg.M, cfg.clamp_len, threads=threads, rows=rows)
         t_total += time.perf_counter() - t0
-        done_flops += oracle.attn_flops(1, cfg.H, cfg.D, cfg.L, cfg.M)
         nb += 1
+    # the metric's flops for the sampled share of one step: attention of nb batch entries plus
+    # nb / B of the position table's product (the oracle recomputes it per call, as it stands)
+    attn, pos = _flops(cfg)
+    done_flops = (attn + pos) * nb / cfg.B
     return {"value": done_flops / t_total / 1e12, "unit": "TFLOP/s", "cores": threads,
             "kind": "oracle",
             "sample": "%d of %d batch entries (all %d heads x %d queries), fp64, %.1f s" % (
@@ -236,14 +243,12 @@ def run_reference(args):
         vals.append(cpu_baseline(cfg, target_s=max(1.0, 60.0 / max(args.steps, 1))))
     dt = time.perf_counter() - t0
     value = sum(v["value"] for v in vals) / len(vals)
-    attn, _ = _flops(cfg)
     line = {
-        "impl": "reference", "metric": "rel-attn TFLOP/s (L384 M384 H16 D64)", "value": value,
+        "impl": "reference", "metric": METRIC, "value": value,
         "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * dt / max(args.steps, 1), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "large: B16 H16 D64 d_model1024 L384 M384 clamp1000",
-                   "sample": vals[-1]["sample"]},
+        "config": {"workload": WORKLOAD_NAME, "sample": vals[-1]["sample"]},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": vals[-1]["cores"],
                          "kind": "oracle", "sample": vals[-1]["sample"]},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -720,7 +725,7 @@ def run_txl(args):
     achieved = attn_flops / (t_attn_ms * 1e-3) / 1e12
     kernel_src = os.path.join(ROOT, "transformer_xl_relative_gb300", "csrc", "txl_attn_persist.cu")
     line = {
-        "metric": "rel-attn TFLOP/s (L384 M384 H16 D64 bf16), whole step: pos-gen + fused attention + memory push",
+        "metric": METRIC,
         "value": value,
         "unit": "TFLOP/s",
         "n_gpus": world,
@@ -732,7 +737,7 @@ def run_txl(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) q/k/v, N(0,0.02^2) u/v_bias, N(0,1/d_model) W_R)",
-        "config": {"workload": "large: B16 H16 D64 d_model1024 L384 M384 clamp1000 (per GPU)",
+        "config": {"workload": WORKLOAD_NAME,
                    "global_batch": B * world, "seq_len": L, "mem_len": M,
                    "l2": "4 rotating input sets, 252 MB > 129 MB L2",
                    "parallelism": "dp%d: independent replicas, no collective on the data path" % world},
