@@ -49,3 +49,21 @@ def test_key_gradient_sums_to_zero():
     g = oracle.rel_attn_bwd(c["q"], c["k"], c["v"], c["u"], c["vb"], c["W_R"], 3, 2, 4, c["dO"])
     assert np.allclose(g["dk"].sum(axis=1), 0.0, atol=1e-12)
     assert np.all(g["dk"][:, 0] == 0.0) and np.all(g["dv"][:, 0] == 0.0)      # the invalid memory key
+
+
+def test_value_gradients_sum_to_the_upstream_gradient():
+    """Every row of P sums to one, so the value gradients dv_j = sum_i P_ij dO_i of one (b, h),
+    summed over all its keys (memory included), equal sum_i dO_i."""
+    c = _case(33, B=2, L=5, M=4, H=3, D=4, dm=6)
+    g = oracle.rel_attn_bwd(c["q"], c["k"], c["v"], c["u"], c["vb"], c["W_R"], 4, 3, 6, c["dO"])
+    assert np.allclose(g["dv"].sum(axis=1), c["dO"].sum(axis=1), atol=1e-12)
+
+
+def test_clamp_zero_leaves_no_position_bias_gradient():
+    """With clamp_len 0 every pair uses r[0]: the position term (q + v_bias) . r[0] is the same for all
+    keys of a query and the softmax ignores it, so v_bias gets no gradient, and dr puts the whole
+    gradient of that term, which is zero, on row 0."""
+    c = _case(44, B=2, L=4, M=3, H=2, D=3, dm=4)
+    g = oracle.rel_attn_bwd(c["q"], c["k"], c["v"], c["u"], c["vb"], c["W_R"], 3, 3, 0, c["dO"])
+    assert np.max(np.abs(g["dvb"])) <= 1e-12
+    assert np.max(np.abs(g["dr"])) <= 1e-12
