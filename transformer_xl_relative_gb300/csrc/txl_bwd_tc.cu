@@ -37,7 +37,8 @@ constexpr int kBT = 128;                 // threads: four warps
 constexpr int kQT = 64;                  // queries per CTA
 constexpr int kKT = 64;                  // keys per tile
 constexpr int kWin = 128;                // position rows per tile window (127 used)
-constexpr int kBdPitch = 136;            // bf16 per row of the BD staging buffer
+constexpr int kBdRing = 192;             // BD ring columns per query row
+constexpr int kBdPitch = 196;            // bf16 per ring row (padded; two CTAs still fit an SM)
 
 // Shared memory (bytes).  Tiles of 64 bf16 per row are stored as 128-byte rows with the 16-byte
 // chunk index xor-ed with the row (mod 8), so that ldmatrix reads of eight rows hit eight
@@ -52,7 +53,7 @@ struct BSmem {
     static constexpr int P = R + kWin * 128;             // [64][64] P (bf16)
     static constexpr int DS = P + kQT * 128;             // [64][64] dS (bf16)
     static constexpr int G = DS + kQT * 128;             // [64][128] dS by distance
-    static constexpr int BD = G + kQT * 256;             // [64][kBdPitch] BD (bf16)
+    static constexpr int BD = G + kQT * 256;             // [64][kBdPitch] ring of BD window products (bf16)
     static constexpr int Size = BD + kQT * kBdPitch * 2;
 };
 
@@ -107,10 +108,13 @@ __device__ __forceinline__ void issue_tiles(const BwdParams& p, uint8_t* sm, int
     cp_async_commit();
 }
 
-// Scores of this warp's 16 rows against the key tile, in the log2 domain (c s), masked to -inf:
-// S = Q' K^T from the tensor cores plus BD remapped from the window product Q'' R_win^T.
+// Scores of this warp's 16 rows against key tile t (keys from j0), in the log2 domain (c s), masked
+// to -inf: S = Q' K^T from the tensor cores plus BD remapped from the window product Q'' R_win^T.
+// Window row w of tile t + 1 is window row w + 64 of tile t, so the products live in a per-row ring
+// (row w of tile t in column (w + 64 t) mod 192) and every tile after a sweep's first multiplies
+// only its 64 new rows.
 __device__ __forceinline__ void tile_scores(const BwdParams& p, uint8_t* sm, int warp, int lane, int i0, int j0,
-                                            float c, float (&s)[8][4])
+                                            int t, float c, float (&s)[8][4])
 {
     const AttnSimtParams& a = p.a;
     const uint32_t sbase = cvta_smem(sm);
@@ -133,10 +137,12 @@ __device__ __forceinline__ void tile_scores(const BwdParams& p, uint8_t* sm, int
             mma16816(s[2 * np + 1], a0, a1, a2, a3, b2, b3);
         }
     }
-    // BD over the window, two halves of 64 rows, staged as bf16 in this warp's rows
+    // BD over the window's new rows (both halves on the first tile, rows 64..127 after), staged as
+    // bf16 in this warp's ring rows
     __nv_bfloat16* bd = reinterpret_cast<__nv_bfloat16*>(sm + BSmem::BD);
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
+    const int roff = (kKT * t) % kBdRing;
+#pragma unroll 1
+    for (int half = t == 0 ? 0 : 1; half < 2; ++half) {
         float w[8][4];
 #pragma unroll
         for (int n = 0; n < 8; ++n) w[n][0] = w[n][1] = w[n][2] = w[n][3] = 0.f;
@@ -157,7 +163,7 @@ __device__ __forceinline__ void tile_scores(const BwdParams& p, uint8_t* sm, int
         }
 #pragma unroll
         for (int n = 0; n < 8; ++n) {
-            const int col = 64 * half + 8 * n + 2 * tg;
+            const int col = (64 * half + 8 * n + 2 * tg + roff) % kBdRing;
             const int r0 = 16 * warp + g;
             *reinterpret_cast<uint32_t*>(bd + r0 * kBdPitch + col) = pack2(w[n][0], w[n][1]);
             *reinterpret_cast<uint32_t*>(bd + (r0 + 8) * kBdPitch + col) = pack2(w[n][2], w[n][3]);
@@ -176,7 +182,9 @@ __device__ __forceinline__ void tile_scores(const BwdParams& p, uint8_t* sm, int
                 const int jl = 8 * n + 2 * tg + e;
                 const int j = j0 + jl;
                 const bool vis = i < a.L && j >= a.lo && j <= a.M + i && j < a.M + a.L;
-                const float x = s[n][2 * hr + e] + __bfloat162float(bd[il * kBdPitch + (il - jl + 63)]);
+                int cw = il - jl + 63 + roff;
+                cw = cw >= kBdRing ? cw - kBdRing : cw;
+                const float x = s[n][2 * hr + e] + __bfloat162float(bd[il * kBdPitch + cw]);
                 s[n][2 * hr + e] = vis ? c * x : -INFINITY;
             }
         }
@@ -255,7 +263,7 @@ __global__ void __launch_bounds__(kBT) bwd_tc_kernel(const BwdParams p)
         cp_async_wait_all();
         __syncthreads();
         float s[8][4];
-        tile_scores(p, sm, warp, lane, i0, j0, c, s);
+        tile_scores(p, sm, warp, lane, i0, j0, t, c, s);
 #pragma unroll
         for (int hr = 0; hr < 2; ++hr) {
             float mx = -INFINITY;
@@ -296,7 +304,7 @@ __global__ void __launch_bounds__(kBT) bwd_tc_kernel(const BwdParams p)
         cp_async_wait_all();
         __syncthreads();
         float s[8][4];
-        tile_scores(p, sm, warp, lane, i0, j0, c, s);
+        tile_scores(p, sm, warp, lane, i0, j0, t, c, s);
         // P, in place
 #pragma unroll
         for (int n = 0; n < 8; ++n)

@@ -7,9 +7,12 @@
 // 16w .. 16w + 15.  For key tile j0 the table indices of the pairs fill a window of 127 rows
 // starting at i0 - j0 - 63 + max_len - 1 (clamped into the table), so the table term is the window
 // product (scale q + v) W^T remapped per row through shared memory, exactly as the relative shift
-// of the Transformer-XL kernels.  bf16 mma.sync products with fp32 accumulation, an online softmax
-// in the log2 domain, O += P V with P taken straight from the accumulators; the next key tile,
-// value tile and window are copied in with cp.async while the current tile is computed.
+// of the Transformer-XL kernels.  The window of tile t + 1 shares 64 rows with the window of tile t
+// (for the same query rows), so the window products live in a per-row ring of 192 columns and every
+// tile after the first loads and multiplies only its 64 new rows.  bf16 mma.sync products with fp32
+// accumulation, an online softmax in the log2 domain, O += P V with P taken straight from the
+// accumulators; the next key tile, value tile and window rows are copied in with cp.async while the
+// current tile is computed.
 #include <cuda_bf16.h>
 
 #include "txl_internal.h"
@@ -25,7 +28,8 @@ constexpr int kTT = 128;                 // threads: four warps
 constexpr int kTQ = 64;                  // queries per CTA
 constexpr int kTK = 64;                  // keys per tile
 constexpr int kTWin = 128;               // table rows per window (127 used)
-constexpr int kTBdPitch = 136;           // bf16 per row of the window-product staging buffer
+constexpr int kTRing = 192;              // window-product ring columns per query row
+constexpr int kTBdPitch = 200;           // bf16 per ring row (padded)
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct TSmem {
@@ -34,12 +38,13 @@ struct TSmem {
     static constexpr int BUF = QB + kTQ * 128;           // two buffers of: key tile, value tile, window
     static constexpr int K = 0, V = kTK * 128, W = 2 * kTK * 128;
     static constexpr int BufBytes = W + kTWin * 128;
-    static constexpr int BD = BUF + 2 * BufBytes;        // [64][kTBdPitch] window product (bf16)
+    static constexpr int BD = BUF + 2 * BufBytes;        // [64][kTBdPitch] ring of window products (bf16)
     static constexpr int Size = BD + kTQ * kTBdPitch * 2;
 };
 
+// Copies of key tile j0, its value tile and the first n_win (64 or 128) rows of its table window.
 __device__ __forceinline__ void issue_table_tiles(const TableParams& p, uint8_t* buf, int b, int h, int i0, int j0,
-                                                  int tid)
+                                                  int n_win, int tid)
 {
     const __nv_bfloat16* kb = static_cast<const __nv_bfloat16*>(p.k);
     const __nv_bfloat16* vb = static_cast<const __nv_bfloat16*>(p.v);
@@ -60,6 +65,7 @@ __device__ __forceinline__ void issue_table_tiles(const TableParams& p, uint8_t*
     for (int x = 0; x < (kTWin * 8) / kTT; ++x) {
         const int id = tid + kTT * x;
         const int row = id >> 3, ch = id & 7;
+        if (row >= n_win) break;
         const int rr = min(max(w0 + row, 0), top);
         cp_async16(buf + TSmem::W + swz64(row, 8 * ch),
                    static_cast<const __nv_bfloat16*>(p.r) + static_cast<int64_t>(rr) * p.r_row + h * p.r_head + 8 * ch,
@@ -78,7 +84,7 @@ __global__ void __launch_bounds__(kTT) table_tc_kernel(const TableParams p)
     const uint32_t sbase = cvta_smem(sm);
     const int n_kt = (p.L + kTK - 1) / kTK;
 
-    issue_table_tiles(p, sm + TSmem::BUF, b, h, i0, 0, tid);
+    issue_table_tiles(p, sm + TSmem::BUF, b, h, i0, 0, kTWin, tid);
 
     // scale q + u and scale q + v of the CTA's rows (bf16, zero past L)
 #pragma unroll
@@ -116,7 +122,11 @@ __global__ void __launch_bounds__(kTT) table_tc_kernel(const TableParams p)
         const int j0 = kTK * t;
         cp_async_wait_all();
         __syncthreads();                 // tile t landed; every warp is done with buffer (t + 1) & 1
-        if (t + 1 < n_kt) issue_table_tiles(p, sm + TSmem::BUF + ((t + 1) & 1) * TSmem::BufBytes, b, h, i0, j0 + kTK, tid);
+        if (t + 1 < n_kt)
+            issue_table_tiles(p, sm + TSmem::BUF + ((t + 1) & 1) * TSmem::BufBytes, b, h, i0, j0 + kTK, kTK, tid);
+        // window row w of this tile sits in ring column (w + 128 t) mod 192: tile t + 1's rows 64..127
+        // are tile t's rows 0..63, already in the ring
+        const int roff = (128 * t) % kTRing;
         const uint32_t buf = sbase + TSmem::BUF + (t & 1) * TSmem::BufBytes;
 
         // S = Qa K^T
@@ -138,9 +148,10 @@ __global__ void __launch_bounds__(kTT) table_tc_kernel(const TableParams p)
                 mma16816(s[2 * np + 1], a0, a1, a2, a3, b2, b3);
             }
         }
-        // window product Qb W^T in two halves of 64 rows, staged as bf16 in this warp's rows
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
+        // window product Qb W^T of the new rows (both halves on the first tile, rows 0..63 after),
+        // staged as bf16 in this warp's ring rows
+#pragma unroll 1
+        for (int half = 0; half < (t == 0 ? 2 : 1); ++half) {
             float w[8][4];
 #pragma unroll
             for (int n = 0; n < 8; ++n) w[n][0] = w[n][1] = w[n][2] = w[n][3] = 0.f;
@@ -161,7 +172,7 @@ __global__ void __launch_bounds__(kTT) table_tc_kernel(const TableParams p)
             }
 #pragma unroll
             for (int n = 0; n < 8; ++n) {
-                const int col = 64 * half + 8 * n + 2 * tg;
+                const int col = (64 * half + 8 * n + 2 * tg + roff) % kTRing;
                 const int r0 = 16 * warp + g;
                 *reinterpret_cast<uint32_t*>(bd + r0 * kTBdPitch + col) = pack2(w[n][0], w[n][1]);
                 *reinterpret_cast<uint32_t*>(bd + (r0 + 8) * kTBdPitch + col) = pack2(w[n][2], w[n][3]);
@@ -180,7 +191,9 @@ __global__ void __launch_bounds__(kTT) table_tc_kernel(const TableParams p)
 #pragma unroll
                 for (int hr = 0; hr < 2; ++hr) {
                     const int il = 16 * warp + g + 8 * hr;
-                    const float x = s[n][2 * hr + e] + __bfloat162float(bd[il * kTBdPitch + (il - jl + 63)]);
+                    int c = il - jl + 63 + roff;
+                    c = c >= kTRing ? c - kTRing : c;
+                    const float x = s[n][2 * hr + e] + __bfloat162float(bd[il * kTBdPitch + c]);
                     s[n][2 * hr + e] = keep ? kLog2e * x : (in ? -1e9f * kLog2e : -INFINITY);
                 }
             }
