@@ -182,7 +182,10 @@ size_t txl_rel_attn_decode_workspace_size(int B, int L, int H, int D, const txl_
  *   - B*H*L*ceil((M+L)/256)*(D+2)*4 must not exceed 8388608 bytes (TXL_ERR_WORKSPACE otherwise;
  *     use txl_rel_attn_decode with a workspace for such shapes);
  *   - the first call on a device looks up the array's device address (cudaGetSymbolAddress, with
- *     that device current) and caches it; make that first call before any stream capture;
+ *     that device current) and caches it with the id of the current context; make that first
+ *     call before any stream capture.  After cudaDeviceReset the device's new context has another
+ *     id, and the first call in it looks the address up again (so that call, too, belongs before
+ *     any capture);
  *   - every call shares the array.  Each call writes every partial it reads, so nothing has to
  *     start at zero, but calls that overlap on the GPU (two streams, or two host threads on
  *     different streams) race on it and their results are undefined: keep them ordered, for

@@ -727,22 +727,61 @@ static __device__ __align__(256) float g_decode_scratch[kDecodeStaticScratchByte
 }  // namespace
 
 // Device address of the static scratch on the current device.  In host code the array's name is
-// only a host-side stand-in, so the address is looked up with cudaGetSymbolAddress, once per
-// device with that device current (the first call on a device does it), and cached.
+// only a host-side stand-in, so the address is looked up with cudaGetSymbolAddress with the device
+// current and cached per device.  The cache entry carries the unique id of the context it was
+// looked up in: after cudaDeviceReset the device gets a new primary context (the library's module
+// is loaded again, possibly elsewhere), the id differs, and the first call in the new context looks
+// the address up again instead of using a stale one.
+namespace {
+
+using PFN_ctx_get_current = CUresult (*)(CUcontext*);
+using PFN_ctx_get_id = CUresult (*)(CUcontext, unsigned long long*);
+
+bool current_context_id(unsigned long long* id)
+{
+    static PFN_ctx_get_current get_current = nullptr;
+    static PFN_ctx_get_id get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PFN_ctx_get_current>(fn);
+        fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_ctx_get_id>(fn);
+    });
+    if (!get_current || !get_id) return false;
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
+    return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
 cudaError_t decode_static_scratch(float** out)
 {
     static std::mutex mu;
     static float* addr[kMaxDevices] = {};
+    static unsigned long long ctx_of[kMaxDevices] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    // no context may be current yet on this thread: the runtime creates (or binds) the device's
+    // primary context in cudaGetSymbolAddress, after which the id is read
+    unsigned long long ctx = 0;
+    const bool have_ctx = current_context_id(&ctx);
     std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
+    if (!have_ctx || !addr[dev] || ctx_of[dev] != ctx) {
         void* ptr = nullptr;
         e = cudaGetSymbolAddress(&ptr, g_decode_scratch);
         if (e != cudaSuccess) return e;
+        if (!have_ctx && !current_context_id(&ctx)) return cudaErrorDeviceUninitialized;
         addr[dev] = static_cast<float*>(ptr);
+        ctx_of[dev] = ctx;
     }
     *out = addr[dev];
     return cudaSuccess;

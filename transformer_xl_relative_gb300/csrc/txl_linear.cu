@@ -11,14 +11,8 @@
 // a 4-stage ring; warp 1 issues 128 x 256 x 16 UMMAs into one of two TMEM accumulators; warps 2-5
 // drain the other accumulator (TMEM lane quarter = warp mod 4) to bf16 rows of Y while the next
 // tile accumulates.  Tails are handled by the TMA zero fill (rows, columns and K past the
-// extents read as zeros) and by masking the stores.
-//
-// With two or more row blocks the CTAs run as clusters of two over vertically adjacent tiles
-// (row blocks 2 i and 2 i + 1, the same column block): both need the same W slice, so each CTA
-// loads two of its four 64-column boxes and multicasts them to both, halving the W traffic from
-// L2 (the operand streams from L2, not the tensor pipe, bound this product at 128 x 256 tiles).  A
-// stage is then free only when both CTAs' UMMAs have read it: each MMA warp commits the stage to
-// the empty barrier of both CTAs (count 2).
+// extents read as zeros) and by masking the stores.  Every CTA loads its own X and W boxes; CTAs
+// of one wave that share a row or column block find it in L2.
 #include <cuda_bf16.h>
 
 #include "txl_internal.h"
@@ -47,10 +41,8 @@ struct LinSmem {
     static constexpr int Size = Misc + 16;
 };
 
-template <int CL>
 __global__ void __launch_bounds__(kLinThreads, 1) linear_kernel(const __grid_constant__ LinearParams p)
 {
-    constexpr uint16_t kPair = 0x3;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -71,7 +63,7 @@ __global__ void __launch_bounds__(kLinThreads, 1) linear_kernel(const __grid_con
     if (tid == 0) {
         for (int s = 0; s < kLinStages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], CL);                    // one commit per CTA of the cluster
+            mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&acc_full[b], 1);
@@ -84,13 +76,11 @@ __global__ void __launch_bounds__(kLinThreads, 1) linear_kernel(const __grid_con
     if (warp == kLinMmaWarp) tmem_alloc(tmem_holder, kLinTmemCols);
     tc_fence_before();
     __syncthreads();
-    if (CL > 1) cluster_sync();                          // the peer's barriers exist before any multicast
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
-    // work units: CL vertically adjacent 128 x 256 tiles; this CTA takes row block CL * i + rank
-    const int rank = CL > 1 ? static_cast<int>(cluster_ctarank()) : 0;
-    const int unit0 = blockIdx.x / CL, unit_step = gridDim.x / CL;
-    const int n_units = ((p.m_tiles + CL - 1) / CL) * p.tiles_n;
+    // work units: 128 x 256 output tiles, row block unit / tiles_n, column block unit mod tiles_n
+    const int unit0 = blockIdx.x, unit_step = gridDim.x;
+    const int n_units = p.n_tiles;
     const WaitCtl wc{abort_flag, p.err_flag, kWaitTimeoutNs};
     int never = 0;
     const WaitCtl dw{&never, nullptr, 100000000ull};
@@ -104,34 +94,21 @@ __global__ void __launch_bounds__(kLinThreads, 1) linear_kernel(const __grid_con
             int it = 0;
             bool ok = true;
             for (int unit = unit0; ok && unit < n_units; unit += unit_step) {
-                const int m0 = (CL * (unit / p.tiles_n) + rank) * 128, n0 = (unit % p.tiles_n) * 256;
+                const int m0 = (unit / p.tiles_n) * 128, n0 = (unit % p.tiles_n) * 256;
                 for (int kt = 0; kt < p.k_tiles; ++kt, ++it) {
                     const int s = it % kLinStages;
                     if (!(ok = mbar_wait(&empty[s], ((it / kLinStages) & 1) ^ 1, wc, 1))) break;
                     mbar_expect_tx(&full[s], kStageBytes);
                     uint8_t* a = smem + LinSmem::Stages + s * kStageBytes;
                     tma_load_2d(a, &p.tm_x, kt * 64, m0, &full[s]);
-                    if (CL == 1) {
 #pragma unroll
-                        for (int c = 0; c < 4; ++c)
-                            tma_load_2d(a + kABytes + c * 8192, &p.tm_w, n0 + 64 * c, kt * 64, &full[s]);
-                    } else {
-#pragma unroll
-                        for (int c = 2 * rank; c < 2 * rank + 2; ++c)
-                            tma_load_2d_multicast(a + kABytes + c * 8192, &p.tm_w, n0 + 64 * c, kt * 64, &full[s],
-                                                  kPair);
-                    }
+                    for (int c = 0; c < 4; ++c)
+                        tma_load_2d(a + kABytes + c * 8192, &p.tm_w, n0 + 64 * c, kt * 64, &full[s]);
                 }
             }
             if (!ok) {                                   // loads in flight land before teardown
                 for (int j = it - kLinStages; j < it; ++j)
                     if (j >= 0) (void)mbar_wait(&full[j % kLinStages], (j / kLinStages) & 1, dw, 2);
-            }
-            if (CL > 1) {
-                // the last phase of every stage's empty barrier: after it no commit of the peer is
-                // on its way here, and the peer has read everything this CTA multicast to it
-                for (int j = it - kLinStages; j < it; ++j)
-                    if (j >= 0) (void)mbar_wait(&empty[j % kLinStages], (j / kLinStages) & 1, dw, 7);
             }
         }
     } else if (warp == kLinMmaWarp) {
@@ -157,8 +134,7 @@ __global__ void __launch_bounds__(kLinThreads, 1) linear_kernel(const __grid_con
                     for (int kk = 0; kk < 4; ++kk)
                         umma_ss(acc, a_desc0 + off + 2 * kk, b_desc0 + off + 128 * kk, idesc,
                                 (kt > 0 || kk > 0) ? 1u : 0u);
-                    if (CL == 1) umma_commit(&empty[s]);
-                    else umma_commit_multicast(&empty[s], kPair);
+                    umma_commit(&empty[s]);
                 }
                 if (ok) umma_commit(&acc_full[b]);
             }
@@ -182,7 +158,7 @@ __global__ void __launch_bounds__(kLinThreads, 1) linear_kernel(const __grid_con
             const int b = tc & 1;
             if (!warp_wait(&acc_full[b], (tc >> 1) & 1, wc, 6)) break;
             tc_fence_after();
-            const int m0 = (CL * (unit / p.tiles_n) + rank) * 128;
+            const int m0 = (unit / p.tiles_n) * 128;
             const int row = m0 + 32 * q + lane;
             const int n0 = (unit % p.tiles_n) * 256;
             const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16) + 256u * b;
@@ -249,59 +225,10 @@ __global__ void __launch_bounds__(kLinThreads, 1) linear_kernel(const __grid_con
     }
     tc_fence_before();
     __syncthreads();
-    if (CL > 1) cluster_sync();                          // no CTA leaves while its peer may address it
     if (warp == kLinMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, kLinTmemCols);
     }
-}
-
-}  // namespace
-
-namespace {
-
-template <int CL>
-cudaError_t launch_cl(const LinearParams& p, int grid, cudaStream_t s)
-{
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kLinThreads);
-    cfg.dynamicSmemBytes = LinSmem::Size;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = CL;
-    attr[1].val.clusterDim.y = 1;
-    attr[1].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = CL > 1 ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, linear_kernel<CL>, p);
-}
-
-// Whether clusters of two CTAs of this size can be resident (checked once per process).
-bool pairs_fit()
-{
-    static int fits = -1;
-    if (fits < 0) {
-        int n = 0;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(2);
-        cfg.blockDim = dim3(kLinThreads);
-        cfg.dynamicSmemBytes = LinSmem::Size;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, linear_kernel<2>, &cfg);
-        if (e != cudaSuccess) (void)cudaGetLastError();
-        fits = (e == cudaSuccess && n > 0) ? 1 : 0;
-    }
-    return fits == 1;
 }
 
 }  // namespace
@@ -311,20 +238,13 @@ cudaError_t launch_linear(const LinearParams& p, int sm_count, cudaStream_t s)
     if (p.n_tiles == 0) return cudaSuccess;
     static bool attr_done = false;
     if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(linear_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             LinSmem::Size);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(linear_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, LinSmem::Size);
+        const cudaError_t e = cudaFuncSetAttribute(linear_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   LinSmem::Size);
         if (e != cudaSuccess) return e;
         attr_done = true;
     }
-    if (p.m_tiles >= 2 && sm_count >= 2 && pairs_fit()) {
-        const int units = ((p.m_tiles + 1) / 2) * p.tiles_n;
-        const int pairs = units < sm_count / 2 ? units : sm_count / 2;
-        return launch_cl<2>(p, 2 * pairs, s);
-    }
     const int grid = p.n_tiles < sm_count ? p.n_tiles : sm_count;
-    return launch_cl<1>(p, grid, s);
+    return launch_dependent(linear_kernel, dim3(grid), dim3(kLinThreads), LinSmem::Size, s, p);
 }
 
 }  // namespace txl

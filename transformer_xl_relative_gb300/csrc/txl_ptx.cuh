@@ -225,19 +225,6 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, i
         : "memory");
 }
 
-// The same 2D load delivered to every CTA of the cluster set in `mask`: the box lands at the
-// same shared-memory offset in each, and each one's mbarrier at `bar`'s offset receives the bytes.
-__device__ __forceinline__ void tma_load_2d_multicast(void* dst, const CUtensorMap* map, int c0, int c1,
-                                                      uint64_t* bar, uint16_t mask)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%2, %3}], [%4], %5;"
-        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar)),
-          "h"(mask)
-        : "memory");
-}
-
 // 2D tile store from this CTA's shared memory (laid out as the map's swizzle expects) to global
 // memory; elements outside the tensor's extents are not written.  Completion is tracked per
 // thread with bulk groups.
@@ -252,21 +239,6 @@ template <int N>
 __device__ __forceinline__ void bulk_wait_group_read() { asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory"); }
 // Wait until every committed group of this thread has completed its writes.
 __device__ __forceinline__ void bulk_wait_group_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
-// ------------------------------------------------------------------------------- clusters
-__device__ __forceinline__ uint32_t cluster_ctarank()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-// Every thread of every CTA of the cluster: release this CTA's prior writes, acquire the others'.
-// (The non-.aligned form: callers may arrive from diverged lanes.)
-__device__ __forceinline__ void cluster_sync()
-{
-    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
-}
 
 // Generic-proxy writes to shared memory made visible to the async proxy (tensor core, TMA).
 __device__ __forceinline__ void fence_proxy_async_smem()
@@ -346,14 +318,6 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar)
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
         ::"r"(smem_u32(bar)) : "memory");
-}
-
-// The same, arriving on the mbarrier at this offset in every CTA of the cluster set in `mask`.
-__device__ __forceinline__ void umma_commit_multicast(uint64_t* bar, uint16_t mask)
-{
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
-        ::"r"(smem_u32(bar)), "h"(mask) : "memory");
 }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread l of the warp receives lane (32*(warp%4)+l).
