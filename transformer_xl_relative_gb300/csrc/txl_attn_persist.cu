@@ -174,12 +174,31 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_persist_kernel(const __grid
     }
     int* sched_first = reinterpret_cast<int*>(smem + PSmem::Sched);
     int* sched_count = sched_first + kMaxSchedClasses;
-    if (p.sched_mode && tid < p.n_qt) {                  // this CTA's row of the table, prefix sums
-        const int q = tid;
-        int f = 0;
-        for (int c = 0; c < static_cast<int>(blockIdx.x); ++c) f += p.sched_counts[c * p.n_qt + q];
-        sched_first[q] = f;
-        sched_count[q] = p.sched_counts[blockIdx.x * p.n_qt + q];
+    if (p.sched_mode) {
+        // this CTA's row of the count table and its prefix sums over the CTAs before it: one warp
+        // per query-tile class, lanes striding over the CTAs
+        for (int q = warp; q < p.n_qt; q += kPThreads / 32) {
+            int f = 0;
+            for (int c = lane; c < static_cast<int>(blockIdx.x); c += 32) f += p.sched_counts[c * p.n_qt + q];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) f += __shfl_xor_sync(0xffffffffu, f, o);
+            if (lane == 0) {
+                sched_first[q] = f;
+                sched_count[q] = p.sched_counts[blockIdx.x * p.n_qt + q];
+            }
+        }
+    }
+    // the tensor maps are kernel parameters, valid before the previous grid ends: start fetching
+    // them now so that the first loads do not wait for them
+    if (warp == kPProducerWarp && lane == 0) {
+        tma_prefetch_desc(&p.tm_qe);
+        tma_prefetch_desc(&p.tm_qo);
+        tma_prefetch_desc(&p.tm_kcur);
+        tma_prefetch_desc(&p.tm_r);
+        if (p.M > 0) tma_prefetch_desc(&p.tm_kmem);
+    } else if (warp == kPValueWarp && lane == 0) {
+        tma_prefetch_desc(&p.tm_vcur);
+        if (p.M > 0) tma_prefetch_desc(&p.tm_vmem);
     }
     if (warp == kPMmaWarp) tmem_alloc(tmem_holder, 512);
     tc_fence_before();
@@ -198,11 +217,6 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_persist_kernel(const __grid
     if (warp == kPProducerWarp) {
         // =========================================================== TMA producer: raw q, K, r
         if (lane == 0) {
-            tma_prefetch_desc(&p.tm_qe);
-            tma_prefetch_desc(&p.tm_qo);
-            tma_prefetch_desc(&p.tm_kcur);
-            tma_prefetch_desc(&p.tm_r);
-            if (p.M > 0) tma_prefetch_desc(&p.tm_kmem);
             int nq = 0, rc = 0, kc = 0;               // loads issued per pipeline
             bool ok = true;
             auto load_r = [&](int row0, int h) -> bool {
@@ -370,8 +384,6 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_persist_kernel(const __grid
     } else if (warp == kPValueWarp) {
         // =========================================================== V tiles + P.V
         if (lane == 0) {
-            tma_prefetch_desc(&p.tm_vcur);
-            if (p.M > 0) tma_prefetch_desc(&p.tm_vmem);
             constexpr uint32_t idesc_pv = idesc_bf16(128, NPV, 0, 1);
             const uint64_t v_d = sdesc_mn_sw128(smem_u32(smem + PSmem::V), kTile);
             constexpr uint64_t kStage = kTile >> 4;
