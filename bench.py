@@ -38,6 +38,9 @@ def _peaks():
         return 1900.0, 1700.0, 6800.0, "fallback"
 
 
+NOMINAL_BF16_TFLOPS = 2250.0     # GB300 dense bf16 tensor rate, nominal (2:4-sparse figures are 2x)
+NOMINAL_HBM_GBS = 7900.0         # GB300 HBM3e bandwidth, nominal
+
 METRIC = "rel-attn TFLOP/s (L384 M384 H16 D64 bf16), whole step: pos-gen + fused attention + memory push"
 WORKLOAD_NAME = "large: B16 H16 D64 d_model1024 L384 M384 clamp1000 (per GPU)"
 
@@ -255,6 +258,187 @@ def run_reference(args):
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def _graph_us(stream, fn, n_calls, reps):
+    """Mean device time per call of `fn(i)`, i = 0 .. n_calls-1 captured in one CUDA graph and
+    replayed `reps` times back to back (CUDA events on the launching stream)."""
+    import torch
+    with torch.cuda.stream(stream):
+        for i in range(n_calls):
+            fn(i)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(n_calls):
+            fn(i)
+    with torch.cuda.stream(stream):
+        graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / (n_calls * reps)
+
+
+def _padded_randn(g, shape, hs, dt, device):
+    """[..., D] N(0, 1) values in [..., hs] storage (the base workload's 48-element head stride)."""
+    import torch
+    D = shape[-1]
+    x = torch.randn(*shape, generator=g, device=device).to(dt)
+    if hs == D:
+        return x
+    store = torch.zeros(*shape[:-1], hs, dtype=dt, device=device)
+    store[..., :D] = x
+    return store[..., :D]
+
+
+def _oracle_sample(cfg, rows, mem_valid=None, stream=False, threads=None):
+    """The oracle as it stands, on the host cores, for the listed (b, h, i) rows of one call (or of
+    the concatenated stream): (seconds, algorithmic flops of the sampled rows)."""
+    import oracle
+    import txl_inputs
+    from oracle.oracle import _f64
+    threads = threads or (os.cpu_count() or 1)
+    u, vb, W = txl_inputs.make_params(cfg, cfg.seed + 10_000)
+    W = _f64(W[:, : cfg.H * cfg.D])
+    if not stream:
+        q, k, v = txl_inputs.make_qkv(cfg, cfg.seed)
+        valid = cfg.M if mem_valid is None else mem_valid
+        t0 = time.perf_counter()
+        oracle.rel_attn(q, k, v, u, vb, W, cfg.M, valid, cfg.clamp_len, threads=threads, rows=rows)
+        dt = time.perf_counter() - t0
+        keys = [valid + i + 1 for (_, _, i) in rows]
+    else:
+        import torch
+        segs = [txl_inputs.make_segment(cfg, s_) for s_ in range(cfg.segments)]
+        q, k, v = (torch.cat([sg[j] for sg in segs], dim=1) for j in range(3))
+        t0 = time.perf_counter()
+        oracle.stream_attn(q, k, v, u, vb, W, cfg.L, cfg.M, cfg.clamp_len, threads=threads, rows=rows)
+        dt = time.perf_counter() - t0
+        keys = [t - max(0, (t // cfg.L) * cfg.L - cfg.M) + 1 for (_, _, t) in rows]
+    return dt, 6 * cfg.D * sum(keys), threads
+
+
+def bench_configs(txl, device, stream, rank, args, with_oracle):
+    """The other synthetic workloads at one GPU: base (B32 H10 D41 L150 M150), long memory
+    (B8 H16 D64 L128 M1600) and the 8-segment stream through the FIFO memory (B4 H16 D128 L512
+    M2048).  Each reports the attention kernel's time per call, TFLOP/s (6 D per visible pair),
+    query tokens/s and its fraction of the bound it sits under, plus the oracle on a sample."""
+    import torch
+    import oracle
+    import txl_inputs
+    peak, _, hbm, kind = _peaks()
+    out = {}
+    for name in ("base", "longmem"):
+        cfg = txl_inputs.CONFIGS[name]
+        B, H, D, L, M, C, hs = cfg.B, cfg.H, cfg.D, cfg.L, cfg.M, cfg.clamp_len, cfg.hs
+        dt = cfg.torch_dtype
+        g = torch.Generator(device=device).manual_seed(rank_seed(cfg.seed, rank))
+        per_set = 2 * B * (2 * (M + L) + 2 * L) * H * hs                       # q, k, v, out bytes
+        nsets = max(2, min(8, -(-400_000_000 // per_set)))   # rotate > L2
+        sets = [(_padded_randn(g, (B, L, H, D), hs, dt, device), _padded_randn(g, (B, M + L, H, D), hs, dt, device),
+                 _padded_randn(g, (B, M + L, H, D), hs, dt, device), _padded_randn(g, (B, L, H, D), hs, dt, device))
+                for _ in range(nsets)]
+        mems = [txl.Memory.full(k[:, :M], v[:, :M]) for (_, k, v, _) in sets]
+        u = (0.02 * torch.randn(H, D, generator=g, device=device)).float()
+        vb = (0.02 * torch.randn(H, D, generator=g, device=device)).float()
+        W = torch.zeros(cfg.d_model, cfg.ldw, dtype=dt, device=device)
+        W[:, : H * D] = (torch.randn(cfg.d_model, H * D, generator=g, device=device) * cfg.d_model ** -0.5).to(dt)
+        ld_r = (D + 7) // 8 * 8
+        r = torch.empty(cfg.n_rows, H, ld_r, dtype=dt, device=device)
+        txl.rel_pos_gen(W, r, cfg.n_rows, cfg.d_model, H, D)
+        q0, k0, v0, o0 = sets[0]
+        path = txl.rel_attn_path(q0, mems[0], k0[:, M:], v0[:, M:], r, o0)
+
+        def call(i):
+            q, k, v, o = sets[i % nsets]
+            txl.rel_attn_fwd(q, mems[i % nsets], k[:, M:], v[:, M:], u, vb, r, cfg.n_rows, C, o)
+
+        t_us = _graph_us(stream, call, nsets, max(2, 40 // nsets))
+        flops = oracle.attn_flops(B, H, D, L, M)
+        tf = flops / (t_us * 1e-6) / 1e12
+        nbytes = 2 * (2 * B * L * H * D + 2 * B * (M + L) * H * D + cfg.n_rows * H * D)   # q, out, k, v, r
+        gbs = nbytes / (t_us * 1e-6) / 1e9
+        ai = flops / nbytes
+        ridge = peak * 1e12 / (hbm * 1e9)
+        bound = "hbm" if ai < ridge else "tensor"
+        roof = ({"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                 "peak_source": "%s HBM copy" % kind} if bound == "hbm" else
+                {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s", "frac": tf / peak,
+                 "peak_source": "%s bf16 burst" % kind})
+        roof.update({"algorithmic_flops_per_call": flops, "algorithmic_bytes_per_call": nbytes,
+                     "arithmetic_intensity": ai, "ridge_flop_per_byte": ridge, "tensor_frac": tf / peak})
+        res = {"workload": "%s: B%d H%d D%d d_model%d L%d M%d clamp%d bf16%s" % (
+                   name, B, H, D, cfg.d_model, L, M, C, ", head stride %d" % hs if hs != D else ""),
+               "path": "fused tcgen05 (attn_persist_kernel)" if path == 1 else "SIMT", "us_per_call": t_us,
+               "tflops": tf, "tokens_per_s": B * L / (t_us * 1e-6), "roofline": roof,
+               "l2": "%d rotating input sets" % nsets}
+        if with_oracle:
+            rows = [(0, h, i) for h in range(H) for i in range(0, L, max(1, L // (64 if name == "longmem" else 150)))]
+            sec, fl, th = _oracle_sample(cfg, rows)
+            res["cpu_baseline"] = {"value": fl / sec / 1e12, "unit": "TFLOP/s", "cores": th, "kind": "oracle",
+                                   "sample": "%d of %d query rows of batch entry 0, fp64, %.1f s" % (len(rows), B * H * L, sec)}
+        out[name] = res
+        del sets, mems
+
+    # the stream: 8 consecutive segments, each attending over the FIFO memory (empty at the start)
+    # and then pushed into it; one pass = the position table + 8 x (attention + push)
+    cfg = txl_inputs.CONFIGS["stream"]
+    B, H, D, L, M, C, S = cfg.B, cfg.H, cfg.D, cfg.L, cfg.M, cfg.clamp_len, cfg.segments
+    dt = cfg.torch_dtype
+    g = torch.Generator(device=device).manual_seed(rank_seed(cfg.seed, rank))
+    segs = [tuple(torch.randn(B, L, H, D, generator=g, device=device).to(dt) for _ in range(3)) for _ in range(S)]
+    outs = [torch.empty(B, L, H, D, dtype=dt, device=device) for _ in range(S)]
+    u = (0.02 * torch.randn(H, D, generator=g, device=device)).float()
+    vb = (0.02 * torch.randn(H, D, generator=g, device=device)).float()
+    W = (torch.randn(cfg.d_model, H * D, generator=g, device=device) * cfg.d_model ** -0.5).to(dt)
+    r = torch.empty(cfg.n_rows, H, D, dtype=dt, device=device)
+    ring = txl.Memory.empty(B, M, H, D, dtype=dt, device=device)
+    path = txl.rel_attn_path(segs[0][0], ring, segs[0][1], segs[0][2], r, outs[0])
+
+    def one_pass(_i):
+        ring.restore(0, 0)
+        txl.rel_pos_gen(W, r, cfg.n_rows, cfg.d_model, H, D)
+        for s_ in range(S):
+            q, k, v = segs[s_]
+            txl.rel_attn_fwd(q, ring, k, v, u, vb, r, cfg.n_rows, C, outs[s_])
+            txl.mem_push(ring, k, v)
+
+    def attn_only(_i):
+        ring.restore(0, 0)
+        for s_ in range(S):
+            q, k, v = segs[s_]
+            txl.rel_attn_fwd(q, ring, k, v, u, vb, r, cfg.n_rows, C, outs[s_])
+            ring.restore((ring.wp + L) % M, min(ring.valid + L, M))    # the push's state, no copy
+
+    t_pass = _graph_us(stream, one_pass, 1, 10)
+    t_attn = _graph_us(stream, attn_only, 1, 10)
+    flops = sum(oracle.attn_flops(B, H, D, L, M, min(s_ * L, M)) for s_ in range(S))
+    pos_flops = 2 * cfg.n_rows * cfg.d_model * H * D
+    tf = flops / (t_attn * 1e-6) / 1e12
+    res = {"workload": "stream: B%d H%d D%d d_model%d L%d M%d clamp%d bf16, %d segments through the FIFO memory "
+                       "(empty at the start)" % (B, H, D, cfg.d_model, L, M, C, S),
+           "path": "fused tcgen05 (attn_tc_kernel<2>)" if path == 1 else "SIMT",
+           "us_per_pass": t_pass, "us_attention_per_segment": t_attn / S,
+           "tflops": tf, "tflops_pass": (flops + pos_flops) / (t_pass * 1e-6) / 1e12,
+           "tokens_per_s": S * B * L / (t_pass * 1e-6),
+           "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s", "frac": tf / peak,
+                        "peak_source": "%s bf16 burst" % kind, "algorithmic_flops_per_pass": flops},
+           "gpu_launches_per_pass": 1 + 2 * S}
+    if with_oracle:
+        T = S * L
+        rows = [(0, h, t) for h in (0, 7) for t in range(L - 1, T, L // 4)]
+        sec, fl, th = _oracle_sample(cfg, rows, stream=True)
+        res["cpu_baseline"] = {"value": fl / sec / 1e12, "unit": "TFLOP/s", "cores": th, "kind": "oracle",
+                               "sample": "%d of %d query rows (batch entry 0, heads 0 and 7, every segment), fp64, %.1f s"
+                                         % (len(rows), B * H * T, sec)}
+    out["stream"] = res
+    return out
 
 
 def bench_decode(txl, device, stream, rank, args):
@@ -551,36 +735,38 @@ def run_txl(args):
         for s in range(NSETS):           # warm-up outside capture (first-call attribute setup)
             step(s)
     torch.cuda.synchronize()
-    # The timed graph: NSETS consecutive steps.  A step's position table does not depend on the
-    # previous step's memory push, so from the second step on the table is computed on a side
-    # stream (into the other of two table buffers) while the previous push runs; every step still
-    # runs all three kernels.
+    # One CUDA graph per input set, each holding one whole step.  A step's position table does not
+    # depend on the previous step's memory push, so each step's graph also computes the next
+    # step's table on a side stream (into the other of two table buffers) while its own push
+    # runs; every step still runs all three kernels.  Exactly W warm-up and K timed steps replay
+    # the graphs in rotation.
     r_bufs = [r, torch.empty_like(r)]
     side = torch.cuda.Stream(device=device)
 
-    def steps_overlapped():
-        txl.rel_pos_gen(W, r_bufs[0], n_rows, cfg.d_model, H, D)
-        for s in range(NSETS):
-            q, k, v = sets[s]
-            txl.rel_attn_fwd(q, mems[s], k[:, M:], v[:, M:], u, vb, r_bufs[s % 2], n_rows, C, outs[s])
-            if s + 1 < NSETS:
-                e_attn = torch.cuda.Event()
-                e_attn.record(stream)
-                side.wait_event(e_attn)
-                with torch.cuda.stream(side):
-                    txl.rel_pos_gen(W, r_bufs[(s + 1) % 2], n_rows, cfg.d_model, H, D)
-                e_pos = torch.cuda.Event()
-                e_pos.record(side)
-            txl.mem_push(ring, k[:, M:], v[:, M:])
-            if s + 1 < NSETS:
-                stream.wait_event(e_pos)
+    def step_overlapped(s):
+        q, k, v = sets[s]
+        txl.rel_attn_fwd(q, mems[s], k[:, M:], v[:, M:], u, vb, r_bufs[s % 2], n_rows, C, outs[s])
+        e_attn = torch.cuda.Event()
+        e_attn.record(stream)
+        side.wait_event(e_attn)
+        with torch.cuda.stream(side):
+            txl.rel_pos_gen(W, r_bufs[(s + 1) % 2], n_rows, cfg.d_model, H, D)
+        e_pos = torch.cuda.Event()
+        e_pos.record(side)
+        txl.mem_push(ring, k[:, M:], v[:, M:])
+        stream.wait_event(e_pos)
 
     with torch.cuda.stream(stream):
-        steps_overlapped()
+        txl.rel_pos_gen(W, r_bufs[0], n_rows, cfg.d_model, H, D)
+        for s in range(NSETS):
+            step_overlapped(s)
     torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        steps_overlapped()
+    graphs = []
+    for s in range(NSETS):
+        g_ = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_, stream=stream):
+            step_overlapped(s)
+        graphs.append(g_)
     attn_graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(attn_graph, stream=stream):
         for s in range(NSETS):
@@ -595,15 +781,15 @@ def run_txl(args):
         for s in range(NSETS):
             txl.mem_push(ring, sets[s][1][:, M:], sets[s][2][:, M:])
 
-    reps = max(1, math.ceil(args.steps / NSETS))
-    steps = reps * NSETS
-    warm_reps = max(1, math.ceil(args.warmup / NSETS))
+    steps = max(1, args.steps)
+    reps = max(1, math.ceil(steps / NSETS))
     sampler = ClockSampler(device.index if device.index is not None else 0)
     sampler.start()
     time.sleep(0.3)
     with torch.cuda.stream(stream):
-        for _ in range(warm_reps):
-            graph.replay()
+        txl.rel_pos_gen(W, r_bufs[0], n_rows, cfg.d_model, H, D)
+        for i in range(args.warmup):
+            graphs[i % NSETS].replay()
     torch.cuda.synchronize()
     _barrier(world)
     torch.cuda.synchronize()
@@ -611,8 +797,8 @@ def run_txl(args):
     wall0 = time.time()
     with torch.cuda.stream(stream):
         ev0.record(stream)
-        for _ in range(reps):
-            graph.replay()
+        for i in range(steps):
+            graphs[(args.warmup + i) % NSETS].replay()
         ev1.record(stream)
     torch.cuda.synchronize()
     _barrier(world)
@@ -632,7 +818,7 @@ def run_txl(args):
             attn_graph.replay()
         a1.record(stream)
     torch.cuda.synchronize()
-    t_attn_ms = a0.elapsed_time(a1) / steps
+    t_attn_ms = a0.elapsed_time(a1) / (reps * NSETS)
 
     def graph_ms(g, reps_):
         with torch.cuda.stream(stream):
@@ -717,6 +903,8 @@ def run_txl(args):
     layer = bench_layer(txl, device, stream, rank, args)
     backward = bench_backward(txl, device, stream, rank, args)
     table = bench_table(txl, device, stream, rank, args)
+    configs = bench_configs(txl, device, stream, rank, args,
+                            with_oracle=rank == 0 and world == 1 and not args.no_cpu_baseline)
 
     attn_flops, pos_flops = _flops(cfg)
     step_flops = attn_flops + pos_flops
@@ -730,7 +918,7 @@ def run_txl(args):
         "unit": "TFLOP/s",
         "n_gpus": world,
         "steps": steps,
-        "warmup": warm_reps * NSETS,
+        "warmup": args.warmup,
         "ms_per_step": t_step_ms,
         "higher_is_better": True,
         "scaling": "weak",
@@ -755,6 +943,7 @@ def run_txl(args):
         "layer": layer,
         "backward": backward,
         "table": table,
+        "configs": configs,
         "roofline": {"kernel": "txl_rel_attn_fwd (attn_persist_kernel)", "bound": "tensor",
                      "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "peak_source": "%s bf16 burst (MEASURED_PEAKS.json)" % peak_kind
@@ -762,8 +951,13 @@ def run_txl(args):
                      "traffic": _profile_traffic(kernel_src),
                      "algorithmic_flops_per_launch": attn_flops},
     }
+    # nominal GB300 figures (dense bf16 tensor rate; HBM3e bandwidth), beside the measured peaks
+    line["nominal_peaks"] = {"bf16_dense_tflops": NOMINAL_BF16_TFLOPS, "hbm_gbs": NOMINAL_HBM_GBS,
+                             "attn_frac_of_nominal_bf16": achieved / NOMINAL_BF16_TFLOPS,
+                             "source": "NVIDIA GB300 nominal dense bf16 rate and HBM3e bandwidth"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg)
+        line["cpu_baseline"]["single_thread"] = cpu_baseline(cfg, target_s=1.0, threads=1)
         for key, base in row_baselines().items():
             line[key]["cpu_baseline"] = base
     if rank == 0:
@@ -782,6 +976,16 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["txl", "reference"], default="txl")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
+    world = os.environ.get("WORLD_SIZE")
+    if args.gpus > 1 and world is None:
+        # one process per GPU: relaunch this command under torch.distributed.run
+        cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", str(args.gpus),
+               "--master-addr", "127.0.0.1", "--master-port", os.environ.get("MASTER_PORT", "29517"),
+               os.path.abspath(__file__), *(argv if argv is not None else sys.argv[1:])]
+        return subprocess.call(cmd)
+    if world is not None and int(world) != args.gpus:
+        sys.stderr.write("bench.py: --gpus %d but WORLD_SIZE=%s\n" % (args.gpus, world))
+        return 2
     if args.impl == "reference":
         return run_reference(args)
     return run_txl(args)

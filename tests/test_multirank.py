@@ -48,3 +48,20 @@ def test_two_ranks_max_time_and_aggregate():
     assert [t for _, t, _, _ in res] == [2.0, 2.0]                 # both see the slowest rank
     assert res[0][2] == pytest.approx(2 * 21.762e9 / 2e-3 / 1e12)  # whole-job work / job time
     assert res[0][3] != res[1][3]                                  # independent replicas
+
+
+def test_gpus_flag_launches_one_process_per_gpu(monkeypatch):
+    """`bench.py --gpus N` outside a launcher relaunches itself under torch.distributed.run with N
+    processes; inside one, a WORLD_SIZE that disagrees with --gpus is refused."""
+    import bench
+    seen = []
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    monkeypatch.setattr(bench.subprocess, "call", lambda cmd: seen.append(cmd) or 0)
+    assert bench.main(["--gpus", "4", "--steps", "7", "--warmup", "3"]) == 0
+    cmd = seen[0]
+    assert cmd[1:4] == ["-m", "torch.distributed.run", "--nnodes=1"]
+    assert cmd[cmd.index("--nproc-per-node") + 1] == "4"
+    assert cmd[cmd.index("--master-addr") + 1] == "127.0.0.1"
+    assert cmd[-6:] == ["--gpus", "4", "--steps", "7", "--warmup", "3"]
+    monkeypatch.setenv("WORLD_SIZE", "3")
+    assert bench.main(["--gpus", "2"]) == 2

@@ -243,8 +243,8 @@ txl_status txl_rel_attn_fwd(int B, int L, int H, int D, int clamp_len, const txl
         p.o_sb = out->stride_b;
         p.o_st = out->stride_t;
         p.o_sh = out->stride_h;
-        p.out_vec = (D % 8) == 0 && a16(out->ptr) && s16(out->stride_b, 2) && s16(out->stride_t, 2) &&
-                    s16(out->stride_h, 2);
+        p.out_a16 = a16(out->ptr) && s16(out->stride_b, 2) && s16(out->stride_t, 2) && s16(out->stride_h, 2);
+        p.out_vec = (D % 8) == 0 && p.out_a16;
         p.B = B; p.L = L; p.H = H; p.D = D; p.M = M;
         p.lo = M - valid;
         p.wp = wp;

@@ -617,13 +617,15 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_persist_kernel(const __grid
             }
 
             // ---- epilogue: O / (l_0 + l_1) -> bf16 -> out[b, i0 + pi, h, :].  O is released to the
-            // next item's P.V as soon as it is read.  Each thread stages its normalised half row in
-            // the front of its (now dead) ring row; the pair of warps then writes its 32 rows as
-            // whole 128-byte lines, four rows per store instruction instead of 32 half lines.
+            // next item's P.V as soon as it is read.  With 16-byte aligned output rows each thread
+            // stages its normalised half row in the front of its (now dead) ring row; the pair of
+            // warps then writes its 32 rows as whole 128-byte lines, four rows per store
+            // instruction instead of 32 half lines (a chunk past d_head's end, when D % 8 != 0,
+            // element by element).  Other layouts store element by element from registers.
             if (ok) ok = warp_spin(bar.o_full, n & 1, wc, 35);
             xchg[2 * (it.n_t & 1) + hf] = l_half;
             pair_bar(li);
-            const bool staged = p.out_vec != 0;
+            const bool staged = p.out_a16 != 0;
             if (ok) {
                 uint32_t o[32];
                 tc_fence_after();
@@ -649,8 +651,9 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_persist_kernel(const __grid
                     if (i < p.L) {
                         __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + it.b * p.o_sb +
                                               static_cast<int64_t>(i) * p.o_st + it.h * p.o_sh;
-                        for (int k = 0; k < 32 && d0 + k < p.D; ++k)
-                            orow[d0 + k] = __float2bfloat16_rn(__uint_as_float(o[k]) * inv_l);
+#pragma unroll
+                        for (int k = 0; k < 32; ++k)
+                            if (d0 + k < p.D) orow[d0 + k] = __float2bfloat16_rn(__uint_as_float(o[k]) * inv_l);
                     }
                 }
             }
@@ -668,7 +671,15 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_persist_kernel(const __grid
                         const uint4 v = *reinterpret_cast<const uint4*>(bd0 + r * kBdPitchWords + 4 * c);
                         __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + it.b * p.o_sb +
                                               static_cast<int64_t>(i) * p.o_st + it.h * p.o_sh;
-                        *reinterpret_cast<uint4*>(orow + 8 * c) = v;
+                        if (8 * c + 8 <= p.D) {
+                            *reinterpret_cast<uint4*>(orow + 8 * c) = v;
+                        } else {                    // the chunk holding d_head's end (D % 8 != 0)
+                            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                if (8 * c + e < p.D)
+                                    orow[8 * c + e] = __ushort_as_bfloat16(static_cast<unsigned short>(w[e >> 1] >> (16 * (e & 1))));
+                        }
                     }
                 }
             }

@@ -97,6 +97,7 @@ struct AttnTcParams {
     int k_steps;                 // ceil(D / 16): UMMA K steps for the Q.K and Q.r products
     float qscale;                // scale * log2(e)
     int out_vec;                 // out rows take 16-byte stores: D % 8 == 0, 16-byte base and strides
+    int out_a16;                 // out base and strides 16-byte aligned (whole 8-element chunks take 16-byte stores)
     int* err_flag;
     // persistent kernel only: sched_counts[c * n_qt + qt] = items of query tile qt that CTA c
     // processes (0 entries when sched_mode == 0: serpentine order instead)
