@@ -503,10 +503,11 @@ def bench_decode(txl, device, stream, rank, args):
 
 
 def bench_layer(txl, device, stream, rank, args):
-    """The attention-layer step over hidden states (txl_rel_attn_layer) on the large workload:
-    q|k|v projection of the segment (6144 x 3072 x 1024), the fused attention over [memory ++
-    segment], the output projection (6144 x 1024 x 1024) and the push of the segment's K/V, plus
-    the position table, per step.  Eight hidden-state sets (100 MB) rotate with the 25 MB K/V ring,
+    """The attention-layer step over hidden states on the large workload, as
+    txl_rel_attn_layer_fused runs it: the q|k|v projection of the segment (6144 x 3072 x 1024)
+    writing K and V straight into the memory ring, the fused attention over [memory ++ segment]
+    read from the ring, the output projection (6144 x 1024 x 1024), plus the position table, per
+    step (the unfused step, with its separate push, is timed beside it).  Eight hidden-state sets (100 MB) rotate with the 25 MB K/V ring,
     the 50 MB workspace and 8 MB of weights, so a step does not find its inputs L2-warm.  The
     q|k|v product is also timed alone (same rotation) against the measured bf16 peak."""
     import torch
@@ -525,10 +526,15 @@ def bench_layer(txl, device, stream, rank, args):
     hs = [torch.randn(B, L, dm, generator=g, device=device).to(dt) for _ in range(nsets)]
     ys = [torch.empty(B, L, dm, dtype=dt, device=device) for _ in range(2)]
     mem = txl.Memory.empty(B, M, H, D, device=device)
+    ring = txl.Memory.empty(B, M + L, H, D, device=device)       # memory of M positions + the segment
     ws = torch.empty(txl.rel_attn_layer_workspace_size(B, L, H, D), dtype=torch.uint8, device=device)
     qkv = ws[: B * L * 3 * HD * 2].view(dt).view(B * L, 3 * HD)
 
     def step(i):
+        txl.rel_pos_gen(W_R, r, n_rows, dm, H, D)
+        txl.rel_attn_layer_fused(hs[i], ring, M, W_qkv, W_o, u, vb, r, n_rows, C, H, D, ys[i & 1], workspace=ws)
+
+    def step_unfused(i):
         txl.rel_pos_gen(W_R, r, n_rows, dm, H, D)
         txl.rel_attn_layer(hs[i], mem, W_qkv, W_o, u, vb, r, n_rows, C, H, D, ys[i & 1], workspace=ws)
 
@@ -557,6 +563,7 @@ def bench_layer(txl, device, stream, rank, args):
         return e0.elapsed_time(e1) * 1e3 / (nsets * reps)
 
     t_step = timed(step)
+    t_unfused = timed(step_unfused)
     t_proj = timed(proj)
     # every position of the memory is valid once the warm-up has pushed two segments
     attn = 6 * D * B * H * (L * M + L * (L + 1) // 2)
@@ -566,7 +573,10 @@ def bench_layer(txl, device, stream, rank, args):
     achieved = pflops / (t_proj * 1e-6) / 1e12
     return {"workload": "layer: B16 L384 M384 H16 D64 d_model1024 clamp1000 bf16 (hidden states in, y out)",
             "us_per_step": t_step, "tflops": flops / (t_step * 1e-6) / 1e12,
-            "algorithmic_flops_per_step": flops, "gpu_launches_per_step": 5,
+            "algorithmic_flops_per_step": flops, "gpu_launches_per_step": 4,
+            "step": "txl_rel_attn_layer_fused: position table, q|k|v product writing K and V into the ring "
+                    "(no push), attention from the ring, output product",
+            "us_per_step_unfused": t_unfused, "gpu_launches_per_step_unfused": 5,
             "roofline": {"kernel": "txl_linear (linear_kernel, q|k|v 6144x3072x1024)", "bound": "tensor",
                          "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                          "peak_source": "%s bf16 burst" % kind, "us_per_launch": t_proj,

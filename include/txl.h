@@ -259,6 +259,37 @@ txl_status txl_rel_attn_layer(int B, int L, int H, int D, int d_model, int clamp
 size_t txl_rel_attn_layer_workspace_size(int B, int L, int H, int D);
 
 /*
+ * txl_rel_attn_layer_fused -- the layer step of txl_rel_attn_layer in three launches, with the memory
+ * push folded into the projection.  The memory of mem_len positions lives in a ring of at least
+ * mem_len + L slots (mem->M slots; mem->wp = slot of the oldest memory position, mem->valid = valid
+ * memory positions, 0 .. mem_len): the q|k|v product writes the segment's K and V straight into the
+ * L slots after the memory, (wp + mem_len + t) mod mem->M, and Q into the workspace; the fused
+ * attention reads memory and segment keys from the ring (logical key j of [memory ++ segment] in
+ * slot (wp + j) mod mem->M); the output product follows; then, instead of a copy, the window moves:
+ * mem->wp += L (mod mem->M), mem->valid = min(valid + L, mem_len).  The function is that of
+ * txl_rel_attn_layer with a memory of mem_len positions ("Transformer-XL 和相对位置编码" §2.3.1: the
+ * cached states of the previous segment extend the keys and values; "TransformerXL 相对位置编码" §3.1:
+ * projections without bias).
+ *   h, W_qkv, W_o, u, v_bias, r, ld_r, n_rows, clamp_len, scale, y, ld_y, err_flag : as txl_rel_attn_layer
+ *            (n_rows >= min(mem_len + L, clamp_len + 1)).
+ *   mem    : device bf16 rings k, v, dense [B][mem->M][H][D]; a ring starts zeroed (wp = 0, valid = 0):
+ *            slots past the valid memory are read (and masked), so they must hold finite values.
+ *   workspace : device, >= txl_rel_attn_layer_fused_workspace_size(B, L, H, D) bytes, 16-byte aligned.
+ * Limits (TXL_ERR_UNSUPPORTED otherwise; use txl_rel_attn_layer): bf16; D <= 64 and a multiple of 8;
+ * H*D a multiple of 64; d_model a multiple of 8; L, mem_len, mem->M and mem->wp multiples of 128.
+ */
+txl_status txl_rel_attn_layer_fused(int B, int L, int H, int D, int d_model, int clamp_len,
+                                    const void* h, int64_t ld_h, txl_mem* mem, int mem_len,
+                                    const void* W_qkv, const void* W_o,
+                                    const float* u, const float* v_bias,
+                                    const void* r, int64_t ld_r, int n_rows, float scale,
+                                    void* y, int64_t ld_y, void* workspace, size_t workspace_bytes,
+                                    int* err_flag, void* stream);
+
+/* Bytes of device workspace txl_rel_attn_layer_fused needs: B*L*H*D*4 (0 for an empty shape). */
+size_t txl_rel_attn_layer_fused_workspace_size(int B, int L, int H, int D);
+
+/*
  * txl_rel_attn_bwd -- gradients of one txl_rel_attn_fwd call for an upstream gradient d_out,
  * by the chain rule through the four-term score ("Transformer-XL 和相对位置编码" §2.3.2) and the
  * softmax: with q' = q + u, q'' = q + v_bias, P the attention weights and dS_ij =

@@ -176,3 +176,79 @@ def test_layer_rejections(txl):
     with pytest.raises(txl.TxlError):                    # fp32 projections are not provided
         txl.linear(torch.zeros(4, 8, device="cuda"), torch.zeros(8, 8, device="cuda"))
     assert mem.valid == 0 and mem.wp == 0                # a rejected call leaves the memory alone
+
+
+# --------------------------------------------------------------------------- fused layer step
+def _fused_stream(txl, cfg, S, extra_slots=0):
+    """S steps of txl_rel_attn_layer_fused (memory of M positions in a ring of M + L + extra_slots
+    slots) beside S steps of txl_rel_attn_layer on the same inputs."""
+    lay = txl_inputs.make_layer(cfg, segments=S)
+    H, D, L, M, dm = cfg.H, cfg.D, cfg.L, cfg.M, cfg.d_model
+    n_rows = min(M + L, cfg.clamp_len + 1)
+    r = torch.empty(n_rows, H, ld_r_for(D), dtype=torch.bfloat16, device="cuda")
+    txl.rel_pos_gen(lay["W_R"].cuda(), r, n_rows, dm, H, D)
+    ring = txl.Memory.empty(cfg.B, M + L + extra_slots, H, D)
+    mem = txl.Memory.empty(cfg.B, M, H, D) if M > 0 else None
+    h = lay["h"].cuda()
+    W_qkv, W_o, u, vb = lay["W_qkv"].cuda(), lay["W_o"].cuda(), lay["u"].cuda(), lay["vb"].cuda()
+    fused, plain = [], []
+    for s in range(S):
+        hs = h[:, s * L:(s + 1) * L].contiguous()
+        fused.append(txl.rel_attn_layer_fused(hs, ring, M, W_qkv, W_o, u, vb, r, n_rows, cfg.clamp_len, H, D))
+        plain.append(txl.rel_attn_layer(hs, mem, W_qkv, W_o, u, vb, r, n_rows, cfg.clamp_len, H, D))
+    torch.cuda.synchronize()
+    return lay, fused, plain, ring
+
+
+FUSED = [
+    # B, H, D, d_model, L, M, clamp, segments, extra ring slots
+    (2, 2, 64, 128, 128, 128, 1000, 3, 0),   # memory of one segment, the ring exactly M + L
+    (1, 4, 64, 256, 128, 256, 100, 3, 0),    # memory of two segments, clamp inside the window
+    (2, 2, 64, 192, 256, 128, 1000, 2, 0),   # segment longer than the memory
+    (1, 2, 64, 128, 128, 256, 1000, 5, 128), # spare slots: the window wraps around the ring
+    (2, 2, 64, 128, 128, 0, 1000, 2, 0),     # no memory
+]
+
+
+@pytest.mark.parametrize("shape", FUSED, ids=["B%dH%dD%d_dm%d_L%dM%d_C%d_S%d_x%d" % s for s in FUSED])
+def test_fused_layer_matches_oracle_and_unfused(txl, shape):
+    B, H, D, dm, L, M, C, S, extra = shape
+    cfg = txl_inputs.custom(B=B, H=H, D=D, d_model=dm, L=L, M=M, clamp_len=C, dtype="bf16", seed=70 + S + L + M)
+    lay, fused, plain, ring = _fused_stream(txl, cfg, S, extra)
+    for s in range(S):                      # the same products and the same attention, step by step
+        assert torch.equal(fused[s], plain[s]), s
+    HD = H * D
+    got = torch.cat(fused, dim=1).double().cpu().numpy()
+    Wf = lay["W_qkv"].double().numpy()
+    ref = oracle.stream_layer(lay["h"].double().numpy(), Wf[:, :HD], Wf[:, HD:2 * HD], Wf[:, 2 * HD:],
+                              lay["W_o"].double().numpy(), lay["u"], lay["vb"], lay["W_R"][:, :HD], H, D, L, M, C)
+    err = np.max(np.abs(got - ref))
+    assert np.isfinite(got).all() and err <= TOL["bf16"], err
+    assert ring.valid == min(S * L, M) and ring.wp == (S * L) % (M + L + extra)
+
+
+def test_fused_layer_large_workload(txl):
+    """The large workload's layer step (B16 H16 D64 d_model 1024 L384 M384), two steps in a ring
+    of 768 slots, bit-identical to the unfused step."""
+    cfg = txl_inputs.CONFIGS["large"]
+    _, fused, plain, ring = _fused_stream(txl, cfg, 2)
+    assert torch.equal(fused[0], plain[0]) and torch.equal(fused[1], plain[1])
+    assert ring.valid == cfg.M and ring.wp == 0
+
+
+def test_fused_layer_rejections(txl):
+    cfg = txl_inputs.custom(B=1, H=2, D=64, d_model=128, L=128, M=128, dtype="bf16", seed=3)
+    lay = txl_inputs.make_layer(cfg)
+    r = torch.zeros(257, 2, 64, dtype=torch.bfloat16, device="cuda")
+    h, W_qkv, W_o, u, vb = (lay[n].cuda() for n in ("h", "W_qkv", "W_o", "u", "vb"))
+    small = txl.Memory.empty(1, 128, 2, 64)              # no room for the segment after the memory
+    with pytest.raises(txl.TxlError):
+        txl.rel_attn_layer_fused(h, small, 128, W_qkv, W_o, u, vb, r, 257, 1000, 2, 64)
+    odd = txl.Memory.empty(1, 320, 2, 64)                # slots not a multiple of 128
+    with pytest.raises(txl.TxlError):
+        txl.rel_attn_layer_fused(h, odd, 128, W_qkv, W_o, u, vb, r, 257, 1000, 2, 64)
+    ring = txl.Memory.empty(1, 256, 2, 64)
+    with pytest.raises(txl.TxlError):                    # workspace too small
+        txl.rel_attn_layer_fused(h, ring, 128, W_qkv, W_o, u, vb, r, 257, 1000, 2, 64,
+                                 workspace=torch.empty(64, dtype=torch.uint8, device="cuda"))
+    assert (small.wp, small.valid, odd.wp, odd.valid, ring.wp, ring.valid) == (0, 0, 0, 0, 0, 0)

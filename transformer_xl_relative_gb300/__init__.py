@@ -15,6 +15,8 @@ from .api import (  # noqa: F401
     rel_attn_fwd,
     rel_attn_layer,
     rel_attn_layer_workspace_size,
+    rel_attn_layer_fused,
+    rel_attn_layer_fused_workspace_size,
     rel_attn_path,
     rel_attn_table_fwd,
     rel_pos_bwd,

@@ -244,6 +244,43 @@ def rel_attn_layer(h: torch.Tensor, mem: Memory | None, W_qkv: torch.Tensor, W_o
     return y
 
 
+def rel_attn_layer_fused_workspace_size(B: int, L: int, H: int, D: int) -> int:
+    """Bytes of workspace rel_attn_layer_fused needs (txl_rel_attn_layer_fused_workspace_size)."""
+    return int(_lib().txl_rel_attn_layer_fused_workspace_size(B, L, H, D))
+
+
+def rel_attn_layer_fused(h: torch.Tensor, mem: Memory, mem_len: int, W_qkv: torch.Tensor, W_o: torch.Tensor,
+                         u: torch.Tensor, v_bias: torch.Tensor, r: torch.Tensor, n_rows: int, clamp_len: int,
+                         n_head: int, d_head: int, y: torch.Tensor | None = None, scale: float = 0.0,
+                         workspace: torch.Tensor | None = None, err_flag: torch.Tensor | None = None,
+                         stream=None) -> torch.Tensor:
+    """The layer step of rel_attn_layer with the memory push folded into the projection
+    (txl_rel_attn_layer_fused): `mem` is a ring of at least mem_len + L slots (Memory.empty(B,
+    slots, H, D)) holding a memory of mem_len positions.  Returns y [B, L, d_model]."""
+    B, L, d_model = h.shape
+    if h.stride(2) != 1 or (B > 1 and h.stride(0) != L * h.stride(1)):
+        raise ValueError("h must be [B, L, d_model] with rows b*L + t evenly spaced")
+    if u.dtype != torch.float32 or v_bias.dtype != torch.float32:
+        raise TypeError("u and v_bias are fp32 [H, D]")
+    if not (u.is_contiguous() and v_bias.is_contiguous() and W_qkv.is_contiguous() and W_o.is_contiguous()):
+        raise ValueError("u, v_bias, W_qkv and W_o must be contiguous")
+    if y is None:
+        y = torch.empty(B, L, d_model, dtype=h.dtype, device=h.device)
+    if y.stride(2) != 1 or (B > 1 and y.stride(0) != L * y.stride(1)):
+        raise ValueError("y must be [B, L, d_model] with rows b*L + t evenly spaced")
+    need = rel_attn_layer_fused_workspace_size(B, L, n_head, d_head)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=h.device)
+    nbytes = workspace.numel() * workspace.element_size()
+    st = _lib().txl_rel_attn_layer_fused(
+        B, L, n_head, d_head, d_model, int(clamp_len), h.data_ptr(), h.stride(1), ctypes.byref(mem.c_struct),
+        int(mem_len), W_qkv.data_ptr(), W_o.data_ptr(), u.data_ptr(), v_bias.data_ptr(), r.data_ptr(), r.stride(1),
+        int(n_rows), float(scale), y.data_ptr(), y.stride(1), workspace.data_ptr(), nbytes,
+        err_flag.data_ptr() if err_flag is not None else None, _stream(stream))
+    check(st, "txl_rel_attn_layer_fused")
+    return y
+
+
 def rel_attn_bwd(q: torch.Tensor, mem: Memory | None, k_cur: torch.Tensor, v_cur: torch.Tensor,
                  u: torch.Tensor, v_bias: torch.Tensor, r: torch.Tensor, n_rows: int, clamp_len: int,
                  out: torch.Tensor, d_out: torch.Tensor, scale: float = 0.0,

@@ -202,6 +202,93 @@ int txl_rel_attn_path(int B, int L, int H, int D, const txl_view* q, const txl_m
     return attn_tc_eligible(B, L, H, D, q, mem, k_cur, v_cur, r, ld_r, dtype) ? 1 : 2;
 }
 
+namespace {
+
+// The fused tcgen05 attention (persistent kernel for d_head <= 64, one CTA per query tile above).
+// ring_slots > 0: every key lives in the memory ring (mem->k, mem->v of ring_slots slots); logical
+// key j (0 <= j < M + L, M = mem->M the memory length) in slot (wp + j) mod ring_slots.
+txl_status attn_tc_launch(int B, int L, int H, int D, int clamp_len, const txl_view* q, const txl_mem* mem,
+                          const txl_view* k_cur, const txl_view* v_cur, const float* u, const float* v_bias,
+                          const void* r, int64_t ld_r, int n_rows, float scale, const txl_view* out, int* err_flag,
+                          cudaStream_t s, int ring_slots)
+{
+    const int M = (mem && mem->M > 0) ? mem->M : 0;
+    const int valid = M > 0 ? mem->valid : 0;
+    const int wp = (M > 0 || ring_slots > 0) ? mem->wp : 0;
+    if (!encoder_ready()) return TXL_ERR_CUDA;
+    AttnTcParams p;
+    std::memset(&p, 0, sizeof(p));
+    const int slots = ring_slots > 0 ? ring_slots : M;
+    bool ok = encode_view4(&p.tm_q, q->ptr, D, H, L, B, q->stride_h, q->stride_t, q->stride_b) &&
+              encode_rtab(&p.tm_r, r, D, H, n_rows, ld_r);
+    if (ok && ring_slots > 0) {
+        ok = encode_view4(&p.tm_kmem, mem->k, D, H, slots, B, mem->stride_h, mem->stride_t, mem->stride_b) &&
+             encode_view4(&p.tm_vmem, mem->v, D, H, slots, B, mem->stride_h, mem->stride_t, mem->stride_b);
+        p.tm_kcur = p.tm_kmem;
+        p.tm_vcur = p.tm_vmem;
+    } else if (ok) {
+        ok = encode_view4(&p.tm_kcur, k_cur->ptr, D, H, L, B, k_cur->stride_h, k_cur->stride_t, k_cur->stride_b) &&
+             encode_view4(&p.tm_vcur, v_cur->ptr, D, H, L, B, v_cur->stride_h, v_cur->stride_t, v_cur->stride_b);
+        if (ok && M > 0)
+            ok = encode_view4(&p.tm_kmem, mem->k, D, H, M, B, mem->stride_h, mem->stride_t, mem->stride_b) &&
+                 encode_view4(&p.tm_vmem, mem->v, D, H, M, B, mem->stride_h, mem->stride_t, mem->stride_b);
+        else if (ok) {
+            p.tm_kmem = p.tm_kcur;
+            p.tm_vmem = p.tm_vcur;
+        }
+    }
+    if (!ok) return TXL_ERR_CUDA;
+    p.u = u;
+    p.vb = v_bias;
+    p.out = out->ptr;
+    p.o_sb = out->stride_b;
+    p.o_st = out->stride_t;
+    p.o_sh = out->stride_h;
+    p.out_a16 = a16(out->ptr) && s16(out->stride_b, 2) && s16(out->stride_t, 2) && s16(out->stride_h, 2);
+    p.out_vec = (D % 8) == 0 && p.out_a16;
+    p.B = B; p.L = L; p.H = H; p.D = D; p.M = M;
+    p.lo = M - valid;
+    p.wp = wp;
+    p.slots = slots;
+    p.ring_all = ring_slots > 0 ? 1 : 0;
+    p.C = clamp_len;
+    p.n_rows = n_rows;
+    p.n_qt = (L + 127) / 128;
+    p.n_atoms = D <= 64 ? 1 : 2;
+    p.k_steps = (D + 15) / 16;
+    p.qscale = scale * 1.4426950408889634f;
+    p.err_flag = err_flag;
+    if (p.n_atoms == 1) {
+        if (static_cast<int64_t>(p.n_qt) * H * B > INT32_MAX) return TXL_ERR_UNSUPPORTED;
+        // even and odd query rows as two maps stepping two tokens per row; the odd map starts
+        // one token in and has floor(L/2) rows, so no load reads past the tensor (with L = 1
+        // the odd rows are taken from the even map: they belong to no query and are not stored)
+        const char* q0 = static_cast<const char*>(q->ptr);
+        bool okq = encode_view4(&p.tm_qe, q0, D, H, (L + 1) / 2, B, q->stride_h, 2 * q->stride_t,
+                                q->stride_b, 64);
+        if (okq && L / 2 > 0)
+            okq = encode_view4(&p.tm_qo, q0 + q->stride_t * 2, D, H, L / 2, B, q->stride_h,
+                               2 * q->stride_t, q->stride_b, 64);
+        else
+            p.tm_qo = p.tm_qe;
+        if (!okq) return TXL_ERR_CUDA;
+        const int sms = sm_count();
+        if (sms <= 0) return TXL_ERR_CUDA;
+        const int64_t items = static_cast<int64_t>(p.n_qt) * H * B;
+        const int G = static_cast<int>(std::min<int64_t>(items, sms));
+        const int64_t per_cls = static_cast<int64_t>(H) * B;
+        p.sched_mode = (p.n_qt <= kMaxSchedClasses && per_cls <= INT32_MAX &&
+                        schedule_items(G, p.n_qt, static_cast<int>(per_cls), (M + 127 - p.lo) / 128 + 1,
+                                       p.sched_counts, kSchedCapacity))
+                           ? 1 : 0;
+        return launch_attn_persist(p, sms, s) == cudaSuccess ? TXL_OK : TXL_ERR_CUDA;
+    }
+    if (B > 65535 || H > 65535) return TXL_ERR_UNSUPPORTED;
+    return launch_attn_tc(p, s) == cudaSuccess ? TXL_OK : TXL_ERR_CUDA;
+}
+
+}  // namespace
+
 txl_status txl_rel_attn_fwd(int B, int L, int H, int D, int clamp_len, const txl_view* q, const txl_mem* mem,
                             const txl_view* k_cur, const txl_view* v_cur, const float* u, const float* v_bias,
                             const void* r, int64_t ld_r, int n_rows, float scale, const txl_view* out,
@@ -221,68 +308,9 @@ txl_status txl_rel_attn_fwd(int B, int L, int H, int D, int clamp_len, const txl
     if (scale <= 0.f) scale = 1.0f / std::sqrt(static_cast<float>(D));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-    if (attn_tc_eligible(B, L, H, D, q, mem, k_cur, v_cur, r, ld_r, dtype)) {
-        if (!encoder_ready()) return TXL_ERR_CUDA;
-        AttnTcParams p;
-        std::memset(&p, 0, sizeof(p));
-        bool ok = encode_view4(&p.tm_q, q->ptr, D, H, L, B, q->stride_h, q->stride_t, q->stride_b) &&
-                  encode_view4(&p.tm_kcur, k_cur->ptr, D, H, L, B, k_cur->stride_h, k_cur->stride_t, k_cur->stride_b) &&
-                  encode_view4(&p.tm_vcur, v_cur->ptr, D, H, L, B, v_cur->stride_h, v_cur->stride_t, v_cur->stride_b) &&
-                  encode_rtab(&p.tm_r, r, D, H, n_rows, ld_r);
-        if (ok && M > 0)
-            ok = encode_view4(&p.tm_kmem, mem->k, D, H, M, B, mem->stride_h, mem->stride_t, mem->stride_b) &&
-                 encode_view4(&p.tm_vmem, mem->v, D, H, M, B, mem->stride_h, mem->stride_t, mem->stride_b);
-        else if (ok) {
-            p.tm_kmem = p.tm_kcur;
-            p.tm_vmem = p.tm_vcur;
-        }
-        if (!ok) return TXL_ERR_CUDA;
-        p.u = u;
-        p.vb = v_bias;
-        p.out = out->ptr;
-        p.o_sb = out->stride_b;
-        p.o_st = out->stride_t;
-        p.o_sh = out->stride_h;
-        p.out_a16 = a16(out->ptr) && s16(out->stride_b, 2) && s16(out->stride_t, 2) && s16(out->stride_h, 2);
-        p.out_vec = (D % 8) == 0 && p.out_a16;
-        p.B = B; p.L = L; p.H = H; p.D = D; p.M = M;
-        p.lo = M - valid;
-        p.wp = wp;
-        p.C = clamp_len;
-        p.n_rows = n_rows;
-        p.n_qt = (L + 127) / 128;
-        p.n_atoms = D <= 64 ? 1 : 2;
-        p.k_steps = (D + 15) / 16;
-        p.qscale = scale * 1.4426950408889634f;
-        p.err_flag = err_flag;
-        if (p.n_atoms == 1) {
-            if (static_cast<int64_t>(p.n_qt) * H * B > INT32_MAX) return TXL_ERR_UNSUPPORTED;
-            // even and odd query rows as two maps stepping two tokens per row; the odd map starts
-            // one token in and has floor(L/2) rows, so no load reads past the tensor (with L = 1
-            // the odd rows are taken from the even map: they belong to no query and are not stored)
-            const char* q0 = static_cast<const char*>(q->ptr);
-            bool okq = encode_view4(&p.tm_qe, q0, D, H, (L + 1) / 2, B, q->stride_h, 2 * q->stride_t,
-                                    q->stride_b, 64);
-            if (okq && L / 2 > 0)
-                okq = encode_view4(&p.tm_qo, q0 + q->stride_t * 2, D, H, L / 2, B, q->stride_h,
-                                   2 * q->stride_t, q->stride_b, 64);
-            else
-                p.tm_qo = p.tm_qe;
-            if (!okq) return TXL_ERR_CUDA;
-            const int sms = sm_count();
-            if (sms <= 0) return TXL_ERR_CUDA;
-            const int64_t items = static_cast<int64_t>(p.n_qt) * H * B;
-            const int G = static_cast<int>(std::min<int64_t>(items, sms));
-            const int64_t per_cls = static_cast<int64_t>(H) * B;
-            p.sched_mode = (p.n_qt <= kMaxSchedClasses && per_cls <= INT32_MAX &&
-                            schedule_items(G, p.n_qt, static_cast<int>(per_cls), (M + 127 - p.lo) / 128 + 1,
-                                           p.sched_counts, kSchedCapacity))
-                               ? 1 : 0;
-            return launch_attn_persist(p, sms, s) == cudaSuccess ? TXL_OK : TXL_ERR_CUDA;
-        }
-        if (B > 65535 || H > 65535) return TXL_ERR_UNSUPPORTED;
-        return launch_attn_tc(p, s) == cudaSuccess ? TXL_OK : TXL_ERR_CUDA;
-    }
+    if (attn_tc_eligible(B, L, H, D, q, mem, k_cur, v_cur, r, ld_r, dtype))
+        return attn_tc_launch(B, L, H, D, clamp_len, q, mem, k_cur, v_cur, u, v_bias, r, ld_r, n_rows, scale, out,
+                              err_flag, s, 0);
 
     AttnSimtParams p;
     std::memset(&p, 0, sizeof(p));
@@ -457,14 +485,32 @@ bool encode_rows(CUtensorMap* map, const void* ptr, int64_t cols, int64_t rows, 
 
 }  // namespace
 
-txl_status txl_linear(int m, int n, int k, const void* X, int64_t ld_x, const void* W, int64_t ld_w, void* Y,
-                      int64_t ld_y, txl_dtype dtype, int* err_flag, void* stream)
+namespace {
+
+// K and V column blocks of the q|k|v product routed into ring slots (the fused layer step).
+struct LinearSplit {
+    int hd, seg_len, slot0, slots;
+    void* k_ring;
+    void* v_ring;
+    int64_t ring_stride_b;           // elements between batch entries of a ring ([B][slots][H*D])
+};
+
+// [B][slots][hd] ring as a 3D TMA map (hd, slots, B) with 64 x 32 x 1 boxes, 128-byte swizzle: the
+// layout of one staged 32-row, 64-column block of the product's epilogue.
+bool encode_ring_store(CUtensorMap* map, void* ring, int hd, int slots, int B, int64_t stride_b)
 {
-    if (m < 0 || n < 0 || k <= 0 || !X || !W || !Y) return TXL_ERR_INVALID_ARG;
-    if (ld_x < k || ld_w < n || ld_y < n) return TXL_ERR_INVALID_ARG;
-    if (dtype == TXL_F32) return TXL_ERR_UNSUPPORTED;
-    if (dtype != TXL_BF16) return TXL_ERR_INVALID_ARG;
-    if (m == 0 || n == 0) return TXL_OK;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(hd), static_cast<cuuint64_t>(slots), static_cast<cuuint64_t>(B)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(hd) * 2, static_cast<cuuint64_t>(stride_b) * 2};
+    const cuuint32_t box[3] = {64, 32, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ring, dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+txl_status linear_launch(int m, int n, int k, const void* X, int64_t ld_x, const void* W, int64_t ld_w, void* Y,
+                         int64_t ld_y, int* err_flag, cudaStream_t stream, const LinearSplit* split)
+{
     if (!a16(X) || !a16(W) || !s16(ld_x, 2) || !s16(ld_w, 2)) return TXL_ERR_ALIGNMENT;
     if (static_cast<int64_t>(m) + 127 > INT32_MAX || static_cast<int64_t>(n) + 255 > INT32_MAX) return TXL_ERR_INVALID_ARG;
     if (!encoder_ready()) return TXL_ERR_CUDA;
@@ -483,11 +529,37 @@ txl_status txl_linear(int m, int n, int k, const void* X, int64_t ld_x, const vo
     p.n_tiles = static_cast<int>(tiles);
     p.k_tiles = (k + 63) / 64;
     p.vec = (a16(Y) && s16(ld_y, 2)) ? 1 : 0;
-    p.tma_store = (p.vec && encode_rows(&p.tm_y, Y, n, m, ld_y, 32)) ? 1 : 0;
+    if (split) {
+        // Y receives only the first hd columns; the rest go to the rings
+        if (!p.vec || !encode_rows(&p.tm_y, Y, split->hd, m, ld_y, 32) ||
+            !encode_ring_store(&p.tm_k, split->k_ring, split->hd, split->slots, m / split->seg_len, split->ring_stride_b) ||
+            !encode_ring_store(&p.tm_v, split->v_ring, split->hd, split->slots, m / split->seg_len, split->ring_stride_b))
+            return TXL_ERR_CUDA;
+        p.tma_store = 1;
+        p.split_hd = split->hd;
+        p.seg_len = split->seg_len;
+        p.slot0 = split->slot0;
+        p.slots = split->slots;
+    } else {
+        p.tma_store = (p.vec && encode_rows(&p.tm_y, Y, n, m, ld_y, 32)) ? 1 : 0;
+    }
     p.err_flag = err_flag;
     const int sms = sm_count();
     if (sms <= 0) return TXL_ERR_CUDA;
-    return launch_linear(p, sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? TXL_OK : TXL_ERR_CUDA;
+    return launch_linear(p, sms, stream) == cudaSuccess ? TXL_OK : TXL_ERR_CUDA;
+}
+
+}  // namespace
+
+txl_status txl_linear(int m, int n, int k, const void* X, int64_t ld_x, const void* W, int64_t ld_w, void* Y,
+                      int64_t ld_y, txl_dtype dtype, int* err_flag, void* stream)
+{
+    if (m < 0 || n < 0 || k <= 0 || !X || !W || !Y) return TXL_ERR_INVALID_ARG;
+    if (ld_x < k || ld_w < n || ld_y < n) return TXL_ERR_INVALID_ARG;
+    if (dtype == TXL_F32) return TXL_ERR_UNSUPPORTED;
+    if (dtype != TXL_BF16) return TXL_ERR_INVALID_ARG;
+    if (m == 0 || n == 0) return TXL_OK;
+    return linear_launch(m, n, k, X, ld_x, W, ld_w, Y, ld_y, err_flag, static_cast<cudaStream_t>(stream), nullptr);
 }
 
 size_t txl_rel_attn_layer_workspace_size(int B, int L, int H, int D)
@@ -534,6 +606,71 @@ txl_status txl_rel_attn_layer(int B, int L, int H, int D, int d_model, int clamp
     if (st != TXL_OK) return st;
     // the segment's K, V enter the memory (FIFO)
     if (mem && mem->M > 0) return txl_mem_push(mem, &kc, &vc, L, stream);
+    return TXL_OK;
+}
+
+size_t txl_rel_attn_layer_fused_workspace_size(int B, int L, int H, int D)
+{
+    if (B <= 0 || L <= 0 || H <= 0 || D <= 0) return 0;
+    // q of the segment [B*L][H*D] and the attention output [B*L][H*D], bf16
+    return static_cast<size_t>(B) * L * H * D * 2 * 2;
+}
+
+txl_status txl_rel_attn_layer_fused(int B, int L, int H, int D, int d_model, int clamp_len, const void* h,
+                                    int64_t ld_h, txl_mem* mem, int mem_len, const void* W_qkv, const void* W_o,
+                                    const float* u, const float* v_bias, const void* r, int64_t ld_r, int n_rows,
+                                    float scale, void* y, int64_t ld_y, void* workspace, size_t workspace_bytes,
+                                    int* err_flag, void* stream)
+{
+    if (B < 0 || L < 0 || H <= 0 || D <= 0 || d_model <= 0 || clamp_len < 0 || mem_len < 0) return TXL_ERR_INVALID_ARG;
+    if (!h || !W_qkv || !W_o || !u || !v_bias || !r || !y || !mem || !mem->k || !mem->v) return TXL_ERR_INVALID_ARG;
+    if (ld_h < d_model || ld_y < d_model || ld_r < D) return TXL_ERR_INVALID_ARG;
+    const int slots = mem->M;
+    if (mem->B != B || mem->H != H || mem->D != D || mem->dtype != TXL_BF16) return TXL_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(mem_len) + L > slots || mem->valid < 0 || mem->valid > mem_len || mem->wp < 0 ||
+        mem->wp >= slots)
+        return TXL_ERR_INVALID_ARG;
+    if (n_rows < std::min(mem_len + L, clamp_len + 1)) return TXL_ERR_INVALID_ARG;
+    const int64_t HD = static_cast<int64_t>(H) * D;
+    // the persistent tcgen05 attention with tiles of 128 keys aligned to ring slots, product blocks
+    // of 64 columns that never straddle the q, k, v column ranges
+    if (D > 64 || (D & 7) || (HD % 64) || (d_model & 7) || (L % 128) || (mem_len % 128) || (slots % 128) ||
+        (mem->wp % 128))
+        return TXL_ERR_UNSUPPORTED;
+    if (mem->stride_h != D || mem->stride_t != HD || mem->stride_b != static_cast<int64_t>(slots) * HD)
+        return TXL_ERR_UNSUPPORTED;
+    if (!a16(mem->k) || !a16(mem->v) || !a16(r) || !s16(ld_r, 2) || !a16(y) || !s16(ld_y, 2)) return TXL_ERR_ALIGNMENT;
+    if (B == 0 || L == 0) return TXL_OK;
+    if (static_cast<int64_t>(B) * L > INT32_MAX / 4) return TXL_ERR_INVALID_ARG;
+    const size_t need = txl_rel_attn_layer_fused_workspace_size(B, L, H, D);
+    if (!workspace || workspace_bytes < need) return TXL_ERR_WORKSPACE;
+    if (!a16(workspace)) return TXL_ERR_ALIGNMENT;
+    if (scale <= 0.f) scale = 1.0f / std::sqrt(static_cast<float>(D));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int rows = B * L;
+    __nv_bfloat16* qbuf = static_cast<__nv_bfloat16*>(workspace);
+    __nv_bfloat16* attn = qbuf + static_cast<int64_t>(rows) * HD;
+    // Q = h W_q into the workspace; K = h W_k and V = h W_v straight into the ring slots that follow
+    // the memory, (wp + mem_len + t) mod slots
+    const LinearSplit split{static_cast<int>(HD), L, static_cast<int>((static_cast<int64_t>(mem->wp) + mem_len) % slots),
+                            slots, mem->k, mem->v, mem->stride_b};
+    txl_status st = linear_launch(rows, static_cast<int>(3 * HD), d_model, h, ld_h, W_qkv, 3 * HD, qbuf, HD, err_flag,
+                                  s, &split);
+    if (st != TXL_OK) return st;
+    // the attention over [memory ++ segment], every key read from the ring
+    const txl_view q{qbuf, L * HD, HD, D};
+    const txl_view out{attn, L * HD, HD, D};
+    txl_mem window = *mem;
+    window.M = mem_len;
+    st = attn_tc_launch(B, L, H, D, clamp_len, &q, &window, nullptr, nullptr, u, v_bias, r, ld_r, n_rows, scale, &out,
+                        err_flag, s, slots);
+    if (st != TXL_OK) return st;
+    // y = concat_h(attn) W_o
+    st = linear_launch(rows, d_model, static_cast<int>(HD), attn, HD, W_o, d_model, y, ld_y, err_flag, s, nullptr);
+    if (st != TXL_OK) return st;
+    // the segment is now the newest part of the memory: no copy, the window moves
+    mem->wp = static_cast<int>((static_cast<int64_t>(mem->wp) + L) % slots);
+    mem->valid = std::min(mem->valid + L, mem_len);
     return TXL_OK;
 }
 

@@ -126,17 +126,18 @@ __device__ __forceinline__ bool item_at(const AttnTcParams& p, const int* first,
 __device__ __forceinline__ bool need_chunk(int t, int C) { return 128 * t < C; }
 
 // Key tile t of an item covers keys j0 = M + i0 - 128 t; memory keys come from the ring slot
-// (wp + j0) mod M (or j0 itself for a plain memory; a negative j0 reads TMA zero fill).
+// (wp + j0) mod slots (or j0 itself for a plain memory; a negative j0 reads TMA zero fill), and so
+// do the current segment's keys when the whole sequence lives in the ring (ring_all).
 __device__ __forceinline__ void key_tile(const AttnTcParams& p, const Item& it, int t, bool values,
                                          const CUtensorMap*& map, int& row)
 {
     const int j0 = p.M + it.i0 - 128 * t;
-    if (j0 >= p.M) {
+    if (j0 >= p.M && !p.ring_all) {
         map = values ? &p.tm_vcur : &p.tm_kcur;
         row = j0 - p.M;
     } else {
         map = values ? &p.tm_vmem : &p.tm_kmem;
-        row = p.wp ? static_cast<int>((static_cast<int64_t>(p.wp) + j0) % p.M) : j0;
+        row = p.wp || p.ring_all ? static_cast<int>((static_cast<int64_t>(p.wp) + j0) % p.slots) : j0;
     }
 }
 

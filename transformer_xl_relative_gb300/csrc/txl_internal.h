@@ -92,6 +92,9 @@ struct AttnTcParams {
     const float* u; const float* vb;   // [H][D] fp32
     void* out; int64_t o_sb, o_st, o_sh;
     int B, L, H, D, M, lo, wp, C, n_rows;
+    // ring_all (persistent kernel only): every key, the current segment's too, is read from the
+    // memory ring: logical key j (0 <= j < M + L) lives in slot (wp + j) mod slots
+    int ring_all, slots;
     int n_qt;                    // query tiles of 128
     int n_atoms;                 // 64-column atoms per row: 1 (D <= 64) or 2 (D <= 128)
     int k_steps;                 // ceil(D / 16): UMMA K steps for the Q.K and Q.r products
@@ -166,6 +169,11 @@ struct LinearParams {
     int vec;             // Y 16-byte aligned and ld_y a multiple of 8: 16-byte stores
     int tma_store;       // the same, and tm_y encoded: the epilogue stores tiles by TMA
     int* err_flag;
+    // Split output (split_hd > 0, TMA stores only): columns [0, split_hd) go to tm_y; columns
+    // [split_hd, 2 split_hd) and [2 split_hd, 3 split_hd) go to the rings tm_k, tm_v, (split_hd,
+    // slots, batch) maps, row r = b * seg_len + t into slot (slot0 + t) mod slots of entry b
+    int split_hd, seg_len, slot0, slots;
+    CUtensorMap tm_k, tm_v;
 };
 
 cudaError_t launch_linear(const LinearParams& p, int sm_count, cudaStream_t s);

@@ -186,7 +186,17 @@ __global__ void __launch_bounds__(kLinThreads, 1) linear_kernel(const __grid_con
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d(&p.tm_y, n0 + 64 * c, m0 + 32 * q, stage);
+                        const int n = n0 + 64 * c;
+                        if (p.split_hd > 0 && n >= p.split_hd) {
+                            // a key or value block: rows m0 + 32 q .. of one batch entry, consecutive slots
+                            const int row = m0 + 32 * q;
+                            const int b = row / p.seg_len, tt = row - b * p.seg_len;
+                            const bool val = n >= 2 * p.split_hd;
+                            tma_store_3d(val ? &p.tm_v : &p.tm_k, n - (val ? 2 : 1) * p.split_hd,
+                                         (p.slot0 + tt) % p.slots, b, stage);
+                        } else {
+                            tma_store_2d(&p.tm_y, n, m0 + 32 * q, stage);
+                        }
                         bulk_commit_group();
                     }
                 }

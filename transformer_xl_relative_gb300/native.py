@@ -20,6 +20,7 @@ EXPORTS = (
     "txl_rel_attn_workspace_size", "txl_rel_attn_path", "txl_rel_attn_decode",
     "txl_rel_attn_decode_workspace_size", "txl_rel_attn_decode_noalloc", "txl_mem_push",
     "txl_selftest_wait_timeout", "txl_linear", "txl_rel_attn_layer", "txl_rel_attn_layer_workspace_size",
+    "txl_rel_attn_layer_fused", "txl_rel_attn_layer_fused_workspace_size",
     "txl_rel_attn_bwd", "txl_rel_attn_bwd_workspace_size", "txl_rel_pos_bwd", "txl_rel_attn_table_fwd",
 )
 
@@ -90,6 +91,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.txl_rel_attn_layer.restype = i
     lib.txl_rel_attn_layer_workspace_size.argtypes = [i, i, i, i]
     lib.txl_rel_attn_layer_workspace_size.restype = ctypes.c_size_t
+    lib.txl_rel_attn_layer_fused.argtypes = [i, i, i, i, i, i, vp, i64, Mp, i, vp, vp, vp, vp, vp, i64, i, fp,
+                                             vp, i64, vp, ctypes.c_size_t, vp, vp]
+    lib.txl_rel_attn_layer_fused.restype = i
+    lib.txl_rel_attn_layer_fused_workspace_size.argtypes = [i, i, i, i]
+    lib.txl_rel_attn_layer_fused_workspace_size.restype = ctypes.c_size_t
     lib.txl_rel_attn_bwd.argtypes = [i, i, i, i, i, V, Mp, V, V, vp, vp, vp, i64, i, fp, V, V,
                                      vp, vp, vp, vp, vp, vp, i, vp, ctypes.c_size_t, vp]
     lib.txl_rel_attn_bwd.restype = i
