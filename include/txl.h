@@ -356,6 +356,28 @@ txl_status txl_rel_attn_table_fwd(int B, int L, int H, int D, int max_len,
                                   const void* r_table, int64_t ld_r, const uint8_t* key_mask,
                                   float scale, const txl_view* out, txl_dtype dtype, void* stream);
 
+/*
+ * Checked build.  libtxl_checked.so is this library compiled with -DTXL_CHECKED (the package builds
+ * it on request: transformer_xl_relative_gb300/_build.py --checked; the binding loads it when the
+ * environment variable TXL_CHECKED is 1).  Its kernels range-check the indices they compute before
+ * using them (the key row of every TMA key/value tile of the fused attention, the memory ring slot
+ * of every key in the other attention kernels and of every pushed position, the remapped r row):
+ * an index outside its range is counted in a device counter owned by the library and replaced by a
+ * safe one, so the call completes (its results are then meaningless) and nothing traps or waits.
+ * It stands in for a memory checker; the pages have no counterpart.
+ *   txl_checked_build        : 1 in the checked build, 0 otherwise.
+ *   txl_range_errors         : failed checks since the library was loaded or last cleared, into the
+ *                              host int *count.  Synchronizes the current device (a debugging call).
+ *                              TXL_ERR_UNSUPPORTED (and 0) in the normal build.
+ *   txl_range_errors_clear   : resets the counter (synchronizes the current device).
+ *   txl_selftest_range_check : enqueues one failing and one passing check on `stream`; the counter
+ *                              gains exactly one.  TXL_ERR_UNSUPPORTED in the normal build.
+ */
+int txl_checked_build(void);
+txl_status txl_range_errors(int* count);
+txl_status txl_range_errors_clear(void);
+txl_status txl_selftest_range_check(void* stream);
+
 /* Self-test of the bounded waits used by every kernel: launches one CTA that waits on an
  * mbarrier nothing will signal, gives up after timeout_us microseconds (1 .. 10^7), writes
  * TXL_ERR_TIMEOUT to the device int err_flag and returns.  The context stays usable. */

@@ -13,6 +13,39 @@
 
 using namespace txl;
 
+#ifdef TXL_CHECKED
+// Range-check failures of the checked build's kernels since the library was loaded (or cleared).
+__device__ int g_range_errors;
+#endif
+
+namespace txl {
+
+// The counter's device address in the current context, looked up once per context (null in the
+// normal build, whose kernels check nothing).
+int* range_counter()
+{
+#ifdef TXL_CHECKED
+    static std::mutex mu;
+    static int* addr = nullptr;
+    static unsigned long long ctx_of = 0;
+    unsigned long long ctx = 0;
+    const bool have = current_context_id(&ctx);
+    std::lock_guard<std::mutex> lock(mu);
+    if (!have || !addr || ctx != ctx_of) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_range_errors) != cudaSuccess) return nullptr;
+        if (!have && !current_context_id(&ctx)) return nullptr;
+        addr = static_cast<int*>(p);
+        ctx_of = ctx;
+    }
+    return addr;
+#else
+    return nullptr;
+#endif
+}
+
+}  // namespace txl
+
 namespace {
 
 constexpr int kVersion = 10000;   // 1.0.0
@@ -251,6 +284,7 @@ txl_status attn_tc_launch(int B, int L, int H, int D, int clamp_len, const txl_v
     p.wp = wp;
     p.slots = slots;
     p.ring_all = ring_slots > 0 ? 1 : 0;
+    p.chk = range_counter();
     p.C = clamp_len;
     p.n_rows = n_rows;
     p.n_qt = (L + 127) / 128;
@@ -326,6 +360,8 @@ txl_status txl_rel_attn_fwd(int B, int L, int H, int D, int clamp_len, const txl
     p.r = r; p.r_row = static_cast<int64_t>(H) * ld_r; p.r_head = ld_r;
     p.B = B; p.L = L; p.H = H; p.D = D; p.M = M; p.lo = M - valid; p.wp = wp; p.C = clamp_len;
     p.scale = scale;
+    p.n_rows = n_rows;
+    p.chk = range_counter();
     return launch_attn_simt(p, dtype, s) == cudaSuccess ? TXL_OK : TXL_ERR_CUDA;
 }
 
@@ -447,6 +483,7 @@ txl_status txl_mem_push(txl_mem* mem, const txl_view* k_new, const txl_view* v_n
     if (L == 0) return TXL_OK;
     const int elem = mem->dtype == TXL_F32 ? 4 : 2;
     MemPushParams p{};
+    p.chk = range_counter();
     p.k_new = k_new->ptr; p.v_new = v_new->ptr;
     p.n_sb = k_new->stride_b; p.n_st = k_new->stride_t; p.n_sh = k_new->stride_h;
     p.nv_sb = v_new->stride_b; p.nv_st = v_new->stride_t; p.nv_sh = v_new->stride_h;
@@ -769,6 +806,39 @@ txl_status txl_rel_attn_table_fwd(int B, int L, int H, int D, int max_len, const
     p.B = B; p.L = L; p.H = H; p.D = D; p.max_len = max_len;
     p.scale = scale;
     return launch_table_attn(p, dtype, static_cast<cudaStream_t>(stream)) == cudaSuccess ? TXL_OK : TXL_ERR_CUDA;
+}
+
+int txl_checked_build(void) { return kCheckedBuild ? 1 : 0; }
+
+txl_status txl_range_errors(int* count)
+{
+    if (!count) return TXL_ERR_INVALID_ARG;
+#ifdef TXL_CHECKED
+    if (cudaDeviceSynchronize() != cudaSuccess) return TXL_ERR_CUDA;
+    return cudaMemcpyFromSymbol(count, g_range_errors, sizeof(int)) == cudaSuccess ? TXL_OK : TXL_ERR_CUDA;
+#else
+    *count = 0;
+    return TXL_ERR_UNSUPPORTED;
+#endif
+}
+
+txl_status txl_range_errors_clear(void)
+{
+#ifdef TXL_CHECKED
+    const int zero = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess) return TXL_ERR_CUDA;
+    return cudaMemcpyToSymbol(g_range_errors, &zero, sizeof(int)) == cudaSuccess ? TXL_OK : TXL_ERR_CUDA;
+#else
+    return TXL_ERR_UNSUPPORTED;
+#endif
+}
+
+txl_status txl_selftest_range_check(void* stream)
+{
+    if (!kCheckedBuild) return TXL_ERR_UNSUPPORTED;
+    int* chk = range_counter();
+    if (!chk) return TXL_ERR_CUDA;
+    return launch_selftest_range(chk, static_cast<cudaStream_t>(stream)) == cudaSuccess ? TXL_OK : TXL_ERR_CUDA;
 }
 
 txl_status txl_selftest_wait_timeout(int* err_flag, unsigned timeout_us, void* stream)

@@ -135,9 +135,16 @@ __device__ __forceinline__ void key_tile(const AttnTcParams& p, const Item& it, 
     if (j0 >= p.M && !p.ring_all) {
         map = values ? &p.tm_vcur : &p.tm_kcur;
         row = j0 - p.M;
+        if (!in_range(row, 0, p.L, p.chk)) row = 0;
     } else {
         map = values ? &p.tm_vmem : &p.tm_kmem;
-        row = p.wp || p.ring_all ? static_cast<int>((static_cast<int64_t>(p.wp) + j0) % p.slots) : j0;
+        if (p.wp || p.ring_all) {
+            row = static_cast<int>((static_cast<int64_t>(p.wp) + j0) % p.slots);
+            if (!in_range(row, 0, p.slots, p.chk)) row = 0;
+        } else {
+            row = j0;                                   // a plain memory: rows before 0 read zero fill
+            if (!in_range(row, -127, p.M, p.chk)) row = 0;
+        }
     }
 }
 

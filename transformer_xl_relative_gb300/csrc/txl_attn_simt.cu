@@ -61,7 +61,8 @@ __global__ void __launch_bounds__(32 * kSimtWarps) attn_simt_kernel(AttnSimtPara
         const T* kp;
         const T* vp;
         if (j < p.M) {
-            const int slot = static_cast<int>((static_cast<int64_t>(p.wp) + j) % p.M);
+            int slot = static_cast<int>((static_cast<int64_t>(p.wp) + j) % p.M);
+            if (!in_range(slot, 0, p.M, p.chk)) slot = 0;
             const int64_t off = b * p.m_sb + slot * p.m_st + h * p.m_sh;
             kp = static_cast<const T*>(p.kmem) + off;
             vp = static_cast<const T*>(p.vmem) + off;
@@ -71,7 +72,8 @@ __global__ void __launch_bounds__(32 * kSimtWarps) attn_simt_kernel(AttnSimtPara
             vp = static_cast<const T*>(p.vcur) + b * p.vc_sb + t * p.vc_st + h * p.vc_sh;
         }
         const int delta = qpos - j;
-        const int dc = delta < p.C ? delta : p.C;
+        int dc = delta < p.C ? delta : p.C;
+        if (!in_range(dc, 0, p.n_rows, p.chk)) dc = 0;
         const T* rp = static_cast<const T*>(p.r) + dc * p.r_row + h * p.r_head;
         float part = 0.f;
 #pragma unroll

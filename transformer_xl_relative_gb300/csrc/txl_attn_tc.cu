@@ -159,10 +159,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     // (wp + j0) mod M (or j0 itself for a plain memory; a negative j0 reads TMA zero fill).
     auto key_tile = [&](int t, const CUtensorMap*& km, const CUtensorMap*& vm, int& row) {
         const int j0 = M + plan.i0 - 128 * t;
-        if (j0 >= M) { km = &p.tm_kcur; vm = &p.tm_vcur; row = j0 - M; }
+        if (j0 >= M) {
+            km = &p.tm_kcur; vm = &p.tm_vcur; row = j0 - M;
+            if (!in_range(row, 0, p.L, p.chk)) row = 0;
+        }
         else {
             km = &p.tm_kmem; vm = &p.tm_vmem;
             row = p.wp ? static_cast<int>((static_cast<int64_t>(p.wp) + j0) % M) : j0;
+            if (!in_range(row, p.wp ? 0 : -127, M, p.chk)) row = 0;
         }
     };
 

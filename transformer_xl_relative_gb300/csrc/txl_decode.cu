@@ -733,9 +733,9 @@ static __device__ __align__(256) float g_decode_scratch[kDecodeStaticScratchByte
 // is loaded again, possibly elsewhere), the id differs, and the first call in the new context looks
 // the address up again instead of using a stale one.
 namespace {
-
 using PFN_ctx_get_current = CUresult (*)(CUcontext*);
 using PFN_ctx_get_id = CUresult (*)(CUcontext, unsigned long long*);
+}  // namespace
 
 bool current_context_id(unsigned long long* id)
 {
@@ -758,8 +758,6 @@ bool current_context_id(unsigned long long* id)
     if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
     return get_id(ctx, id) == CUDA_SUCCESS;
 }
-
-}  // namespace
 
 cudaError_t decode_static_scratch(float** out)
 {

@@ -31,6 +31,27 @@ cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, si
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
 }
 
+// Range checks of the checked build (compiled with -DTXL_CHECKED): a computed index outside its
+// range adds one to the library's device counter `chk` and the caller falls back to a safe index
+// (nothing traps, nothing waits); in the normal build every check is `true` and costs nothing.
+#ifdef TXL_CHECKED
+constexpr bool kCheckedBuild = true;
+__device__ __forceinline__ bool in_range(int64_t x, int64_t lo, int64_t hi, int* chk)
+{
+    const bool ok = x >= lo && x < hi;
+    if (!ok && chk) atomicAdd(chk, 1);
+    return ok;
+}
+#else
+constexpr bool kCheckedBuild = false;
+__device__ __forceinline__ bool in_range(int64_t, int64_t, int64_t, int*) { return true; }
+#endif
+
+// Device address of the range-check counter in the current context (null in the normal build).
+int* range_counter();
+// Unique id of the current CUDA context (false if none is current).
+bool current_context_id(unsigned long long* id);
+
 constexpr int kMaxDModel = 4096;   // the bf16 path keeps d_model/2 frequencies in shared memory
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;   // 2 s: far above any healthy wait
 constexpr int kSchedCapacity = 4096;   // bytes of per-CTA item counts carried as kernel parameters
@@ -75,6 +96,8 @@ struct AttnSimtParams {
     const void* r; int64_t r_row, r_head;       // element strides of the r table
     int B, L, H, D, M, lo, wp, C;
     float scale;
+    int n_rows;                                 // rows of the r table (range checks)
+    int* chk;                                   // range-check counter (checked build)
 };
 
 cudaError_t launch_attn_simt(const AttnSimtParams& p, txl_dtype dtype, cudaStream_t s);
@@ -95,6 +118,7 @@ struct AttnTcParams {
     // ring_all (persistent kernel only): every key, the current segment's too, is read from the
     // memory ring: logical key j (0 <= j < M + L) lives in slot (wp + j) mod slots
     int ring_all, slots;
+    int* chk;                    // range-check counter (checked build)
     int n_qt;                    // query tiles of 128
     int n_atoms;                 // 64-column atoms per row: 1 (D <= 64) or 2 (D <= 128)
     int k_steps;                 // ceil(D / 16): UMMA K steps for the Q.K and Q.r products
@@ -215,10 +239,13 @@ struct MemPushParams {
     int B, H, D, M, wp, t0, n_t;        // copy positions t0 .. t0+n_t-1 of the segment
     int elem_bytes;
     int vec16;                          // 1: copy 16-byte chunks
+    int* chk;                           // range-check counter (checked build)
 };
 
 cudaError_t launch_mem_push(const MemPushParams& p, cudaStream_t s);
 
 cudaError_t launch_selftest_wait(int* err_flag, unsigned timeout_us, cudaStream_t s);
+// One failing and one passing range check on the device (the checked build's counter gains one).
+cudaError_t launch_selftest_range(int* chk, cudaStream_t s);
 
 }  // namespace txl

@@ -44,7 +44,8 @@ __global__ void __launch_bounds__(kPushThreads) mem_push_vec16(MemPushParams p)
             for (int k = 0; k < kPushRows; ++k) {
                 const int tt = t + p.t0;                   // position inside the segment
                 if (r0 + k < rows) {
-                    const int slot = (p.wp + tt) % p.M;
+                    int slot = (p.wp + tt) % p.M;
+                    if (!in_range(slot, 0, p.M, p.chk)) slot = 0;
                     val[k] = __ldg(reinterpret_cast<const uint4*>(src + b * ssb + tt * sst + so));
                     doff[k] = b * dsb + slot * dst_t + dso;
                 }
@@ -69,7 +70,8 @@ __global__ void __launch_bounds__(kPushThreads) mem_push_scalar(MemPushParams p)
         const int h = static_cast<int>(rem % p.H); rem /= p.H;
         const int t = static_cast<int>(rem % p.n_t) + p.t0;
         const int b = static_cast<int>(rem / p.n_t);
-        const int slot = static_cast<int>((static_cast<int64_t>(p.wp) + t) % p.M);
+        int slot = static_cast<int>((static_cast<int64_t>(p.wp) + t) % p.M);
+        if (!in_range(slot, 0, p.M, p.chk)) slot = 0;
         const char* src = static_cast<const char*>(which ? p.v_new : p.k_new);
         char* dst = static_cast<char*>(which ? p.v : p.k);
         const int64_t so = which ? (b * p.nv_sb + t * p.nv_st + h * p.nv_sh)
@@ -120,6 +122,22 @@ cudaError_t launch_mem_push(const MemPushParams& p, cudaStream_t s)
         if (blocks > cap) blocks = cap;
         mem_push_scalar<<<static_cast<unsigned>(blocks), kPushThreads, 0, s>>>(p);
     }
+    return cudaGetLastError();
+}
+
+// One index out of its range and one inside it, checked as every kernel of the checked build
+// checks its computed indices: the counter gains exactly one.  Nothing is accessed.
+__global__ void selftest_range_kernel(int* chk, int x_bad, int x_good)
+{
+    const bool bad_ok = in_range(x_bad, 0, 4, chk);
+    const bool good_ok = in_range(x_good, 0, 4, chk);
+    (void)bad_ok;
+    (void)good_ok;
+}
+
+cudaError_t launch_selftest_range(int* chk, cudaStream_t s)
+{
+    selftest_range_kernel<<<1, 1, 0, s>>>(chk, 5, 1);
     return cudaGetLastError();
 }
 

@@ -8,7 +8,10 @@ from __future__ import annotations
 import ctypes
 import os
 
-LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libtxl.so")
+_HERE = os.path.dirname(os.path.abspath(__file__))
+# TXL_CHECKED=1 selects the range-checked build of the same library (built on request by
+# _build.py --checked)
+LIB_PATH = os.path.join(_HERE, "libtxl_checked.so" if os.environ.get("TXL_CHECKED") == "1" else "libtxl.so")
 
 TXL_OK, TXL_ERR_INVALID_ARG, TXL_ERR_UNSUPPORTED, TXL_ERR_ALIGNMENT = 0, 1, 2, 3
 TXL_ERR_CUDA, TXL_ERR_TIMEOUT, TXL_ERR_WORKSPACE = 4, 5, 6
@@ -21,6 +24,7 @@ EXPORTS = (
     "txl_rel_attn_decode_workspace_size", "txl_rel_attn_decode_noalloc", "txl_mem_push",
     "txl_selftest_wait_timeout", "txl_linear", "txl_rel_attn_layer", "txl_rel_attn_layer_workspace_size",
     "txl_rel_attn_layer_fused", "txl_rel_attn_layer_fused_workspace_size",
+    "txl_checked_build", "txl_range_errors", "txl_range_errors_clear", "txl_selftest_range_check",
     "txl_rel_attn_bwd", "txl_rel_attn_bwd_workspace_size", "txl_rel_pos_bwd", "txl_rel_attn_table_fwd",
 )
 
@@ -82,6 +86,14 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.txl_rel_attn_decode_noalloc.restype = i
     lib.txl_mem_push.argtypes = [Mp, V, V, i, vp]
     lib.txl_mem_push.restype = i
+    lib.txl_checked_build.argtypes = []
+    lib.txl_checked_build.restype = i
+    lib.txl_range_errors.argtypes = [ctypes.POINTER(ctypes.c_int)]
+    lib.txl_range_errors.restype = i
+    lib.txl_range_errors_clear.argtypes = []
+    lib.txl_range_errors_clear.restype = i
+    lib.txl_selftest_range_check.argtypes = [vp]
+    lib.txl_selftest_range_check.restype = i
     lib.txl_selftest_wait_timeout.argtypes = [vp, ctypes.c_uint, vp]
     lib.txl_selftest_wait_timeout.restype = i
     lib.txl_linear.argtypes = [i, i, i, vp, i64, vp, i64, vp, i64, i, vp, vp]
