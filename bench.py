@@ -324,7 +324,7 @@ def _oracle_sample(cfg, rows, mem_valid=None, stream=False, threads=None):
     return dt, 6 * cfg.D * sum(keys), threads
 
 
-def bench_configs(txl, device, stream, rank, args, with_oracle):
+def bench_configs(txl, device, stream, rank, args, with_oracle, legs=("base", "longmem", "stream")):
     """The other synthetic workloads at one GPU: base (B32 H10 D41 L150 M150), long memory
     (B8 H16 D64 L128 M1600) and the 8-segment stream through the FIFO memory (B4 H16 D128 L512
     M2048).  Each reports the attention kernel's time per call, TFLOP/s (6 D per visible pair),
@@ -334,7 +334,7 @@ def bench_configs(txl, device, stream, rank, args, with_oracle):
     import txl_inputs
     peak, _, hbm, kind = _peaks()
     out = {}
-    for name in ("base", "longmem"):
+    for name in [n for n in ("base", "longmem") if n in legs]:
         cfg = txl_inputs.CONFIGS[name]
         B, H, D, L, M, C, hs = cfg.B, cfg.H, cfg.D, cfg.L, cfg.M, cfg.clamp_len, cfg.hs
         dt = cfg.torch_dtype
@@ -386,6 +386,8 @@ def bench_configs(txl, device, stream, rank, args, with_oracle):
         out[name] = res
         del sets, mems
 
+    if "stream" not in legs:
+        return out
     # the stream: 8 consecutive segments, each attending over the FIFO memory (empty at the start)
     # and then pushed into it; one pass = the position table + 8 x (attention + push)
     cfg = txl_inputs.CONFIGS["stream"]
@@ -978,6 +980,42 @@ def run_txl(args):
     return 0
 
 
+def profile_leg(args):
+    """A few calls of one workload's kernels and nothing else, for a profiler to capture:
+    large / base / longmem (the fused attention), stream (8 segments: attention + push), layer (the
+    fused layer step), decode.  Prints the per-call device time of the last repetition."""
+    import torch
+    import transformer_xl_relative_gb300 as txl
+    device = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(device=device)
+    if args.profile_leg in ("base", "longmem", "stream"):
+        res = bench_configs(txl, device, stream, 0, args, with_oracle=False, legs=(args.profile_leg,))[args.profile_leg]
+    elif args.profile_leg == "layer":
+        res = bench_layer(txl, device, stream, 0, args)
+    elif args.profile_leg == "decode":
+        res = bench_decode(txl, device, stream, 0, args)
+    else:
+        import txl_inputs
+        cfg = txl_inputs.CONFIGS["large"]
+        B, H, D, L, M, C = cfg.B, cfg.H, cfg.D, cfg.L, cfg.M, cfg.clamp_len
+        g = torch.Generator(device=device).manual_seed(cfg.seed)
+        q = torch.randn(B, L, H, D, generator=g, device=device).to(torch.bfloat16)
+        k = torch.randn(B, M + L, H, D, generator=g, device=device).to(torch.bfloat16)
+        v = torch.randn(B, M + L, H, D, generator=g, device=device).to(torch.bfloat16)
+        u = (0.02 * torch.randn(H, D, generator=g, device=device)).float()
+        vb = (0.02 * torch.randn(H, D, generator=g, device=device)).float()
+        W = (torch.randn(cfg.d_model, H * D, generator=g, device=device) * cfg.d_model ** -0.5).to(torch.bfloat16)
+        r = torch.empty(cfg.n_rows, H, D, dtype=torch.bfloat16, device=device)
+        out = torch.empty_like(q)
+        mem = txl.Memory.full(k[:, :M], v[:, :M])
+        txl.rel_pos_gen(W, r, cfg.n_rows, cfg.d_model, H, D)
+        res = {"us_per_call": _graph_us(stream, lambda i: txl.rel_attn_fwd(q, mem, k[:, M:], v[:, M:], u, vb, r,
+                                                                         cfg.n_rows, C, out), 1, 3)}
+    print(json.dumps({"profile_leg": args.profile_leg,
+                      **{k_: v_ for k_, v_ in res.items() if isinstance(v_, (int, float, str))}}), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -985,6 +1023,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=40)
     ap.add_argument("--impl", choices=["txl", "reference"], default="txl")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-leg", choices=["large", "base", "longmem", "stream", "layer", "decode"],
+                    help="run only a few calls of this workload (for a profiler) and exit")
     args = ap.parse_args(argv)
     world = os.environ.get("WORLD_SIZE")
     if args.gpus > 1 and world is None:
@@ -998,6 +1038,8 @@ def main(argv=None):
         return 2
     if args.impl == "reference":
         return run_reference(args)
+    if args.profile_leg:
+        return profile_leg(args)
     return run_txl(args)
 
 
