@@ -27,6 +27,7 @@
 #include <cuda_bf16.h>
 
 #include "txl_internal.h"
+#include "txl_ptx.cuh"
 
 namespace txl {
 
@@ -84,6 +85,7 @@ template <typename T, int LQ>
 __global__ void __launch_bounds__(kDecThreads) decode_partial_kernel(const __grid_constant__ DecodeParams p)
 {
     extern __shared__ __align__(16) float dsm[];
+    pdl_launch_dependents();                       // the merge may launch (it waits for this grid)
     const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int L = p.L, D = p.D, Dp = p.Dp;
@@ -329,6 +331,7 @@ template <int LQ>
 __global__ void __launch_bounds__(kDecThreads) decode_staged_kernel(const __grid_constant__ DecodeParams p)
 {
     extern __shared__ __align__(16) float dsm[];
+    pdl_launch_dependents();                       // the merge may launch (it waits for this grid)
     const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int rg = lane >> 3, part = lane & 7;
@@ -628,6 +631,7 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_consta
     // partial sums with independent loads
     __shared__ float wsh[1024];
     __shared__ float mred[4];
+    pdl_wait();                                               // the partials are complete
     const int bhi = blockIdx.x;                               // (b * H + h) * L + i
     const int i = bhi % p.L;
     const int bh = bhi / p.L;
@@ -704,8 +708,8 @@ cudaError_t launch_lq(const DecodeParams& p, cudaStream_t s)
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    decode_combine_kernel<T><<<p.B * p.H * p.L, 128, 0, s>>>(p);
-    return cudaGetLastError();
+    // launched as a dependent of the partial kernel: its launch overlaps that grid's tail
+    return launch_dependent(decode_combine_kernel<T>, dim3(p.B * p.H * p.L), dim3(128), 0, s, p);
 }
 
 template <typename T>
