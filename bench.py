@@ -659,8 +659,8 @@ def bench_backward(txl, device, stream, rank, args):
 
 def bench_table(txl, device, stream, rank, args):
     """The learned-table variant (txl_rel_attn_table_fwd): bidirectional attention B16 L384 H16 D64,
-    max_len 512, bf16 inputs, every key visible; on this workload the tensor-core kernel (bf16
-    mma.sync products, fp32 accumulation).  Algorithmic flops 6 D per (query, key) pair (content 2 D,
+    max_len 512, bf16 inputs, every key visible; on this workload the persistent tcgen05 kernel in its
+    learned-table mode (bf16 products, fp32 accumulation in tensor memory).  Algorithmic flops 6 D per (query, key) pair (content 2 D,
     position 2 D, P.V 2 D) against the measured bf16 tensor peak."""
     import torch
     B, H, D, L, max_len = 16, 16, 64, 384, 512
@@ -697,7 +697,7 @@ def bench_table(txl, device, stream, rank, args):
     achieved = flops / (t_us * 1e-6) / 1e12
     return {"workload": "table variant: B16 L384 H16 D64 max_len512 bf16, bidirectional, no mask",
             "us_per_call": t_us, "algorithmic_flops_per_call": flops,
-            "roofline": {"kernel": "txl_rel_attn_table_fwd (table_tc_kernel, bf16 mma.sync)", "bound": "tensor",
+            "roofline": {"kernel": "txl_rel_attn_table_fwd (attn_persist_kernel, learned-table mode)", "bound": "tensor",
                          "achieved": achieved, "peak": bf16_peak, "unit": "TFLOP/s", "frac": achieved / bf16_peak,
                          "peak_source": peak_src + " bf16 burst"}}
 

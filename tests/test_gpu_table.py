@@ -29,7 +29,7 @@ TABLE = [
     (2, 4, 64, 200, 64, "bf16", "random", 0),   # L > max_len: the index clamps at both ends
     (3, 3, 41, 37, 16, "bf16", "one_empty", 48),  # padded heads; batch entry 1 has every key masked
     (2, 2, 128, 33, 8, "f32", "random", 0),     # D = 128, L not a multiple of four
-    # bf16 with d_head 64 and 16-byte rows takes the tensor-core kernel: one position, a ragged
+    # bf16 with d_head 64 and 16-byte rows takes a tensor-core kernel: one position, a ragged
     # key tile with a fully masked batch entry, the bench's per-head shape, a table of five rows
     # (nearly every pair clamped); a 68-element head stride keeps d_head 64 on the SIMT kernel
     (1, 2, 64, 1, 4, "bf16", "none", 0),
@@ -37,6 +37,15 @@ TABLE = [
     (1, 3, 64, 384, 512, "bf16", "none", 0),
     (1, 2, 64, 70, 3, "bf16", "random", 0),
     (1, 2, 64, 50, 16, "bf16", "none", 68),
+    # unmasked bf16 with L <= max_len and d_head <= 64 takes the persistent tcgen05 kernel in its
+    # learned-table mode: a ragged last key tile (130 = 128 + 2 keys), L == max_len (the first and
+    # the last row of the table both used), padded heads with d_head 41, three query tiles with a
+    # ragged tail, and more (b, h) items than SMs
+    (2, 2, 64, 130, 512, "bf16", "none", 0),
+    (1, 2, 64, 257, 257, "bf16", "none", 0),
+    (2, 3, 41, 200, 300, "bf16", "none", 48),
+    (1, 4, 64, 300, 400, "bf16", "none", 0),
+    (8, 24, 32, 128, 128, "bf16", "none", 0),
 ]
 
 

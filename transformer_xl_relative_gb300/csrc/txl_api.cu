@@ -321,6 +321,68 @@ txl_status attn_tc_launch(int B, int L, int H, int D, int clamp_len, const txl_v
     return launch_attn_tc(p, s) == cudaSuccess ? TXL_OK : TXL_ERR_CUDA;
 }
 
+// The learned-table variant on the persistent tcgen05 kernel (table mode): bf16, d_head <= 64, no
+// key mask, L <= max_len (so no pair's index i - j + max_len - 1 leaves the table and no clamp
+// applies), 16-byte aligned bases and strides for q, k, v and the table.
+bool table_tc_eligible(int B, int L, int H, int D, int max_len, const txl_view* q, const txl_view* k,
+                       const txl_view* v, const void* r_table, int64_t ld_r, const uint8_t* key_mask,
+                       txl_dtype dtype)
+{
+    if (dtype != TXL_BF16 || D > 64 || key_mask || L > max_len) return false;
+    if (!view_tma_ok(q, L, H, B) || !view_tma_ok(k, L, H, B) || !view_tma_ok(v, L, H, B)) return false;
+    if (!a16(r_table) || !s16(ld_r, 2)) return false;
+    return static_cast<int64_t>((L + 127) / 128) * H * B <= INT32_MAX;
+}
+
+txl_status table_tc_launch(int B, int L, int H, int D, int max_len, const txl_view* q, const txl_view* k,
+                           const txl_view* v, const float* u, const float* v_bias, const void* r_table, int64_t ld_r,
+                           float scale, const txl_view* out, cudaStream_t s)
+{
+    if (!encoder_ready()) return TXL_ERR_CUDA;
+    AttnTcParams p;
+    std::memset(&p, 0, sizeof(p));
+    const int n_rows = 2 * max_len - 1;
+    bool ok = encode_rtab(&p.tm_r, r_table, D, H, n_rows, ld_r) &&
+              encode_view4(&p.tm_kcur, k->ptr, D, H, L, B, k->stride_h, k->stride_t, k->stride_b) &&
+              encode_view4(&p.tm_vcur, v->ptr, D, H, L, B, v->stride_h, v->stride_t, v->stride_b);
+    // even and odd query rows as two maps stepping two tokens per row (as for the main path)
+    const char* q0 = static_cast<const char*>(q->ptr);
+    ok = ok && encode_view4(&p.tm_qe, q0, D, H, (L + 1) / 2, B, q->stride_h, 2 * q->stride_t, q->stride_b, 64);
+    if (ok && L / 2 > 0)
+        ok = encode_view4(&p.tm_qo, q0 + q->stride_t * 2, D, H, L / 2, B, q->stride_h, 2 * q->stride_t,
+                          q->stride_b, 64);
+    else
+        p.tm_qo = p.tm_qe;
+    if (!ok) return TXL_ERR_CUDA;
+    p.tm_kmem = p.tm_kcur;
+    p.tm_vmem = p.tm_vcur;
+    p.u = u;
+    p.vb = v_bias;
+    p.out = out->ptr;
+    p.o_sb = out->stride_b;
+    p.o_st = out->stride_t;
+    p.o_sh = out->stride_h;
+    p.out_a16 = a16(out->ptr) && s16(out->stride_b, 2) && s16(out->stride_t, 2) && s16(out->stride_h, 2);
+    p.out_vec = (D % 8) == 0 && p.out_a16;
+    p.B = B; p.L = L; p.H = H; p.D = D;
+    p.chk = range_counter();
+    p.C = 1 << 30;                            // no clamp: every chunk is multiplied
+    p.n_rows = n_rows;
+    p.n_qt = (L + 127) / 128;
+    p.n_atoms = 1;
+    p.k_steps = (D + 15) / 16;
+    // s = scale q.k + scale q.r + u.k + v.r in the log2 domain: Qu = log2(e) (scale q + u) and
+    // Qv = log2(e) (scale q + v), the scale on q alone
+    p.qscale = scale * 1.4426950408889634f;
+    p.bscale = 1.4426950408889634f;
+    p.table = 1;
+    p.roff = max_len - 1;
+    p.sched_mode = 0;                         // every item has the same key tiles: serpentine order
+    const int sms = sm_count();
+    if (sms <= 0) return TXL_ERR_CUDA;
+    return launch_attn_persist(p, sms, s) == cudaSuccess ? TXL_OK : TXL_ERR_CUDA;
+}
+
 }  // namespace
 
 txl_status txl_rel_attn_fwd(int B, int L, int H, int D, int clamp_len, const txl_view* q, const txl_mem* mem,
@@ -794,6 +856,9 @@ txl_status txl_rel_attn_table_fwd(int B, int L, int H, int D, int max_len, const
     if (static_cast<int64_t>(max_len) * 2 - 1 > INT32_MAX) return TXL_ERR_INVALID_ARG;
     if (B == 0 || L == 0) return TXL_OK;
     if (scale <= 0.f) scale = 1.0f / std::sqrt(static_cast<float>(D));
+    if (table_tc_eligible(B, L, H, D, max_len, q, k, v, r_table, ld_r, key_mask, dtype))
+        return table_tc_launch(B, L, H, D, max_len, q, k, v, u, v_bias, r_table, ld_r, scale, out,
+                               static_cast<cudaStream_t>(stream));
     TableParams p;
     std::memset(&p, 0, sizeof(p));
     p.q = q->ptr; p.q_sb = q->stride_b; p.q_st = q->stride_t; p.q_sh = q->stride_h;

@@ -15,6 +15,14 @@
 // first S and BD products of an item hide behind the last tiles and the epilogue of the one
 // before, and no CTA launch separates them.
 //
+// The same kernel also serves the learned-table variant ("TransformerXL 相对位置编码" §3.1, the index
+// of §2): attn_persist_kernel<true> attends bidirectionally over the current sequence, reads the
+// position vector of pair (i, j) from table row i - j + max_len - 1 (every row of the sequence's
+// pairs exists when L <= max_len, so nothing clamps) and scales only the q terms: Qu = bf16(log2 e
+// (scale q + u)), Qv = bf16(log2 e (scale q + v)).  Its key tiles run from the sequence's last to its
+// first, so that the distance grows with the tile index as it does with memory, and one extra BD
+// chunk (the distances just below the first tile's) precedes every item.
+//
 // Roles (384 threads): warps 0-7 softmax / correction / epilogue (two warpgroups splitting each
 // tile's columns), warp 8 TMA producer of raw q, K and r tiles, warp 9 TMEM owner and issuer of
 // S and BD, warp 10 TMA producer of V tiles and issuer of P.V, warp 11 converter of raw q into
@@ -94,6 +102,7 @@ struct Item {
 // tile's (b, h) list (first/count: this CTA's row of the table and its prefix sums, in shared
 // memory).  Otherwise items are numbered longest first (every (b, h) of qt = n_qt - 1, then of
 // qt = n_qt - 2, ...) and dealt in serpentine rounds.
+template <bool kTab>
 __device__ __forceinline__ bool item_at(const AttnTcParams& p, const int* first, const int* count, int n, Item& it)
 {
     int qt, rem;
@@ -117,9 +126,14 @@ __device__ __forceinline__ bool item_at(const AttnTcParams& p, const int* first,
     it.h = rem % p.H;
     it.b = rem / p.H;
     it.i0 = qt * 128;
-    it.n_t = (p.M + it.i0 + 127 - p.lo) / 128 + 1;
-    const int max_delta = p.M + min(it.i0 + 127, p.L - 1) - p.lo;
-    it.clampc = p.C <= max_delta;
+    if constexpr (kTab) {
+        it.n_t = p.n_qt;                     // every key tile of the sequence
+        it.clampc = true;                    // one extra BD chunk precedes the tiles (chunk -1)
+    } else {
+        it.n_t = (p.M + it.i0 + 127 - p.lo) / 128 + 1;
+        const int max_delta = p.M + min(it.i0 + 127, p.L - 1) - p.lo;
+        it.clampc = p.C <= max_delta;
+    }
     return true;
 }
 
@@ -128,9 +142,18 @@ __device__ __forceinline__ bool need_chunk(int t, int C) { return 128 * t < C; }
 // Key tile t of an item covers keys j0 = M + i0 - 128 t; memory keys come from the ring slot
 // (wp + j0) mod slots (or j0 itself for a plain memory; a negative j0 reads TMA zero fill), and so
 // do the current segment's keys when the whole sequence lives in the ring (ring_all).
+// In learned-table mode tile t covers keys 128 (n_qt - 1 - t) ..: the last key tile first, so that
+// the distances i - j grow with t as they do with memory.
+template <bool kTab>
 __device__ __forceinline__ void key_tile(const AttnTcParams& p, const Item& it, int t, bool values,
                                          const CUtensorMap*& map, int& row)
 {
+    if constexpr (kTab) {
+        map = values ? &p.tm_vcur : &p.tm_kcur;
+        row = 128 * (p.n_qt - 1 - t);
+        if (!in_range(row, 0, p.L, p.chk)) row = 0;
+        return;
+    }
     const int j0 = p.M + it.i0 - 128 * t;
     if (j0 >= p.M && !p.ring_all) {
         map = values ? &p.tm_vcur : &p.tm_kcur;
@@ -148,6 +171,7 @@ __device__ __forceinline__ void key_tile(const AttnTcParams& p, const Item& it, 
     }
 }
 
+template <bool kTab>
 __global__ void __launch_bounds__(kPThreads, 1) attn_persist_kernel(const __grid_constant__ AttnTcParams p)
 {
     constexpr int NPV = 64;
@@ -236,7 +260,7 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_persist_kernel(const __grid
                 return true;
             };
             Item it;
-            for (int n = 0; ok && item_at(p, sched_first, sched_count, n, it); ++n) {
+            for (int n = 0; ok && item_at<kTab>(p, sched_first, sched_count, n, it); ++n) {
                 // raw q rows in TMEM-lane order: even queries of the tile to rows 0-63, odd
                 // queries to rows 64-127 (the even and odd row maps both step two tokens per row)
                 const int qb = n & 1;
@@ -246,12 +270,14 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_persist_kernel(const __grid
                 tma_load_4d(smem + PSmem::qu(qb) + kTile / 2, &p.tm_qo, 0, it.h, it.i0 >> 1, it.b,
                             &bar.qraw_full[qb]);
                 ++nq;
-                if (it.clampc && !(ok = load_r(C, it.h))) break;
+                // r row of chunk t's first distance: 128 t (learned table: 128 t + roff of the item)
+                const int roff = kTab ? p.roff + it.i0 - 128 * (p.n_qt - 1) : 0;
+                if (it.clampc && !(ok = load_r(kTab ? roff - 128 : C, it.h))) break;
                 for (int t = 0; t < it.n_t; ++t) {
-                    if (need_chunk(t, C) && !(ok = load_r(128 * t, it.h))) break;
+                    if (need_chunk(t, C) && !(ok = load_r(128 * t + roff, it.h))) break;
                     const CUtensorMap* km;
                     int row;
-                    key_tile(p, it, t, false, km, row);
+                    key_tile<kTab>(p, it, t, false, km, row);
                     const int s = kc % kNK;
                     if (!(ok = mbar_wait(&bar.k_empty[s], ((kc / kNK) & 1) ^ 1, wc, 12))) break;
                     mbar_expect_tx(&bar.k_full[s], kTile);
@@ -276,15 +302,16 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_persist_kernel(const __grid
         const int c = lane & 7;
         bool ok = true;
         Item it;
-        for (int n = 0; ok && item_at(p, sched_first, sched_count, n, it); ++n) {
+        for (int n = 0; ok && item_at<kTab>(p, sched_first, sched_count, n, it); ++n) {
             const int qb = n & 1;
             float us[8], vs[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const int d = 8 * c + e;
                 const bool in = d < p.D;
-                us[e] = in ? __ldg(p.u + static_cast<int64_t>(it.h) * p.D + d) * p.qscale : 0.f;
-                vs[e] = in ? __ldg(p.vb + static_cast<int64_t>(it.h) * p.D + d) * p.qscale : 0.f;
+                const float bs = kTab ? p.bscale : p.qscale;
+                us[e] = in ? __ldg(p.u + static_cast<int64_t>(it.h) * p.D + d) * bs : 0.f;
+                vs[e] = in ? __ldg(p.vb + static_cast<int64_t>(it.h) * p.D + d) * bs : 0.f;
             }
             const uint64_t sc2 = f2_pack(p.qscale, p.qscale);
             if (!(ok = warp_wait(&bar.qraw_full[qb], (n >> 1) & 1, wc, 40))) break;
@@ -364,7 +391,7 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_persist_kernel(const __grid
                 return true;
             };
             Item it;
-            for (int n = 0; ok && item_at(p, sched_first, sched_count, n, it); ++n) {
+            for (int n = 0; ok && item_at<kTab>(p, sched_first, sched_count, n, it); ++n) {
                 const int qb = n & 1;
                 if (!(ok = mbar_wait(&bar.q_ready[qb], (n >> 1) & 1, wc, 20))) break;
                 tc_fence_after();
@@ -406,18 +433,18 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_persist_kernel(const __grid
                 if (++cu.t >= cu.it.n_t) {
                     ++cu.n;
                     cu.t = 0;
-                    cu.valid = item_at(p, sched_first, sched_count, cu.n, cu.it);
+                    cu.valid = item_at<kTab>(p, sched_first, sched_count, cu.n, cu.it);
                 }
             };
             Cursor ld, cs;
-            ld.n = 0; ld.t = 0; ld.valid = item_at(p, sched_first, sched_count, 0, ld.it);
+            ld.n = 0; ld.t = 0; ld.valid = item_at<kTab>(p, sched_first, sched_count, 0, ld.it);
             cs = ld;
             int vc = 0, T = 0;
             bool ok = true;
             auto load_v = [&](const Cursor& cu) -> bool {
                 const CUtensorMap* vm;
                 int row;
-                key_tile(p, cu.it, cu.t, true, vm, row);
+                key_tile<kTab>(p, cu.it, cu.t, true, vm, row);
                 const int s = vc % kNV;
                 if (!mbar_wait(&bar.v_empty[s], ((vc / kNV) & 1) ^ 1, wc, 16)) return false;
                 mbar_expect_tx(&bar.v_full[s], kTile);
@@ -474,10 +501,26 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_persist_kernel(const __grid
         bool ok = true;
         int T = 0, bd = 0;                           // tiles and BD products consumed so far
         Item it;
-        for (int n = 0; item_at(p, sched_first, sched_count, n, it); ++n) {
+        for (int n = 0; item_at<kTab>(p, sched_first, sched_count, n, it); ++n) {
             const int M = p.M;
             float m_run = -INFINITY, l_half = 0.f;
             uint32_t bdc_bits = 0;                  // fp32 bits of (q+v).r[clamp_len] for this row
+            if constexpr (kTab) {
+                // learned table: chunk -1, the distances just below the first key tile's, goes
+                // into ring slot 1 (no key is masked by position)
+                if (ok) ok = warp_wait(bar.bd_full, bd & 1, wc, 31);
+                if (ok) {
+                    tc_fence_after();
+                    uint32_t bdv[64];
+                    tmem_ld64(tmem + lane_base + kColBD + 64 * hf, bdv);
+                    tmem_ld_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    mbar_arrive_if(bar.bd_free, lane == 0);
+                    ring_write_half(bdrow, row_saddr, bdv, -1, hf, sh);
+                }
+                ++bd;
+            } else {
             // The ring starts as bf16 -inf.  The positions the diagonal tile reads for future
             // keys (lj > pi) are never written before that tile, so those keys come out masked.
             {
@@ -500,6 +543,7 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_persist_kernel(const __grid
                     mbar_arrive_if(bar.bd_free, lane == 0);
                 }
                 ++bd;
+            }
             }
 
             for (int t = 0; t < it.n_t; ++t, ++T) {
@@ -543,16 +587,28 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_persist_kernel(const __grid
                 }
                 if (chunk) ++bd;
                 if (chunk || fill) pair_bar(li);            // both halves of the slot are in the ring
-                const int j0 = M + it.i0 - 128 * t;
-                const int lm = p.lo - j0;                   // keys lj < lm precede the valid memory
                 const int wbase = 64 * (t & 1) + wbase_row;
-                if (ok && lm > 0) {
-                    // only the last (oldest) tile can start before the valid memory: its invalid
-                    // keys read -inf; each thread writes exactly the positions it reads itself
-                    const int hi_lj = min(lm, 64 * hf + 64);
+                if constexpr (kTab) {
+                    // keys past the sequence's end (only in the first tile, the last key tile)
+                    // read -inf; each thread writes exactly the positions it reads itself
+                    const int lk = p.L - 128 * (p.n_qt - 1 - t);
+                    if (ok && lk < 64 * hf + 64) {
 #pragma unroll 1
-                    for (int lj = 64 * hf; lj < hi_lj; ++lj)
-                        sts_u16(row_saddr + 2u * ((128 * (t & 1) + pi - lj + sh) & 255), 0xFF80);
+                        for (int lj = max(lk, 64 * hf); lj < 64 * hf + 64; ++lj)
+                            sts_u16(row_saddr + 2u * ((128 * (t & 1) + pi - lj + sh) & 255), 0xFF80);
+                    }
+                } else {
+                    const int j0 = M + it.i0 - 128 * t;
+                    const int lm = p.lo - j0;               // keys lj < lm precede the valid memory
+                    if (ok && lm > 0) {
+                        // only the last (oldest) tile can start before the valid memory: its
+                        // invalid keys read -inf; each thread writes exactly the positions it
+                        // reads itself
+                        const int hi_lj = min(lm, 64 * hf + 64);
+#pragma unroll 1
+                        for (int lj = 64 * hf; lj < hi_lj; ++lj)
+                            sts_u16(row_saddr + 2u * ((128 * (t & 1) + pi - lj + sh) & 255), 0xFF80);
+                    }
                 }
                 float mloc = -INFINITY;
                 if (ok) {
@@ -710,14 +766,17 @@ cudaError_t launch_attn_persist(const AttnTcParams& p, int sm_count, cudaStream_
     if (p.B == 0 || p.L == 0 || p.H == 0) return cudaSuccess;
     static bool attr_done = false;
     if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(attn_persist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(attn_persist_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              PSmem::Size);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(attn_persist_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, PSmem::Size);
         if (e != cudaSuccess) return e;
         attr_done = true;
     }
     const int64_t items = static_cast<int64_t>(p.n_qt) * p.H * p.B;
     const int grid = static_cast<int>(items < sm_count ? items : sm_count);
-    return launch_dependent(attn_persist_kernel, dim3(grid), dim3(kPThreads), PSmem::Size, s, p);
+    if (p.table) return launch_dependent(attn_persist_kernel<true>, dim3(grid), dim3(kPThreads), PSmem::Size, s, p);
+    return launch_dependent(attn_persist_kernel<false>, dim3(grid), dim3(kPThreads), PSmem::Size, s, p);
 }
 
 }  // namespace txl

@@ -130,6 +130,11 @@ struct AttnTcParams {
     // processes (0 entries when sched_mode == 0: serpentine order instead)
     int sched_mode;
     uint8_t sched_counts[kSchedCapacity];
+    // persistent kernel, learned-table mode (table = 1): bidirectional attention over the current
+    // sequence alone (no memory, no causal mask, no clamp: every distance i - j of the sequence has
+    // its own row i - j + roff of the table); the biases are scaled by bscale instead of qscale
+    int table, roff;
+    float bscale;
 };
 
 cudaError_t launch_attn_tc(const AttnTcParams& p, cudaStream_t s);
