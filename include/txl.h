@@ -155,6 +155,10 @@ int txl_rel_attn_path(int B, int L, int H, int D, const txl_view* q, const txl_m
  * The keys of every (b, h) are split into chunks of 256 processed by separate CTAs on the CUDA
  * cores (the work is bound by HBM bandwidth: about one flop per byte at L = 1), then the chunks
  * are merged (split-K softmax).  Calls that share a workspace must not overlap on the GPU.
+ * With L >= 3, bf16, D <= 64 and inputs that txl_rel_attn_fwd's fused kernel takes (16-byte aligned
+ * rows and strides; a ring's write pointer and length multiples of 128), the call runs that fused
+ * tensor-core kernel instead (one query tile over every key, faster from three queries on) and
+ * leaves the workspace untouched; the argument checks, the workspace check included, are the same.
  */
 txl_status txl_rel_attn_decode(int B, int L, int H, int D, int clamp_len,
                                const txl_view* q, const txl_mem* mem,
@@ -190,6 +194,8 @@ size_t txl_rel_attn_decode_workspace_size(int B, int L, int H, int D, const txl_
  *     start at zero, but calls that overlap on the GPU (two streams, or two host threads on
  *     different streams) race on it and their results are undefined: keep them ordered, for
  *     instance on one stream.
+ * Calls that txl_rel_attn_decode sends to the fused kernel (L >= 3, see there) do so here as well
+ * and do not touch the array (the size limit above still applies to them).
  */
 txl_status txl_rel_attn_decode_noalloc(int B, int L, int H, int D, int clamp_len,
                                        const txl_view* q, const txl_mem* mem,

@@ -59,6 +59,10 @@ DECODE = [
     (2, 4, 64, 128, 1, 4096, 4096, 1000, 1000, "bf16", 0),  # long memory: 17 chunks, distances clamp
     (1, 2, 8, 16, 8, 8, 8, 3, 16, "f32", 0),                # fp32, tiny
     (1, 2, 32, 32, 2, 777, 500, 600, 64, "f32", 0),         # fp32 ring, clamp far inside
+    # three or more queries with d_head <= 64 on memories the fused kernel takes go to it: a plain
+    # memory, and a partly valid ring whose write pointer and length are multiples of 128
+    (2, 4, 64, 128, 8, 1024, 1024, 0, 1000, "bf16", 0),
+    (1, 3, 64, 128, 4, 512, 300, 256, 200, "bf16", 0),
 ]
 
 

@@ -87,7 +87,8 @@ def oracle_of(c, rows=None):
 def test_noalloc_matches_the_workspace_entry_point_twice(txl):
     from transformer_xl_relative_gb300 import native
     calls = [make_call(txl, 2, 4, 64, 3, 1000, 900, 37, 500, seed=11),     # 4 chunks per (b, h)
-             make_call(txl, 3, 2, 64, 1, 2200, 2200, 300, 1000, seed=12)]  # 9 chunks, other shape
+             make_call(txl, 3, 2, 64, 1, 2200, 2200, 300, 1000, seed=12),  # 9 chunks, other shape
+             make_call(txl, 2, 2, 64, 4, 640, 640, 128, 1000, seed=16)]    # the fused kernel's route
     refs = [with_workspace(txl, c) for c in calls]
     outs = [torch.full_like(c["q"], float("nan")) for c in calls]
     # two calls in a row on one stream: the second reuses the scratch the first has just used

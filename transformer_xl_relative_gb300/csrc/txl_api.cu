@@ -383,6 +383,18 @@ txl_status table_tc_launch(int B, int L, int H, int D, int max_len, const txl_vi
     return launch_attn_persist(p, sms, s) == cudaSuccess ? TXL_OK : TXL_ERR_CUDA;
 }
 
+// Decode calls with three or more new queries per (b, h) take the persistent fused kernel when it
+// accepts the inputs: one query tile over every key outruns the chunked decode kernels there (B8
+// H16 D64 M4096 bf16: 54 us for any L <= 16, against 76 us at L = 3, 220 us at L = 8 and 574 us at
+// L = 16; at L = 1 and 2 the decode kernels take 40 and 49 us).  It needs no workspace.
+constexpr int kDecodeFusedMinL = 3;
+
+bool decode_takes_fused(int B, int L, int H, int D, const txl_view* q, const txl_mem* mem, const txl_view* k_cur,
+                        const txl_view* v_cur, const void* r, int64_t ld_r, txl_dtype dtype)
+{
+    return L >= kDecodeFusedMinL && D <= 64 && attn_tc_eligible(B, L, H, D, q, mem, k_cur, v_cur, r, ld_r, dtype);
+}
+
 }  // namespace
 
 txl_status txl_rel_attn_fwd(int B, int L, int H, int D, int clamp_len, const txl_view* q, const txl_mem* mem,
@@ -453,6 +465,9 @@ txl_status txl_rel_attn_decode(int B, int L, int H, int D, int clamp_len, const 
     if (!workspace || workspace_bytes < need || !a16(workspace)) return TXL_ERR_WORKSPACE;
     if (B > 65535 || H > 65535) return TXL_ERR_UNSUPPORTED;
     if (scale <= 0.f) scale = 1.0f / std::sqrt(static_cast<float>(D));
+    if (decode_takes_fused(B, L, H, D, q, mem, k_cur, v_cur, r, ld_r, dtype))
+        return attn_tc_launch(B, L, H, D, clamp_len, q, mem, k_cur, v_cur, u, v_bias, r, ld_r, n_rows, scale, out,
+                              nullptr, static_cast<cudaStream_t>(stream), 0);
     const int elem = dtype == TXL_F32 ? 4 : 2;
     auto rows16 = [&](const void* ptr, int64_t sb, int64_t st_, int64_t sh) {
         return a16(ptr) && s16(sb, elem) && s16(st_, elem) && s16(sh, elem);
@@ -502,9 +517,12 @@ txl_status txl_rel_attn_decode_noalloc(int B, int L, int H, int D, int clamp_len
     const double need = static_cast<double>(B) * H * L * n_chunks * (D + 2) * sizeof(float);
     if (need > static_cast<double>(kDecodeStaticScratchBytes)) return TXL_ERR_WORKSPACE;
     if (B > 65535 || H > 65535) return TXL_ERR_UNSUPPORTED;
+    if (scale <= 0.f) scale = 1.0f / std::sqrt(static_cast<float>(D));
+    if (decode_takes_fused(B, L, H, D, q, mem, k_cur, v_cur, r, ld_r, dtype))
+        return attn_tc_launch(B, L, H, D, clamp_len, q, mem, k_cur, v_cur, u, v_bias, r, ld_r, n_rows, scale, out,
+                              nullptr, static_cast<cudaStream_t>(stream), 0);
     float* scratch = nullptr;
     if (decode_static_scratch(&scratch) != cudaSuccess || !scratch) return TXL_ERR_CUDA;
-    if (scale <= 0.f) scale = 1.0f / std::sqrt(static_cast<float>(D));
     const int elem = dtype == TXL_F32 ? 4 : 2;
     auto rows16 = [&](const void* ptr, int64_t sb, int64_t st_, int64_t sh) {
         return a16(ptr) && s16(sb, elem) && s16(st_, elem) && s16(sh, elem);

@@ -35,6 +35,8 @@ namespace {
 
 constexpr int kDecThreads = 256;
 constexpr int kDecWarps = kDecThreads / 32;
+constexpr int kCopyRows = kDecThreads / 8;         // rows one pass of 16-byte copies covers
+static_assert(kDecThreads == kDecodeChunk, "one thread per key of a chunk");
 
 template <typename T> __device__ __forceinline__ float to_f(T x);
 template <> __device__ __forceinline__ float to_f<float>(float x) { return x; }
@@ -365,8 +367,8 @@ __global__ void __launch_bounds__(kDecThreads) decode_staged_kernel(const __grid
         const uint32_t ks_s = static_cast<uint32_t>(__cvta_generic_to_shared(ks)) + r0 * kStRowBytes + 16 * pc;
         const uint32_t vs_s = static_cast<uint32_t>(__cvta_generic_to_shared(vs)) + r0 * kStRowBytes + 16 * pc;
 #pragma unroll
-        for (int k = 0; k < kDecodeChunk / 32; ++k) {
-            const int j = j0 + r0 + 32 * k;
+        for (int k = 0; k < kDecodeChunk / kCopyRows; ++k) {
+            const int j = j0 + r0 + kCopyRows * k;
             const bool live = j < K && j >= p.lo;
             const __nv_bfloat16* ksrc = dummy;
             const __nv_bfloat16* vsrc = dummy;
@@ -380,8 +382,8 @@ __global__ void __launch_bounds__(kDecThreads) decode_staged_kernel(const __grid
                     vsrc = vcur + static_cast<int64_t>(j - p.M) * p.vc_st;
                 }
             }
-            cp_async16(ks_s + 32 * k * kStRowBytes, ksrc, live);
-            cp_async16(vs_s + 32 * k * kStRowBytes, vsrc, live);
+            cp_async16(ks_s + kCopyRows * k * kStRowBytes, ksrc, live);
+            cp_async16(vs_s + kCopyRows * k * kStRowBytes, vsrc, live);
         }
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
@@ -415,11 +417,11 @@ __global__ void __launch_bounds__(kDecThreads) decode_staged_kernel(const __grid
     // 2. position band, eight lanes per row (lane part holds 16-byte piece part); each lane
     //    requests its pieces of all its rows before using any
     if (!band_const) {
-        constexpr int kBandIter = (kDecodeChunk + kDecodeMaxL + 31) / 32;
+        constexpr int kBandIter = (kDecodeChunk + kDecodeMaxL + 4 * kDecWarps - 1) / (4 * kDecWarps);
         uint4 raw[kBandIter];
 #pragma unroll
         for (int k = 0; k < kBandIter; ++k) {
-            const int rho = 4 * warp + 32 * k + rg;
+            const int rho = 4 * warp + 4 * kDecWarps * k + rg;
             const int delta = delta_top - rho;
             raw[k] = make_uint4(0u, 0u, 0u, 0u);
             if (rho < n_band && delta >= 0 && part < dch) {
@@ -430,7 +432,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_staged_kernel(const __grid
         }
 #pragma unroll
         for (int k = 0; k < kBandIter; ++k) {
-            const int rho = 4 * warp + 32 * k + rg;
+            const int rho = 4 * warp + 4 * kDecWarps * k + rg;
             float acc[LQ];
 #pragma unroll
             for (int i = 0; i < LQ; ++i) acc[i] = 0.f;
