@@ -352,10 +352,12 @@ txl_status txl_rel_pos_bwd(int n_rows, int d_model, int n_head, int d_head, cons
  *   q, k, v, out : views of [B][L][H][D] (device, dtype).  u, v_bias : device fp32 [H][D].
  *   r_table : device [2*max_len - 1][H][ld_r], dtype.  key_mask : device uint8 [B][L] or NULL.
  *   scale   : <= 0 selects 1/sqrt(D).
- * Limits: 1 <= D <= 128, max_len >= 1.  bf16 with D <= 64, no key_mask, L <= max_len and 16-byte
- * aligned bases and strides (q, k, v, r_table): the persistent tcgen05 kernel of txl_rel_attn_fwd in
- * a learned-table mode (log2(e)(scale*q + u), log2(e)(scale*q + v) and P rounded to bf16 as product
- * operands, fp32 accumulation in tensor memory).  Other bf16 calls with D = 64 and 16-byte aligned
+ * Limits: 1 <= D <= 128, max_len >= 1.  bf16 with D <= 64, L <= max_len and 16-byte aligned bases
+ * and strides (q, k, v, r_table): the persistent tcgen05 kernel of txl_rel_attn_fwd in a learned-table
+ * mode (log2(e)(scale*q + u), log2(e)(scale*q + v) and P rounded to bf16 as product operands, fp32
+ * accumulation in tensor memory; a masked key's score is about -1e30 there, which gives it the same
+ * weight as -1e9: exactly 0 beside any unmasked key, equal weights in a fully masked row).  Other bf16
+ * calls with D = 64 and 16-byte aligned
  * rows and strides (q, k, v, out, r_table): bf16 mma.sync products with fp32 accumulation (scale*q + u,
  * scale*q + v and P rounded to bf16).  Every other case: fp32 arithmetic on the CUDA cores.
  */

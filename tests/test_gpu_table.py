@@ -46,6 +46,10 @@ TABLE = [
     (2, 3, 41, 200, 300, "bf16", "none", 48),
     (1, 4, 64, 300, 400, "bf16", "none", 0),
     (8, 24, 32, 128, 128, "bf16", "none", 0),
+    # ... and with a key mask (masked keys read a score of about -1e30 from the ring): random masks
+    # over three query tiles and over padded heads; the one_empty case above (L = 130) takes it too
+    (2, 3, 64, 300, 512, "bf16", "random", 0),
+    (1, 2, 41, 150, 200, "bf16", "random", 48),
 ]
 
 

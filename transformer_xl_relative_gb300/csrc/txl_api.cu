@@ -321,14 +321,15 @@ txl_status attn_tc_launch(int B, int L, int H, int D, int clamp_len, const txl_v
     return launch_attn_tc(p, s) == cudaSuccess ? TXL_OK : TXL_ERR_CUDA;
 }
 
-// The learned-table variant on the persistent tcgen05 kernel (table mode): bf16, d_head <= 64, no
-// key mask, L <= max_len (so no pair's index i - j + max_len - 1 leaves the table and no clamp
-// applies), 16-byte aligned bases and strides for q, k, v and the table.
+// The learned-table variant on the persistent tcgen05 kernel (table mode, with or without a key
+// mask): bf16, d_head <= 64, L <= max_len (so no pair's index i - j + max_len - 1 leaves the table and
+// no clamp applies), 16-byte aligned bases and strides for q, k, v and the table.
 bool table_tc_eligible(int B, int L, int H, int D, int max_len, const txl_view* q, const txl_view* k,
                        const txl_view* v, const void* r_table, int64_t ld_r, const uint8_t* key_mask,
                        txl_dtype dtype)
 {
-    if (dtype != TXL_BF16 || D > 64 || key_mask || L > max_len) return false;
+    (void)key_mask;
+    if (dtype != TXL_BF16 || D > 64 || L > max_len) return false;
     if (!view_tma_ok(q, L, H, B) || !view_tma_ok(k, L, H, B) || !view_tma_ok(v, L, H, B)) return false;
     if (!a16(r_table) || !s16(ld_r, 2)) return false;
     return static_cast<int64_t>((L + 127) / 128) * H * B <= INT32_MAX;
@@ -336,7 +337,7 @@ bool table_tc_eligible(int B, int L, int H, int D, int max_len, const txl_view* 
 
 txl_status table_tc_launch(int B, int L, int H, int D, int max_len, const txl_view* q, const txl_view* k,
                            const txl_view* v, const float* u, const float* v_bias, const void* r_table, int64_t ld_r,
-                           float scale, const txl_view* out, cudaStream_t s)
+                           const uint8_t* key_mask, float scale, const txl_view* out, cudaStream_t s)
 {
     if (!encoder_ready()) return TXL_ERR_CUDA;
     AttnTcParams p;
@@ -375,7 +376,8 @@ txl_status table_tc_launch(int B, int L, int H, int D, int max_len, const txl_vi
     // Qv = log2(e) (scale q + v), the scale on q alone
     p.qscale = scale * 1.4426950408889634f;
     p.bscale = 1.4426950408889634f;
-    p.table = 1;
+    p.table = key_mask ? 2 : 1;
+    p.key_mask = key_mask;
     p.roff = max_len - 1;
     p.sched_mode = 0;                         // every item has the same key tiles: serpentine order
     const int sms = sm_count();
@@ -875,7 +877,7 @@ txl_status txl_rel_attn_table_fwd(int B, int L, int H, int D, int max_len, const
     if (B == 0 || L == 0) return TXL_OK;
     if (scale <= 0.f) scale = 1.0f / std::sqrt(static_cast<float>(D));
     if (table_tc_eligible(B, L, H, D, max_len, q, k, v, r_table, ld_r, key_mask, dtype))
-        return table_tc_launch(B, L, H, D, max_len, q, k, v, u, v_bias, r_table, ld_r, scale, out,
+        return table_tc_launch(B, L, H, D, max_len, q, k, v, u, v_bias, r_table, ld_r, key_mask, scale, out,
                                static_cast<cudaStream_t>(stream));
     TableParams p;
     std::memset(&p, 0, sizeof(p));

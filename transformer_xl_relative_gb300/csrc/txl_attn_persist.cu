@@ -171,7 +171,12 @@ __device__ __forceinline__ void key_tile(const AttnTcParams& p, const Item& it, 
     }
 }
 
-template <bool kTab>
+// kMask (learned-table mode with a key mask): keys whose mask byte is 0 read a score of about -1e30
+// from the ring (bf16 0xF14A); added to any finite logit it stays exactly that value, so such keys
+// get weight 0 beside any unmasked key, and a row whose keys are all masked weighs them equally.
+constexpr uint16_t kMaskedKeyBf16 = 0xF14A;
+
+template <bool kTab, bool kMask = false>
 __global__ void __launch_bounds__(kPThreads, 1) attn_persist_kernel(const __grid_constant__ AttnTcParams p)
 {
     constexpr int NPV = 64;
@@ -553,6 +558,14 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_persist_kernel(const __grid
                 const bool fill = it.clampc && !chunk && (t < 2 || need_chunk(t - 2, C));
                 const uint32_t scol = tmem + lane_base + ((T & 1) ? kColS1 : kColS0) + 64 * hf;
                 float s[64];
+                bool kz0 = false, kz1 = false;              // keys lane, lane + 32 of this half masked
+                if constexpr (kMask) {
+                    // requested now, used after the ring write: the loads fly during the waits
+                    const int jk = 128 * (p.n_qt - 1 - t) + 64 * hf + lane;
+                    const uint8_t* km = p.key_mask + static_cast<int64_t>(it.b) * p.L;
+                    kz0 = jk < p.L && __ldg(km + jk) == 0;
+                    kz1 = jk + 32 < p.L && __ldg(km + jk + 32) == 0;
+                }
                 if (chunk && ok) ok = warp_wait(bar.bd_full, bd & 1, wc, 32);
                 if (ok) ok = warp_wait(&bar.s_full[T & 1], (T >> 1) & 1, wc, 33);
                 if (ok) {
@@ -596,6 +609,16 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_persist_kernel(const __grid
 #pragma unroll 1
                         for (int lj = max(lk, 64 * hf); lj < 64 * hf + 64; ++lj)
                             sts_u16(row_saddr + 2u * ((128 * (t & 1) + pi - lj + sh) & 255), 0xFF80);
+                    }
+                    if constexpr (kMask) {
+                        // masked keys of this half (the same for every row: a warp-uniform loop)
+                        uint64_t z = (static_cast<uint64_t>(__ballot_sync(0xffffffffu, kz1)) << 32) |
+                                     __ballot_sync(0xffffffffu, kz0);
+                        while (ok && z) {
+                            const int lj = 64 * hf + __ffsll(static_cast<long long>(z)) - 1;
+                            z &= z - 1;
+                            sts_u16(row_saddr + 2u * ((128 * (t & 1) + pi - lj + sh) & 255), kMaskedKeyBf16);
+                        }
                     }
                 } else {
                     const int j0 = M + it.i0 - 128 * t;
@@ -771,10 +794,15 @@ cudaError_t launch_attn_persist(const AttnTcParams& p, int sm_count, cudaStream_
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(attn_persist_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, PSmem::Size);
         if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(attn_persist_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 PSmem::Size);
+        if (e != cudaSuccess) return e;
         attr_done = true;
     }
     const int64_t items = static_cast<int64_t>(p.n_qt) * p.H * p.B;
     const int grid = static_cast<int>(items < sm_count ? items : sm_count);
+    if (p.table == 2)
+        return launch_dependent(attn_persist_kernel<true, true>, dim3(grid), dim3(kPThreads), PSmem::Size, s, p);
     if (p.table) return launch_dependent(attn_persist_kernel<true>, dim3(grid), dim3(kPThreads), PSmem::Size, s, p);
     return launch_dependent(attn_persist_kernel<false>, dim3(grid), dim3(kPThreads), PSmem::Size, s, p);
 }

@@ -135,6 +135,7 @@ struct AttnTcParams {
     // its own row i - j + roff of the table); the biases are scaled by bscale instead of qscale
     int table, roff;
     float bscale;
+    const uint8_t* key_mask;     // learned-table mode 2: [B][L], keys with 0 score -1e9
 };
 
 cudaError_t launch_attn_tc(const AttnTcParams& p, cudaStream_t s);
