@@ -311,8 +311,10 @@ size_t txl_rel_attn_layer_fused_workspace_size(int B, int L, int H, int D);
  *   workspace : device, >= txl_rel_attn_bwd_workspace_size(B, L, H, D) bytes, 16-byte aligned.
  * Scores are recomputed and P is never stored.  bf16 with D = 64 and 16-byte aligned rows and
  * strides (q, k, v, the memory, d_out, r): bf16 products on the tensor cores with fp32 accumulation
- * (P and dS rounded to bf16 as product operands; pairs whose distance reaches clamp_len summed in
- * fp32).  Every other case: fp32 arithmetic on the CUDA cores.  Enqueues several launches.
+ * (c(q + u), c(q + v), P and dS rounded to bf16 as product operands, c = scale log2 e; pairs whose
+ * distance reaches clamp_len summed in fp32), the row log-sum-exp taken by the fused forward kernel
+ * when that kernel takes the inputs (written into the workspace).  Every other case: fp32
+ * arithmetic on the CUDA cores.  Enqueues several launches.
  */
 txl_status txl_rel_attn_bwd(int B, int L, int H, int D, int clamp_len,
                             const txl_view* q, const txl_mem* mem,

@@ -243,7 +243,7 @@ namespace {
 txl_status attn_tc_launch(int B, int L, int H, int D, int clamp_len, const txl_view* q, const txl_mem* mem,
                           const txl_view* k_cur, const txl_view* v_cur, const float* u, const float* v_bias,
                           const void* r, int64_t ld_r, int n_rows, float scale, const txl_view* out, int* err_flag,
-                          cudaStream_t s, int ring_slots)
+                          cudaStream_t s, int ring_slots, float* lse = nullptr)
 {
     const int M = (mem && mem->M > 0) ? mem->M : 0;
     const int valid = M > 0 ? mem->valid : 0;
@@ -292,6 +292,8 @@ txl_status attn_tc_launch(int B, int L, int H, int D, int clamp_len, const txl_v
     p.k_steps = (D + 15) / 16;
     p.qscale = scale * 1.4426950408889634f;
     p.err_flag = err_flag;
+    p.lse = lse;
+    if (lse && p.n_atoms != 1) return TXL_ERR_UNSUPPORTED;
     if (p.n_atoms == 1) {
         if (static_cast<int64_t>(p.n_qt) * H * B > INT32_MAX) return TXL_ERR_UNSUPPORTED;
         // even and odd query rows as two maps stepping two tokens per row; the odd map starts
@@ -851,6 +853,15 @@ txl_status txl_rel_attn_bwd(int B, int L, int H, int D, int clamp_len, const txl
     p.dd = ws + rows;
     p.pac = ws + 2 * rows;
     p.pbd = ws + 2 * rows + rows * D;
+    // On the tensor-core gradient path the fused forward kernel computes every row's log-sum-exp
+    // (its statistics alone, nothing else written), in place of the gradient kernel's own first
+    // pass over the keys
+    if (bwd_tc_eligible(p, dtype) && attn_tc_eligible(B, L, H, D, q, mem, k_cur, v_cur, r, ld_r, dtype)) {
+        const txl_status fs = attn_tc_launch(B, L, H, D, clamp_len, q, mem, k_cur, v_cur, u, v_bias, r, ld_r, n_rows,
+                                             scale, out, nullptr, s, 0, p.lse);
+        if (fs != TXL_OK) return fs;
+        p.lse_given = 1;
+    }
     return launch_rel_attn_bwd(p, dtype, s) == cudaSuccess ? TXL_OK : TXL_ERR_CUDA;
 }
 

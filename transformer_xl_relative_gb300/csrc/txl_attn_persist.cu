@@ -176,7 +176,8 @@ __device__ __forceinline__ void key_tile(const AttnTcParams& p, const Item& it, 
 // get weight 0 beside any unmasked key, and a row whose keys are all masked weighs them equally.
 constexpr uint16_t kMaskedKeyBf16 = 0xF14A;
 
-template <bool kTab, bool kMask = false>
+// kLse: the row statistics alone (log-sum-exp for the gradient kernels): no output is written.
+template <bool kTab, bool kMask = false, bool kLse = false>
 __global__ void __launch_bounds__(kPThreads, 1) attn_persist_kernel(const __grid_constant__ AttnTcParams p)
 {
     constexpr int NPV = 64;
@@ -657,6 +658,16 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_persist_kernel(const __grid
                     const uint64_t negm = f2_pack(-m_run, -m_run);
                     float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
                     uint32_t pw[32];
+                    if constexpr (kLse) {
+                        // the row sum alone, from fp32 exponentials of the fp32 logits (P is not
+                        // needed: zeros go through P.V)
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) {
+                            a0 += ex2_approx(s[2 * k] - m_run);
+                            b0 += ex2_approx(s[2 * k + 1] - m_run);
+                            pw[k] = 0u;
+                        }
+                    } else {
 #pragma unroll
                     for (int k = 0; k < 32; ++k) {
                         float y0, y1;
@@ -669,6 +680,7 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_persist_kernel(const __grid
                             a0 = add_bf16lo_f32(pw[k], a0);
                             a1 = add_bf16hi_f32(pw[k], a1);
                         }
+                    }
                     }
                     l_half = fmaf(l_half, alpha, (a0 + a1) + (b0 + b1));
                     // P.V of the previous tile (of this item or the one before) must be complete
@@ -713,7 +725,15 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_persist_kernel(const __grid
             xchg[2 * (it.n_t & 1) + hf] = l_half;
             pair_bar(li);
             const bool staged = p.out_a16 != 0;
-            if (ok) {
+            if (ok && kLse) {
+                // log2-domain log-sum-exp of the row, in the scaled score units of the logits
+                __syncwarp();
+                mbar_arrive_if(bar.o_free, lane == 0);
+                const int i = it.i0 + pi;
+                if (hf == 0 && i < p.L)
+                    p.lse[(static_cast<int64_t>(it.b) * p.L + i) * p.H + it.h] =
+                        m_run + __log2f(l_half + xchg[2 * (it.n_t & 1) + 1]);
+            } else if (ok) {
                 uint32_t o[32];
                 tc_fence_after();
                 tmem_ld32(tmem + lane_base + kColO + (NPV / 2) * hf, o);
@@ -745,7 +765,7 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_persist_kernel(const __grid
                 }
             }
             pair_bar(li);                                   // both halves of every row are staged
-            if (ok && staged) {
+            if (!kLse && ok && staged) {
                 // this warp stores rows (li & ~31) + 16 hf + 0..15: lane -> row + lane / 8, chunk
                 // of 8 columns lane mod 8
                 const uint32_t* bd0 = reinterpret_cast<const uint32_t*>(smem + PSmem::BD);
@@ -797,10 +817,16 @@ cudaError_t launch_attn_persist(const AttnTcParams& p, int sm_count, cudaStream_
         e = cudaFuncSetAttribute(attn_persist_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  PSmem::Size);
         if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(attn_persist_kernel<false, false, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, PSmem::Size);
+        if (e != cudaSuccess) return e;
         attr_done = true;
     }
     const int64_t items = static_cast<int64_t>(p.n_qt) * p.H * p.B;
     const int grid = static_cast<int>(items < sm_count ? items : sm_count);
+    if (p.lse && !p.table)
+        return launch_dependent(attn_persist_kernel<false, false, true>, dim3(grid), dim3(kPThreads), PSmem::Size,
+                                s, p);
     if (p.table == 2)
         return launch_dependent(attn_persist_kernel<true, true>, dim3(grid), dim3(kPThreads), PSmem::Size, s, p);
     if (p.table) return launch_dependent(attn_persist_kernel<true>, dim3(grid), dim3(kPThreads), PSmem::Size, s, p);

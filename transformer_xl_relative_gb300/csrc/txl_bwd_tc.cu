@@ -19,7 +19,10 @@
 // Pairs whose distance reaches clamp_len all share r[clamp_len]; their dS nearly cancel (each row of
 // dS sums to zero), so they stay out of the bf16 G: their fp32 sum per row c_i enters dq_i as
 // c_i r[clamp_len] and dr[clamp_len] as sum_i c_i q''_i.
-// A first sweep over the key tiles takes the row log-sum-exp; the second computes the gradients.
+// The scores use the forward kernel's query forms Qc' = bf16(c q') and Qc'' = bf16(c q''), so the
+// row log-sum-exp L2_i the persistent forward kernel writes (txl_rel_attn_bwd has it computed when
+// that kernel takes the inputs) belongs to them; otherwise a first sweep over the key tiles takes
+// it here.  The sweep over the key tiles then computes the gradients.
 // dq goes straight to its rows (one CTA per query row); the per-query parts of du and dv_bias go
 // to the workspace the bias reduction of txl_bwd.cu sums.
 #include <cuda_bf16.h>
@@ -34,6 +37,7 @@ namespace {
 using namespace mma;
 
 constexpr int kBT = 128;                 // threads: four warps
+constexpr float kLn2 = 0.693147180559945309f;   // scale / c: the gradients through Qc' and Qc''
 constexpr int kQT = 64;                  // queries per CTA
 constexpr int kKT = 64;                  // keys per tile
 constexpr int kWin = 128;                // position rows per tile window (127 used)
@@ -109,12 +113,13 @@ __device__ __forceinline__ void issue_tiles(const BwdParams& p, uint8_t* sm, int
 }
 
 // Scores of this warp's 16 rows against key tile t (keys from j0), in the log2 domain (c s), masked
-// to -inf: S = Q' K^T from the tensor cores plus BD remapped from the window product Q'' R_win^T.
+// to -inf: S = Qc' K^T from the tensor cores plus BD remapped from the window product Qc'' R_win^T,
+// with the scaled query forms Qc' = bf16(c q'), Qc'' = bf16(c q'') of the forward kernel.
 // Window row w of tile t + 1 is window row w + 64 of tile t, so the products live in a per-row ring
 // (row w of tile t in column (w + 64 t) mod 192) and every tile after a sweep's first multiplies
 // only its 64 new rows.
 __device__ __forceinline__ void tile_scores(const BwdParams& p, uint8_t* sm, int warp, int lane, int i0, int j0,
-                                            int t, float c, float (&s)[8][4])
+                                            int t, float (&s)[8][4])
 {
     const AttnSimtParams& a = p.a;
     const uint32_t sbase = cvta_smem(sm);
@@ -170,7 +175,7 @@ __device__ __forceinline__ void tile_scores(const BwdParams& p, uint8_t* sm, int
         }
     }
     __syncwarp();
-    // s_ij = c (S_ij + BD[i][i - j + 63]) for visible pairs, -inf otherwise
+    // s_ij = S_ij + BD[i][i - j + 63] (both already scaled by c) for visible pairs, -inf otherwise
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr) {
         const int il = 16 * warp + g + 8 * hr;
@@ -185,7 +190,7 @@ __device__ __forceinline__ void tile_scores(const BwdParams& p, uint8_t* sm, int
                 int cw = il - jl + 63 + roff;
                 cw = cw >= kBdRing ? cw - kBdRing : cw;
                 const float x = s[n][2 * hr + e] + __bfloat162float(bd[il * kBdPitch + cw]);
-                s[n][2 * hr + e] = vis ? c * x : -INFINITY;
+                s[n][2 * hr + e] = vis ? x : -INFINITY;
             }
         }
     }
@@ -204,7 +209,9 @@ __global__ void __launch_bounds__(kBT) bwd_tc_kernel(const BwdParams p)
     const uint32_t sbase = cvta_smem(sm);
     const float c = a.scale * 1.4426950408889634f;
 
-    // ---- Q' = q + u, Q'' = q + v_bias and dO of the CTA's rows (bf16, zero past L)
+    // ---- Qc' = c (q + u), Qc'' = c (q + v_bias) and dO of the CTA's rows (bf16, zero past L), the
+    //      query forms rounded exactly as the forward kernel rounds them (one fma of q with c and the
+    //      product c u), so that the forward's log-sum-exp belongs to these scores
 #pragma unroll
     for (int x = 0; x < (kQT * 8) / kBT; ++x) {
         const int id = tid + kBT * x;
@@ -222,8 +229,8 @@ __global__ void __launch_bounds__(kBT) bwd_tc_kernel(const BwdParams p)
             for (int e = 0; e < 4; ++e) {
                 const int d = 8 * ch + 2 * e;
                 const float x0 = bf16_lo(qw[e]), x1 = bf16_hi(qw[e]);
-                ou[e] = pack2(x0 + __ldg(a.u + h * 64 + d), x1 + __ldg(a.u + h * 64 + d + 1));
-                ov[e] = pack2(x0 + __ldg(a.vb + h * 64 + d), x1 + __ldg(a.vb + h * 64 + d + 1));
+                ou[e] = pack2(fmaf(x0, c, __ldg(a.u + h * 64 + d) * c), fmaf(x1, c, __ldg(a.u + h * 64 + d + 1) * c));
+                ov[e] = pack2(fmaf(x0, c, __ldg(a.vb + h * 64 + d) * c), fmaf(x1, c, __ldg(a.vb + h * 64 + d + 1) * c));
             }
             wu = make_uint4(ou[0], ou[1], ou[2], ou[3]);
             wv = make_uint4(ov[0], ov[1], ov[2], ov[3]);
@@ -254,16 +261,16 @@ __global__ void __launch_bounds__(kBT) bwd_tc_kernel(const BwdParams p)
 
     const int n_t = (a.M + i0 + kQT - 1 - a.lo) / kKT + 1;
 
-    // ---- sweep 1: row log-sum-exp (log2 domain)
+    // ---- sweep 1: row log-sum-exp (log2 domain), unless the fused forward kernel has written it
     float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
-    for (int t = 0; t < n_t; ++t) {
+    for (int t = 0; t < (p.lse_given ? 0 : n_t); ++t) {
         const int j0 = a.M + i0 - kKT * t;
         __syncthreads();
         issue_tiles(p, sm, b, h, j0, kKT * t - (kKT - 1), false, tid);
         cp_async_wait_all();
         __syncthreads();
         float s[8][4];
-        tile_scores(p, sm, warp, lane, i0, j0, t, c, s);
+        tile_scores(p, sm, warp, lane, i0, j0, t, s);
 #pragma unroll
         for (int hr = 0; hr < 2; ++hr) {
             float mx = -INFINITY;
@@ -285,7 +292,13 @@ __global__ void __launch_bounds__(kBT) bwd_tc_kernel(const BwdParams p)
     }
     float L2[2];
 #pragma unroll
-    for (int hr = 0; hr < 2; ++hr) L2[hr] = lrow[hr] > 0.f ? mrow[hr] + __log2f(lrow[hr]) : 0.f;
+    for (int hr = 0; hr < 2; ++hr) {
+        const int i = i0 + 16 * warp + g + 8 * hr;
+        if (p.lse_given)
+            L2[hr] = i < a.L ? p.lse[(static_cast<int64_t>(b) * a.L + i) * a.H + h] : 0.f;
+        else
+            L2[hr] = lrow[hr] > 0.f ? mrow[hr] + __log2f(lrow[hr]) : 0.f;
+    }
 
     // ---- sweep 2: gradients
     float dqa[8][4], dqb[8][4];
@@ -304,7 +317,7 @@ __global__ void __launch_bounds__(kBT) bwd_tc_kernel(const BwdParams p)
         cp_async_wait_all();
         __syncthreads();
         float s[8][4];
-        tile_scores(p, sm, warp, lane, i0, j0, t, c, s);
+        tile_scores(p, sm, warp, lane, i0, j0, t, s);
         // P, in place
 #pragma unroll
         for (int n = 0; n < 8; ++n)
@@ -424,7 +437,7 @@ __global__ void __launch_bounds__(kBT) bwd_tc_kernel(const BwdParams p)
                     }
                 }
                 float* dst = pass == 0 ? p.dv : p.dk;
-                const float f = pass == 0 ? 1.f : scale;
+                const float f = pass == 0 ? 1.f : kLn2;     // scale dS^T q' = ln 2 dS^T Qc'
 #pragma unroll
                 for (int hr = 0; hr < 2; ++hr) {
                     const int j = jw + g + 8 * hr;
@@ -473,7 +486,7 @@ __global__ void __launch_bounds__(kBT) bwd_tc_kernel(const BwdParams p)
 #pragma unroll
                     for (int n = 0; n < 8; ++n)
                         atomicAdd(reinterpret_cast<float2*>(dst + 8 * n + 2 * tg),
-                                  make_float2(scale * acc[m][n][2 * hr], scale * acc[m][n][2 * hr + 1]));
+                                  make_float2(kLn2 * acc[m][n][2 * hr], kLn2 * acc[m][n][2 * hr + 1]));
                 }
         }
     }
@@ -515,7 +528,7 @@ __global__ void __launch_bounds__(kBT) bwd_tc_kernel(const BwdParams p)
 #pragma unroll
             for (int n = 0; n < 8; ++n)
                 atomicAdd(reinterpret_cast<float2*>(dst + 8 * n + 2 * tg),
-                          make_float2(scale * part[n][0], scale * part[n][1]));
+                          make_float2(kLn2 * part[n][0], kLn2 * part[n][1]));
         }
     }
 

@@ -136,6 +136,9 @@ struct AttnTcParams {
     int table, roff;
     float bscale;
     const uint8_t* key_mask;     // learned-table mode 2: [B][L], keys with 0 score -1e9
+    // persistent kernel, log-sum-exp mode (lse != null): every query row's log2-domain
+    // log-sum-exp m + log2(l) is written to lse[(b L + i) H + h]; out is not written
+    float* lse;
 };
 
 cudaError_t launch_attn_tc(const AttnTcParams& p, cudaStream_t s);
@@ -151,6 +154,7 @@ struct BwdParams {
     float* dr; int n_rows;                      // [n_rows][H][D]
     float* lse; float* dd;                      // workspace [B][L][H]: log-sum-exp, dO . out
     float* pac; float* pbd;                     // workspace [B][L][H][D]: per-query parts of du, dv_bias
+    int lse_given;                              // lse already holds every row's log-sum-exp
 };
 
 struct PosBwdParams {
