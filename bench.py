@@ -596,9 +596,10 @@ def bwd_flops(B, H, D, L, M, n_rows, d_model):
 
 def bench_backward(txl, device, stream, rank, args):
     """Gradients of one fused-attention call on the large workload: txl_rel_attn_bwd (on this
-    workload the tensor-core kernel: bf16 mma.sync products, fp32 accumulation and gradients)
-    and the position table's txl_rel_pos_bwd, timed together and each alone.  The attention
-    backward is reported against the measured bf16 tensor peak."""
+    workload the fused forward kernel's row log-sum-exp pass on tcgen05, then the gradient kernel:
+    bf16 mma.sync products, fp32 accumulation and gradients) and the position table's
+    txl_rel_pos_bwd, timed together and each alone.  The attention backward is reported against the
+    measured bf16 tensor peak."""
     import torch
     B, H, D, L, M, C, dm = 16, 16, 64, 384, 384, 1000, 1024
     dt = torch.bfloat16
@@ -651,7 +652,7 @@ def bench_backward(txl, device, stream, rank, args):
     return {"workload": "backward: B16 H16 D64 d_model1024 L384 M384 clamp1000, bf16 inputs, fp32 gradients",
             "us_per_call": t_us, "us_attn_bwd": t_attn, "us_pos_bwd": t_pos,
             "algorithmic_flops_per_call": f_attn + f_pos, "tflops": (f_attn + f_pos) / (t_us * 1e-6) / 1e12,
-            "roofline": {"kernel": "txl_rel_attn_bwd (bwd_tc_kernel, bf16 mma.sync, + bias reduction)",
+            "roofline": {"kernel": "txl_rel_attn_bwd (attn_persist_kernel log-sum-exp pass + bwd_tc_kernel, bf16 mma.sync, + bias reduction)",
                          "bound": "tensor", "achieved": achieved, "peak": bf16_peak, "unit": "TFLOP/s",
                          "frac": achieved / bf16_peak, "algorithmic_flops_per_launch": f_attn,
                          "peak_source": peak_src + " bf16 burst"}}
