@@ -33,10 +33,12 @@ std::mutex g_sched_mu;
 SchedKey g_sched_key{0, 0, 0, 0};
 std::vector<uint8_t> g_sched_counts;
 
-// Class q costs len0 + q key tiles plus `tau` (tiles) of per-item overhead.
+// Class q costs len0 + q key tiles plus `tau` (tiles) of per-item overhead: an item transition of
+// the persistent kernel (waiting for the item's last P.V, the epilogue, the ring reset) takes about
+// 5 K cycles against about 2.6 K per key tile.
 bool compute(int G, int n_cls, int per_cls, int len0, std::vector<uint8_t>& out)
 {
-    const float tau = 0.5f;
+    const float tau = 1.9f;
     std::vector<float> cost(n_cls);
     for (int q = 0; q < n_cls; ++q) cost[q] = static_cast<float>(len0 + q) + tau;
     std::vector<int> cnt(static_cast<size_t>(G) * n_cls, 0);
