@@ -172,6 +172,14 @@ txl_status txl_rel_attn_decode(int B, int L, int H, int D, int clamp_len,
  * (0 when the shape is outside the decode path). */
 size_t txl_rel_attn_decode_workspace_size(int B, int L, int H, int D, const txl_mem* mem);
 
+/* Which kernels txl_rel_attn_decode (and txl_rel_attn_decode_noalloc) would run for these
+ * arguments: 1 = the fused persistent tcgen05 kernel (L >= 3, see txl_rel_attn_decode), 4 = the
+ * split-key decode kernels and their merge, or a negative txl_status if the arguments are rejected.
+ * Nothing is launched; the workspace is not checked. */
+int txl_rel_attn_decode_path(int B, int L, int H, int D, const txl_view* q, const txl_mem* mem,
+                             const txl_view* k_cur, const txl_view* v_cur, const void* r,
+                             int64_t ld_r, const txl_view* out, txl_dtype dtype);
+
 /*
  * txl_rel_attn_decode_noalloc -- txl_rel_attn_decode without a caller workspace, for callers that
  * cannot obtain device memory at call time.  The pages have no counterpart to this entry point: it
@@ -368,6 +376,14 @@ txl_status txl_rel_attn_table_fwd(int B, int L, int H, int D, int max_len,
                                   const float* u, const float* v_bias,
                                   const void* r_table, int64_t ld_r, const uint8_t* key_mask,
                                   float scale, const txl_view* out, txl_dtype dtype, void* stream);
+
+/* Which kernel txl_rel_attn_table_fwd would run for these arguments: 1 = the persistent tcgen05
+ * kernel (learned-table mode), 3 = the mma.sync tensor-core kernel, 2 = the CUDA-core kernel, or a
+ * negative txl_status if the arguments are rejected.  Nothing is launched. */
+int txl_rel_attn_table_path(int B, int L, int H, int D, int max_len,
+                            const txl_view* q, const txl_view* k, const txl_view* v,
+                            const void* r_table, int64_t ld_r, const uint8_t* key_mask,
+                            const txl_view* out, txl_dtype dtype);
 
 /*
  * Checked build.  libtxl_checked.so is this library compiled with -DTXL_CHECKED (the package builds

@@ -40,6 +40,13 @@ def run_decode(txl, cfg, case, M, valid, wp, C, via_fwd=False):
         mem = txl.Memory(store_k, store_v, wp, valid)
     out = to_dev(torch.full_like(case["q"], float("nan")), cfg.hs)
     u, vb = case["u"].cuda(), case["vb"].cuda()
+    if not via_fwd:
+        # three or more bf16 queries with d_head <= 64 on inputs the fused kernel takes (16-byte rows,
+        # a ring's write pointer and length multiples of 128) go to it; everything else to the
+        # split-key decode kernels
+        fused = (cfg.dtype == "bf16" and L >= 3 and cfg.D <= 64 and
+                 (M == 0 or wp == 0 or (wp % 128 == 0 and M % 128 == 0)))
+        assert txl.rel_attn_decode_path(q, mem, k[:, M:], v[:, M:], r, out) == (1 if fused else 4)
     if via_fwd:
         txl.rel_attn_fwd(q, mem, k[:, M:], v[:, M:], u, vb, r, n_rows, C, out)
     else:

@@ -70,8 +70,18 @@ def test_table_variant_matches_oracle(txl, shape):
     r_dev = torch.zeros(nt, H, ld_r_for(D), dtype=cfg.torch_dtype, device="cuda")
     r_dev[..., :D] = rt.cuda()
     out = to_dev(torch.full_like(q, float("nan")), cfg.hs)
-    txl.rel_attn_table_fwd(to_dev(q, cfg.hs), to_dev(k, cfg.hs), to_dev(v, cfg.hs), u.cuda(), vb.cuda(), r_dev,
-                           max_len, out, key_mask=mask.cuda() if mask is not None else None)
+    qd, kd, vd = to_dev(q, cfg.hs), to_dev(k, cfg.hs), to_dev(v, cfg.hs)
+    md = mask.cuda() if mask is not None else None
+    # the route the host takes: the persistent tcgen05 kernel for bf16, d_head <= 64, L <= max_len and
+    # 16-byte rows; the mma.sync kernel for the other bf16 calls with d_head 64 and 16-byte rows
+    path = txl.rel_attn_table_path(qd, kd, vd, r_dev, max_len, out, key_mask=md)
+    if dtype == "bf16" and D <= 64 and L <= max_len and hs != 68:
+        assert path == 1, path
+    elif dtype == "bf16" and D == 64 and hs == 0:
+        assert path == 3, path
+    else:
+        assert path in (2, 3), path
+    txl.rel_attn_table_fwd(qd, kd, vd, u.cuda(), vb.cuda(), r_dev, max_len, out, key_mask=md)
     torch.cuda.synchronize()
     ref = oracle.table_attn(q, k, v, u, vb, rt, max_len, key_mask=mask.numpy() if mask is not None else None)
     err = np.max(np.abs(out.double().cpu().numpy() - ref))

@@ -11,6 +11,7 @@ from .api import (  # noqa: F401
     mem_push,
     rel_attn_bwd,
     rel_attn_decode,
+    rel_attn_decode_path,
     rel_attn_decode_workspace_size,
     rel_attn_fwd,
     rel_attn_layer,
@@ -19,6 +20,7 @@ from .api import (  # noqa: F401
     rel_attn_layer_fused_workspace_size,
     rel_attn_path,
     rel_attn_table_fwd,
+    rel_attn_table_path,
     rel_pos_bwd,
     rel_pos_gen,
     selftest_wait_timeout,

@@ -173,6 +173,14 @@ def rel_attn_path(q, mem, k_cur, v_cur, r, out) -> int:
                                     dtype_code(q))
 
 
+def rel_attn_decode_path(q, mem, k_cur, v_cur, r, out) -> int:
+    """1 = fused tcgen05 kernel, 4 = split-key decode kernels (txl_rel_attn_decode_path)."""
+    (B, L, H, D), memc, vq, vk, vv, vo = _attn_args(q, mem, k_cur, v_cur, r, out)
+    return _lib().txl_rel_attn_decode_path(B, L, H, D, ctypes.byref(vq), memc, ctypes.byref(vk),
+                                           ctypes.byref(vv), r.data_ptr(), r.stride(1), ctypes.byref(vo),
+                                           dtype_code(q))
+
+
 def mem_push(mem: Memory, k_new: torch.Tensor, v_new: torch.Tensor, stream=None) -> Memory:
     """Append k_new/v_new [B, L, H, D] to the FIFO memory (txl_mem_push)."""
     vk, vv = view(k_new), view(v_new)
@@ -340,6 +348,16 @@ def rel_attn_table_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, u: tor
         _stream(stream))
     check(st, "txl_rel_attn_table_fwd")
     return out
+
+
+def rel_attn_table_path(q, k, v, r_table, max_len: int, out, key_mask=None) -> int:
+    """1 = persistent tcgen05 kernel, 3 = mma.sync tensor-core kernel, 2 = CUDA-core kernel
+    (txl_rel_attn_table_path)."""
+    B, L, H, D = q.shape
+    vq, vk, vv, vo = view(q), view(k), view(v), view(out)
+    return _lib().txl_rel_attn_table_path(
+        B, L, H, D, int(max_len), ctypes.byref(vq), ctypes.byref(vk), ctypes.byref(vv), r_table.data_ptr(),
+        r_table.stride(1), key_mask.data_ptr() if key_mask is not None else None, ctypes.byref(vo), dtype_code(q))
 
 
 def selftest_wait_timeout(err_flag: torch.Tensor, timeout_us: int, stream=None) -> None:

@@ -326,7 +326,7 @@ txl_status attn_tc_launch(int B, int L, int H, int D, int clamp_len, const txl_v
 // The learned-table variant on the persistent tcgen05 kernel (table mode, with or without a key
 // mask): bf16, d_head <= 64, L <= max_len (so no pair's index i - j + max_len - 1 leaves the table and
 // no clamp applies), 16-byte aligned bases and strides for q, k, v and the table.
-bool table_tc_eligible(int B, int L, int H, int D, int max_len, const txl_view* q, const txl_view* k,
+bool table_persist_eligible(int B, int L, int H, int D, int max_len, const txl_view* q, const txl_view* k,
                        const txl_view* v, const void* r_table, int64_t ld_r, const uint8_t* key_mask,
                        txl_dtype dtype)
 {
@@ -874,22 +874,25 @@ txl_status txl_rel_pos_bwd(int n_rows, int d_model, int n_head, int d_head, cons
     return launch_pos_bwd(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? TXL_OK : TXL_ERR_CUDA;
 }
 
-txl_status txl_rel_attn_table_fwd(int B, int L, int H, int D, int max_len, const txl_view* q, const txl_view* k,
-                                  const txl_view* v, const float* u, const float* v_bias, const void* r_table,
-                                  int64_t ld_r, const uint8_t* key_mask, float scale, const txl_view* out,
-                                  txl_dtype dtype, void* stream)
+namespace {
+
+// Argument checks of txl_rel_attn_table_fwd / txl_rel_attn_table_path.
+txl_status check_table(int B, int L, int H, int D, int max_len, const txl_view* q, const txl_view* k,
+                       const txl_view* v, const void* r_table, int64_t ld_r, const txl_view* out, txl_dtype dtype)
 {
     if (B < 0 || L < 0 || H <= 0 || D <= 0 || max_len < 1) return TXL_ERR_INVALID_ARG;
     if (D > 128) return TXL_ERR_UNSUPPORTED;
     if (dtype != TXL_F32 && dtype != TXL_BF16) return TXL_ERR_INVALID_ARG;
-    if (!view_ok(q) || !view_ok(k) || !view_ok(v) || !view_ok(out) || !u || !v_bias || !r_table || ld_r < D)
+    if (!view_ok(q) || !view_ok(k) || !view_ok(v) || !view_ok(out) || !r_table || ld_r < D)
         return TXL_ERR_INVALID_ARG;
     if (static_cast<int64_t>(max_len) * 2 - 1 > INT32_MAX) return TXL_ERR_INVALID_ARG;
-    if (B == 0 || L == 0) return TXL_OK;
-    if (scale <= 0.f) scale = 1.0f / std::sqrt(static_cast<float>(D));
-    if (table_tc_eligible(B, L, H, D, max_len, q, k, v, r_table, ld_r, key_mask, dtype))
-        return table_tc_launch(B, L, H, D, max_len, q, k, v, u, v_bias, r_table, ld_r, key_mask, scale, out,
-                               static_cast<cudaStream_t>(stream));
+    return TXL_OK;
+}
+
+TableParams table_params(int B, int L, int H, int D, int max_len, const txl_view* q, const txl_view* k,
+                         const txl_view* v, const float* u, const float* v_bias, const void* r_table, int64_t ld_r,
+                         const uint8_t* key_mask, float scale, const txl_view* out)
+{
     TableParams p;
     std::memset(&p, 0, sizeof(p));
     p.q = q->ptr; p.q_sb = q->stride_b; p.q_st = q->stride_t; p.q_sh = q->stride_h;
@@ -901,7 +904,48 @@ txl_status txl_rel_attn_table_fwd(int B, int L, int H, int D, int max_len, const
     p.mask = key_mask;
     p.B = B; p.L = L; p.H = H; p.D = D; p.max_len = max_len;
     p.scale = scale;
+    return p;
+}
+
+}  // namespace
+
+txl_status txl_rel_attn_table_fwd(int B, int L, int H, int D, int max_len, const txl_view* q, const txl_view* k,
+                                  const txl_view* v, const float* u, const float* v_bias, const void* r_table,
+                                  int64_t ld_r, const uint8_t* key_mask, float scale, const txl_view* out,
+                                  txl_dtype dtype, void* stream)
+{
+    const txl_status st = check_table(B, L, H, D, max_len, q, k, v, r_table, ld_r, out, dtype);
+    if (st != TXL_OK) return st;
+    if (!u || !v_bias) return TXL_ERR_INVALID_ARG;
+    if (B == 0 || L == 0) return TXL_OK;
+    if (scale <= 0.f) scale = 1.0f / std::sqrt(static_cast<float>(D));
+    if (table_persist_eligible(B, L, H, D, max_len, q, k, v, r_table, ld_r, key_mask, dtype))
+        return table_tc_launch(B, L, H, D, max_len, q, k, v, u, v_bias, r_table, ld_r, key_mask, scale, out,
+                               static_cast<cudaStream_t>(stream));
+    const TableParams p = table_params(B, L, H, D, max_len, q, k, v, u, v_bias, r_table, ld_r, key_mask, scale, out);
     return launch_table_attn(p, dtype, static_cast<cudaStream_t>(stream)) == cudaSuccess ? TXL_OK : TXL_ERR_CUDA;
+}
+
+int txl_rel_attn_table_path(int B, int L, int H, int D, int max_len, const txl_view* q, const txl_view* k,
+                            const txl_view* v, const void* r_table, int64_t ld_r, const uint8_t* key_mask,
+                            const txl_view* out, txl_dtype dtype)
+{
+    const txl_status st = check_table(B, L, H, D, max_len, q, k, v, r_table, ld_r, out, dtype);
+    if (st != TXL_OK) return -static_cast<int>(st);
+    if (table_persist_eligible(B, L, H, D, max_len, q, k, v, r_table, ld_r, key_mask, dtype)) return 1;
+    const TableParams p = table_params(B, L, H, D, max_len, q, k, v, nullptr, nullptr, r_table, ld_r, key_mask, 1.f,
+                                       out);
+    return table_tc_eligible(p, dtype) ? 3 : 2;
+}
+
+int txl_rel_attn_decode_path(int B, int L, int H, int D, const txl_view* q, const txl_mem* mem,
+                             const txl_view* k_cur, const txl_view* v_cur, const void* r, int64_t ld_r,
+                             const txl_view* out, txl_dtype dtype)
+{
+    const txl_status st = check_attn(B, L, H, D, q, mem, k_cur, v_cur, r, ld_r, out, dtype);
+    if (st != TXL_OK) return -static_cast<int>(st);
+    if (L > kDecodeMaxL) return -static_cast<int>(TXL_ERR_UNSUPPORTED);
+    return decode_takes_fused(B, L, H, D, q, mem, k_cur, v_cur, r, ld_r, dtype) ? 1 : 4;
 }
 
 int txl_checked_build(void) { return kCheckedBuild ? 1 : 0; }

@@ -26,6 +26,7 @@ EXPORTS = (
     "txl_rel_attn_layer_fused", "txl_rel_attn_layer_fused_workspace_size",
     "txl_checked_build", "txl_range_errors", "txl_range_errors_clear", "txl_selftest_range_check",
     "txl_rel_attn_bwd", "txl_rel_attn_bwd_workspace_size", "txl_rel_pos_bwd", "txl_rel_attn_table_fwd",
+    "txl_rel_attn_table_path", "txl_rel_attn_decode_path",
 )
 
 
@@ -117,6 +118,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.txl_rel_pos_bwd.restype = i
     lib.txl_rel_attn_table_fwd.argtypes = [i, i, i, i, i, V, V, V, vp, vp, vp, i64, vp, fp, V, i, vp]
     lib.txl_rel_attn_table_fwd.restype = i
+    lib.txl_rel_attn_table_path.argtypes = [i, i, i, i, i, V, V, V, vp, i64, vp, V, i]
+    lib.txl_rel_attn_table_path.restype = i
+    lib.txl_rel_attn_decode_path.argtypes = [i, i, i, i, V, Mp, V, V, vp, i64, V, i]
+    lib.txl_rel_attn_decode_path.restype = i
     _lib = lib
     return lib
 
