@@ -1,5 +1,8 @@
 // txl_attn_tc.cu -- fused relative attention for sm_103a: TMA tiles, tcgen05 UMMA with TMEM
 // accumulators, the relative shift as an index remap, online softmax, P.V on tensor cores.
+// It serves 64 < d_head <= 128 (two 64-column atoms per row); d_head <= 64 takes the persistent
+// kernel of txl_attn_persist.cu, and the one-atom branches below are kept only as that template
+// parameter's other value (not instantiated).
 //
 // Per CTA: one tile of 128 queries of one (batch, head).  Score of query i and key j
 // ("跨窗口的相对位置编码" §3, "Transformer-XL 和相对位置编码" §2.3.2 terms (a)-(d)):
@@ -658,10 +661,13 @@ cudaError_t launch_na(const AttnTcParams& p, cudaStream_t s)
 
 }  // namespace
 
+// 64 < d_head <= 128 (two 64-column atoms).  d_head <= 64 takes the persistent kernel
+// (txl_attn_persist.cu); the one-atom form of this kernel is not instantiated.
 cudaError_t launch_attn_tc(const AttnTcParams& p, cudaStream_t s)
 {
     if (p.B == 0 || p.L == 0 || p.H == 0) return cudaSuccess;
-    return p.n_atoms == 1 ? launch_na<1>(p, s) : launch_na<2>(p, s);
+    if (p.n_atoms != 2) return cudaErrorInvalidValue;
+    return launch_na<2>(p, s);
 }
 
 }  // namespace txl
