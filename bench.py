@@ -984,7 +984,7 @@ def run_txl(args):
 def profile_leg(args):
     """A few calls of one workload's kernels and nothing else, for a profiler to capture:
     large / base / longmem (the fused attention), stream (8 segments: attention + push), layer (the
-    fused layer step), decode, table (the learned-table variant).  Prints the per-call device time of the last repetition."""
+    fused layer step), decode, table (the learned-table variant), backward.  Prints the per-call device time of the last repetition."""
     import torch
     import transformer_xl_relative_gb300 as txl
     device = torch.device("cuda", 0)
@@ -997,6 +997,8 @@ def profile_leg(args):
         res = bench_decode(txl, device, stream, 0, args)
     elif args.profile_leg == "table":
         res = bench_table(txl, device, stream, 0, args)
+    elif args.profile_leg == "backward":
+        res = bench_backward(txl, device, stream, 0, args)
     else:
         import txl_inputs
         cfg = txl_inputs.CONFIGS["large"]
@@ -1026,7 +1028,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=40)
     ap.add_argument("--impl", choices=["txl", "reference"], default="txl")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile-leg", choices=["large", "base", "longmem", "stream", "layer", "decode", "table"],
+    ap.add_argument("--profile-leg", choices=["large", "base", "longmem", "stream", "layer", "decode", "table",
+                                              "backward"],
                     help="run only a few calls of this workload (for a profiler) and exit")
     args = ap.parse_args(argv)
     world = os.environ.get("WORLD_SIZE")
