@@ -107,3 +107,16 @@ def test_decode_rejects_without_workspace(txl):
     with pytest.raises(txl.TxlError):
         txl.rel_attn_decode(q, mem, case["k"][:, 300:].cuda(), case["v"][:, 300:].cuda(),
                             case["u"].cuda(), case["vb"].cuda(), r, 301, 1000, out, workspace=tiny)
+
+
+def test_decode_full_workload_several_queries(txl):
+    """The decode workload's full size (B8 H16 D64, a 4096-key memory, clamp 1000) with four new
+    queries per (b, h): the fused kernel's route, sampled rows against the oracle."""
+    B, H, D, L, M, C = 8, 16, 64, 4, 4096, 1000
+    cfg = txl_inputs.custom(B=B, H=H, D=D, d_model=1024, L=L, M=M, clamp_len=C, dtype="bf16", seed=4444)
+    case = txl_inputs.make_case(cfg)
+    out = run_decode(txl, cfg, case, M, M, 0, C)
+    rows = [(b, h, i) for b in (0, 5, 7) for h in (0, 9, 15) for i in range(L)]
+    ref = oracle.rel_attn(case["q"], case["k"], case["v"], case["u"], case["vb"],
+                          case["W_R"][:, : H * D], M, M, C, rows=rows)
+    assert max_err(out, ref, rows=rows) <= TOL["bf16"]

@@ -123,3 +123,28 @@ def test_table_large_workload_sampled(txl):
         ref = oracle.table_attn(q[sl], k[sl], v[sl], u[h:h + 1], vb[h:h + 1], rt[:, h:h + 1], max_len)
         err = np.max(np.abs(out[sl].double().cpu().numpy() - ref))
         assert err <= TOL["bf16"], (b, h, err)
+
+
+def test_table_large_workload_masked_sampled(txl):
+    """The same full-size workload with a random key mask (a quarter of the keys masked, batch entry
+    3 fully masked): the persistent kernel's masked instantiation, sampled (b, h) slices."""
+    B, H, D, L, max_len = 16, 16, 64, 384, 512
+    cfg = txl_inputs.custom(B=B, H=H, D=D, d_model=2 * D, L=L, M=0, dtype="bf16", seed=6161)
+    q, k, v = txl_inputs.make_qkv(cfg, seed=6162, L=L, T=L)
+    u, vb, _ = txl_inputs.make_params(cfg, seed=6163)
+    nt = 2 * max_len - 1
+    rt = txl_inputs.make_matrix(nt, H * D, seed=6164, dtype=torch.bfloat16).reshape(nt, H, D)
+    gen = torch.Generator().manual_seed(6165)
+    mask = (torch.rand(B, L, generator=gen) > 0.25).to(torch.uint8)
+    mask[3] = 0
+    out = torch.empty_like(q).cuda()
+    qd, kd, vd, rd, md = q.cuda(), k.cuda(), v.cuda(), rt.cuda(), mask.cuda()
+    assert txl.rel_attn_table_path(qd, kd, vd, rd, max_len, out, key_mask=md) == 1
+    txl.rel_attn_table_fwd(qd, kd, vd, u.cuda(), vb.cuda(), rd, max_len, out, key_mask=md)
+    torch.cuda.synchronize()
+    for b, h in [(0, 0), (3, 7), (15, 15)]:
+        sl = (slice(b, b + 1), slice(None), slice(h, h + 1))
+        ref = oracle.table_attn(q[sl], k[sl], v[sl], u[h:h + 1], vb[h:h + 1], rt[:, h:h + 1], max_len,
+                                key_mask=mask[b:b + 1].numpy())
+        err = np.max(np.abs(out[sl].double().cpu().numpy() - ref))
+        assert err <= TOL["bf16"], (b, h, err)
