@@ -88,6 +88,46 @@ def test_path_selection(native):
     assert _path(native, wp=128, valid=128) == -native.TXL_ERR_INVALID_ARG   # wp >= M
 
 
+def _table_path(native, B=2, L=300, H=4, D=64, max_len=512, dtype=1, sh=None, masked=False, ld_r=64):
+    sh = sh or D
+    V = native.TxlView
+    x = V(FAKE, L * H * sh, H * sh, sh)
+    return native.load().txl_rel_attn_table_path(B, L, H, D, max_len, ctypes.byref(x), ctypes.byref(x),
+                                                 ctypes.byref(x), FAKE, ld_r, FAKE if masked else None,
+                                                 ctypes.byref(x), dtype)
+
+
+def test_table_path_selection(native):
+    assert _table_path(native) == 1                               # bf16, L <= max_len: persistent tcgen05
+    assert _table_path(native, masked=True) == 1                  # a key mask too
+    assert _table_path(native, D=41, sh=48, ld_r=48) == 1         # padded heads, d_head <= 64
+    assert _table_path(native, L=600) == 3                        # L > max_len: the mma.sync kernel
+    assert _table_path(native, L=600, D=32, ld_r=32) == 2         # ... which wants d_head 64
+    assert _table_path(native, dtype=0) == 2                      # fp32: CUDA cores
+    assert _table_path(native, D=128, ld_r=128) == 2              # d_head above 64
+    assert _table_path(native, D=130, ld_r=136) == -native.TXL_ERR_UNSUPPORTED
+    assert _table_path(native, max_len=0) == -native.TXL_ERR_INVALID_ARG
+
+
+def _decode_path(native, L=4, M=1024, wp=0, D=64, dtype=1):
+    B, H = 2, 4
+    V = native.TxlView
+    q = V(FAKE, L * H * D, H * D, D)
+    kc = V(FAKE, (M + L) * H * D, H * D, D)
+    mem = native.TxlMem(FAKE, FAKE, (M + L) * H * D, H * D, D, B, M, H, D, dtype, wp, M)
+    return native.load().txl_rel_attn_decode_path(B, L, H, D, ctypes.byref(q), ctypes.byref(mem), ctypes.byref(kc),
+                                                  ctypes.byref(kc), FAKE, D, ctypes.byref(q), dtype)
+
+
+def test_decode_path_selection(native):
+    assert _decode_path(native) == 1                  # three or more queries: the fused kernel
+    assert _decode_path(native, L=2) == 4             # one or two: the split-key decode kernels
+    assert _decode_path(native, wp=100) == 4          # ring not aligned to 128
+    assert _decode_path(native, dtype=0) == 4         # fp32
+    assert _decode_path(native, D=128) == 4           # d_head above 64
+    assert _decode_path(native, L=17) == -native.TXL_ERR_UNSUPPORTED
+
+
 def test_rejections_before_any_launch(native):
     lib = native.load()
     V = native.TxlView
