@@ -1,0 +1,603 @@
+// txl_bwd_umma.cu -- gradients of the relative attention on the 5th-generation tensor cores
+// (bf16, d_head = 64): every product a tcgen05 MMA with its fp32 accumulator in tensor memory.
+//
+// The gradients are those of txl_bwd_tc.cu: the chain rule through the four-term score of
+// "Transformer-XL 和相对位置编码" §2.3.2 and the softmax, the memory's keys and values being the
+// stop-gradient part of §2.3.1.  With the forward kernel's row log-sum-exp L2_i (log2 domain) and
+// its query forms Qc' = bf16(c (q + u)), Qc'' = bf16(c (q + v_bias)), c = scale log2 e:
+//   s_ij = Qc'_i . k_j + Qc''_i . r[delta_ij],   P_ij = 2^(s_ij - L2_i),
+//   dS_ij = P_ij (dO_i . v_j - dO_i . out_i),
+//   dq_i = scale sum_j dS_ij (k_j + r[delta_ij]),   dk_j = ln 2 sum_i dS_ij Qc'_i,
+//   dv_j = sum_i P_ij dO_i,   dr[delta] = ln 2 sum_{delta_ij = delta} dS_ij Qc''_i,
+// delta_ij = min(M + i - j, clamp_len).
+//
+// One launch holds two kinds of CTA, each on 128 rows of one (b, h):
+//  * a query CTA owns a query tile and sweeps the key tiles of 128 its queries see, newest
+//    first (tile t starts at key M + i0 - 128 t, so its distances are 128 t + i - j with i, j
+//    local, window column c = i - j + 127 in [0, 255) over position rows 128 t - 127 + c).  It
+//    accumulates dq_ac = dS K and dq_bd = G R_win in TMEM over the sweep, where G, dS scattered
+//    by distance (G[i][i - j + 127] = dS_ij), sits in shared memory as the A operand of that
+//    product and, read transposed, of dr_win = G^T Qc''.  The window's lower 128 rows are the
+//    upper 128 of the tile before, so every block of 128 distance rows receives the products of
+//    two consecutive tiles and is added to dr (fp32 atomics) once.
+//  * a key CTA owns a key tile of the current segment and sweeps the query tiles that see it,
+//    with dv += P^T dO and dk += dS^T Qc' accumulated in TMEM (P and dS in shared memory, read
+//    transposed): every key has one owner, so dk and dv are written once, without atomics.
+// Both recompute, per (query tile, key tile), S = Qc' K^T, the window products W = Qc'' R_win^T
+// (both 128-row halves), P and dP = dO V^T.  W reaches each row's positions through a shared-
+// memory stage (the relative shift as a per-row index remap, bf16 like the forward's ring), so
+// the scores are the forward kernel's and L2_i belongs to them.
+// Pairs whose distance reaches clamp_len share r[clamp_len]; their dS nearly cancel, so they stay
+// out of the bf16 G and enter dq_i as c_i r[clamp_len] and dr[clamp_len] as ln 2 sum_i c_i Qc''_i
+// with c_i their fp32 sum per row.
+//
+// 256 threads: thread (li, hf) serves TMEM lane / tile row li and the column half hf of every
+// 128-column product; thread 0 issues the MMAs.  Steps run in phases separated by CTA barriers
+// and one mbarrier that each group of MMAs commits to; every wait is bounded (2 s).
+#include <cuda_bf16.h>
+
+#include "txl_internal.h"
+#include "txl_ptx.cuh"
+#include "txl_mma.cuh"
+
+namespace txl {
+
+namespace {
+
+constexpr int kUThreads = 256;
+constexpr int kTileBytes = 16384;                  // 128 rows x 128 B, one 128-byte swizzle atom wide
+constexpr int kStagePitch = 84;                    // 32-bit words per stage row (80 used)
+constexpr float kLn2u = 0.693147180559945309f;
+constexpr uint64_t kUWaitNs = 2000000000ull;
+
+// TMEM columns.  Query CTA: S, then dr_win (lower block in 0..63, upper in 64..127); W over
+// 128..383, then dP in 128..255 and dS (bf16 pairs) in 256..319; dq_ac, dq_bd.  Key CTA: S; W,
+// then dP; dv, dk.
+constexpr uint32_t kColS = 0, kColW = 128, kColDP = 128, kColDS = 256, kColA0 = 384, kColA1 = 448;
+
+struct USmem {
+    static constexpr int QU = 0;                           // [128][64] Qc'  (query rows)
+    static constexpr int QV = QU + kTileBytes;             // [128][64] Qc''
+    static constexpr int GO = QV + kTileBytes;             // [128][64] dO
+    static constexpr int K = GO + kTileBytes;              // [128][64] key tile
+    static constexpr int V = K + kTileBytes;               // [128][64] value tile
+    static constexpr int R = V + kTileBytes;               // two [128][64] blocks of position rows
+    static constexpr int X = R + 2 * kTileBytes;           // query CTA: G, 4 atoms [128][64];
+                                                           // key CTA: P, 2 atoms, then dS, 2 atoms
+    static constexpr int ST = X + 4 * kTileBytes;          // W stage: [128][kStagePitch] words
+    static constexpr int Bar = ST + 128 * kStagePitch * 4;
+    static constexpr int Misc = Bar + 8;                   // TMEM base, abort flag
+    static constexpr int Csum = Misc + 16;                 // float [2][128]
+    static constexpr int Size = Csum + 2 * 128 * 4;
+};
+static_assert(USmem::Size <= 232448, "shared memory per CTA");
+
+// Key j of (b, h): memory ring slot for lo <= j < M, current segment for M <= j < M + L, else
+// null (zero-filled: such keys are masked, and zeros keep their products finite).
+__device__ __forceinline__ void kv_rows(const AttnSimtParams& a, int b, int h, int j, const __nv_bfloat16*& kp,
+                                        const __nv_bfloat16*& vp)
+{
+    kp = vp = nullptr;
+    if (j < a.lo || j >= a.M + a.L) return;
+    if (j < a.M) {
+        int slot = a.wp + j;
+        if (slot >= a.M) slot -= a.M;
+        const int64_t off = b * a.m_sb + static_cast<int64_t>(slot) * a.m_st + h * a.m_sh;
+        kp = static_cast<const __nv_bfloat16*>(a.kmem) + off;
+        vp = static_cast<const __nv_bfloat16*>(a.vmem) + off;
+    } else {
+        const int t = j - a.M;
+        kp = static_cast<const __nv_bfloat16*>(a.kcur) + b * a.kc_sb + static_cast<int64_t>(t) * a.kc_st + h * a.kc_sh;
+        vp = static_cast<const __nv_bfloat16*>(a.vcur) + b * a.vc_sb + static_cast<int64_t>(t) * a.vc_st + h * a.vc_sh;
+    }
+}
+
+// Keys j0 .. j0 + 127 into the K and V tiles (128-byte swizzled rows, the K-major layout of the
+// MMA descriptors).
+__device__ __forceinline__ void load_keys(const AttnSimtParams& a, uint8_t* sm, int b, int h, int j0, int tid)
+{
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+        const int id = tid + kUThreads * x;
+        const int row = id >> 3, ch = id & 7;
+        const __nv_bfloat16 *kp, *vp;
+        kv_rows(a, b, h, j0 + row, kp, vp);
+        const uint32_t nb = kp ? 16u : 0u;
+        mma::cp_async16(sm + USmem::K + mma::swz64(row, 8 * ch), kp ? static_cast<const void*>(kp + 8 * ch) : a.r, nb);
+        mma::cp_async16(sm + USmem::V + mma::swz64(row, 8 * ch), vp ? static_cast<const void*>(vp + 8 * ch) : a.r, nb);
+    }
+}
+
+// Position block beta (distances 128 beta - 127 + x, x = 0 .. 127, clamped into [0, min(C,
+// n_rows - 1)]: rows below 0 pair only with masked keys, rows past clamp_len repeat r[clamp_len])
+// into R slot beta mod 2.
+__device__ __forceinline__ void load_rblock(const BwdParams& p, uint8_t* sm, int h, int beta, int tid)
+{
+    const AttnSimtParams& a = p.a;
+    const int rmax = min(a.C, p.n_rows - 1);
+    uint8_t* dst = sm + USmem::R + (beta & 1) * kTileBytes;
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+        const int id = tid + kUThreads * x;
+        const int row = id >> 3, ch = id & 7;
+        const int rr = min(max(128 * beta - 127 + row, 0), rmax);
+        mma::cp_async16(dst + mma::swz64(row, 8 * ch),
+                        static_cast<const __nv_bfloat16*>(a.r) + static_cast<int64_t>(rr) * a.r_row + h * a.r_head +
+                            8 * ch,
+                        16u);
+    }
+}
+
+// Qc', Qc'' and dO of query rows i0 .. i0 + 127 (zero past L).  The query forms are rounded as
+// the forward kernel rounds them: one fma of q with c and the product c u (c v_bias).
+__device__ __forceinline__ void load_queries(const BwdParams& p, uint8_t* sm, int b, int h, int i0, float c, int tid)
+{
+    const AttnSimtParams& a = p.a;
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+        const int id = tid + kUThreads * x;
+        const int row = id >> 3, ch = id & 7;
+        const int i = i0 + row;
+        uint4 wu = make_uint4(0, 0, 0, 0), wv = wu, wg = wu;
+        if (i < a.L) {
+            const uint4 qq = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) + b * a.q_sb +
+                                                                  static_cast<int64_t>(i) * a.q_st + h * a.q_sh) + ch);
+            wg = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.dout) + b * p.g_sb +
+                                                      static_cast<int64_t>(i) * p.g_st + h * p.g_sh) + ch);
+            const uint32_t qw[4] = {qq.x, qq.y, qq.z, qq.w};
+            uint32_t ou[4], ov[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int d = 8 * ch + 2 * e;
+                const float x0 = mma::bf16_lo(qw[e]), x1 = mma::bf16_hi(qw[e]);
+                ou[e] = pack_bf16x2(fmaf(x0, c, __ldg(a.u + h * 64 + d) * c), fmaf(x1, c, __ldg(a.u + h * 64 + d + 1) * c));
+                ov[e] = pack_bf16x2(fmaf(x0, c, __ldg(a.vb + h * 64 + d) * c),
+                                    fmaf(x1, c, __ldg(a.vb + h * 64 + d + 1) * c));
+            }
+            wu = make_uint4(ou[0], ou[1], ou[2], ou[3]);
+            wv = make_uint4(ov[0], ov[1], ov[2], ov[3]);
+        }
+        *reinterpret_cast<uint4*>(sm + USmem::QU + mma::swz64(row, 8 * ch)) = wu;
+        *reinterpret_cast<uint4*>(sm + USmem::QV + mma::swz64(row, 8 * ch)) = wv;
+        *reinterpret_cast<uint4*>(sm + USmem::GO + mma::swz64(row, 8 * ch)) = wg;
+    }
+}
+
+// D_i = dO_i . out_i and the log-sum-exp of query row i (zero past L).
+__device__ __forceinline__ void row_stats(const BwdParams& p, int b, int h, int i, float& dd, float& l2)
+{
+    const AttnSimtParams& a = p.a;
+    dd = 0.f;
+    l2 = 0.f;
+    if (i >= a.L) return;
+    const uint4* go = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.dout) + b * p.g_sb +
+                                                     static_cast<int64_t>(i) * p.g_st + h * p.g_sh);
+    const uint4* oo = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.out) + b * a.o_sb +
+                                                     static_cast<int64_t>(i) * a.o_st + h * a.o_sh);
+    float acc = 0.f;
+#pragma unroll
+    for (int x = 0; x < 8; ++x) {
+        const uint4 g = __ldg(go + x), o = __ldg(oo + x);
+        const uint32_t gw[4] = {g.x, g.y, g.z, g.w}, ow[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            acc = fmaf(mma::bf16_lo(gw[e]), mma::bf16_lo(ow[e]), acc);
+            acc = fmaf(mma::bf16_hi(gw[e]), mma::bf16_hi(ow[e]), acc);
+        }
+    }
+    dd = acc;
+    l2 = p.lse[(static_cast<int64_t>(b) * a.L + i) * a.H + h];
+}
+
+// Byte offset of G[li][c] (window column c of query row li): four K-major swizzle atoms of 64
+// columns.
+__device__ __forceinline__ uint32_t g_off(int li, int c)
+{
+    return static_cast<uint32_t>((c >> 6) * kTileBytes + li * 128 + (((((c >> 3) & 7) ^ li) & 7) << 4) + ((c & 7) << 1));
+}
+
+__global__ void __launch_bounds__(kUThreads, 1) bwd_umma_kernel(const __grid_constant__ BwdParams p)
+{
+    extern __shared__ __align__(1024) uint8_t sm[];
+    const AttnSimtParams& a = p.a;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int li = tid & 127, hf = tid >> 7;
+    if ((smem_u32(sm) & 1023u) != 0) {
+        if (tid == 0 && p.err_flag) atomicCAS(p.err_flag, 0, TXL_ERR_ALIGNMENT);
+        return;
+    }
+    const int h = blockIdx.x, b = blockIdx.y;
+    const int n_qt = (a.L + 127) / 128;
+    // work classes, longest first: query tiles from the last, then key tiles from the first
+    const bool key_cta = static_cast<int>(blockIdx.z) >= n_qt;
+    const int own = key_cta ? static_cast<int>(blockIdx.z) - n_qt : n_qt - 1 - static_cast<int>(blockIdx.z);
+    const int M = a.M, L = a.L, C = a.C;
+    const float c = a.scale * 1.4426950408889634f;
+
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + USmem::Bar);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm + USmem::Misc);
+    int* abort_flag = reinterpret_cast<int*>(sm + USmem::Misc + 4);
+    float* csum_s = reinterpret_cast<float*>(sm + USmem::Csum);
+    uint32_t* srow = reinterpret_cast<uint32_t*>(sm + USmem::ST) + li * kStagePitch;
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(tmem_holder, 512);
+
+    // sweep geometry: step s pairs query tile i0 with the key tile starting at j0 = M + i0 - 128 s
+    const int n_steps = key_cta ? n_qt - own : (M + 128 * own + 127 - a.lo) / 128 + 1;
+    int i0 = 128 * own;                                    // key CTA: the first query tile = own
+    const int jk = M + 128 * own;                          // key CTA: its key tile
+
+    load_queries(p, sm, b, h, i0, c, tid);
+    if (!key_cta) {
+        // G outside each row's band [li, li + 127] stays zero for the whole sweep
+        uint4* g = reinterpret_cast<uint4*>(sm + USmem::X);
+#pragma unroll
+        for (int x = 0; x < 16; ++x) g[tid + kUThreads * x] = make_uint4(0, 0, 0, 0);
+    }
+    load_keys(a, sm, b, h, key_cta ? jk : M + i0, tid);
+    load_rblock(p, sm, h, 0, tid);
+    load_rblock(p, sm, h, 1, tid);
+    mma::cp_async_commit();
+    float dd, l2;
+    row_stats(p, b, h, i0 + li, dd, l2);
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const WaitCtl wc{abort_flag, p.err_flag, kUWaitNs};
+    const int sh = lane & 1;                              // stage position parity of this row
+    const int wq = warp & 3;
+
+    constexpr uint32_t id_nn = idesc_bf16(128, 128, 0, 0);   // K-major A and B
+    constexpr uint32_t id_kn = idesc_bf16(128, 64, 0, 1);    // A K-major (or TMEM), B MN-major
+    constexpr uint32_t id_mm = idesc_bf16(128, 64, 1, 1);    // A and B MN-major
+    const uint32_t s_qu = smem_u32(sm + USmem::QU), s_qv = smem_u32(sm + USmem::QV), s_go = smem_u32(sm + USmem::GO);
+    const uint32_t s_k = smem_u32(sm + USmem::K), s_v = smem_u32(sm + USmem::V), s_r = smem_u32(sm + USmem::R);
+    const uint32_t s_x = smem_u32(sm + USmem::X);
+
+    uint32_t mph = 0;
+    bool ok = true;
+    float csum = 0.f;                                     // fp32 dS of this thread's pairs at or past clamp_len
+    float carry[32];                                      // upper-block dr_win of the previous tile
+#pragma unroll
+    for (int e = 0; e < 32; ++e) carry[e] = 0.f;
+
+    for (int t = 0; t < n_steps; ++t) {
+        const int j0 = key_cta ? jk : M + i0 - 128 * t;
+        const int ra = t & 1, rb = (t + 1) & 1;           // R slots of the window's lower, upper block
+        mma::cp_async_wait_all();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        // ---- S = Qc' K^T, W = Qc'' R_win^T (two halves of 128 window rows)
+        if (tid == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint32_t acc = kk > 0 ? 1u : 0u;
+                umma_ss(tmem + kColS, sdesc_k_sw128(s_qu) + 2 * kk, sdesc_k_sw128(s_k) + 2 * kk, id_nn, acc);
+                umma_ss(tmem + kColW, sdesc_k_sw128(s_qv) + 2 * kk, sdesc_k_sw128(s_r + ra * kTileBytes) + 2 * kk, id_nn,
+                        acc);
+                umma_ss(tmem + kColW + 128, sdesc_k_sw128(s_qv) + 2 * kk, sdesc_k_sw128(s_r + rb * kTileBytes) + 2 * kk,
+                        id_nn, acc);
+            }
+            umma_commit(bar);
+        }
+        ok = mbar_wait(bar, mph & 1, wc, 1) && ok;
+        ++mph;
+        tc_fence_after();
+        // ---- W to the stage: row li keeps window columns [32 wq, 32 wq + 160) (every column its
+        //      rows read) at position c - 32 wq + sh, two bf16 per word, the even position in the
+        //      low half; half 0 writes columns 0 .. 95 of the span, half 1 the rest
+        {
+            float prev = 0.f;                             // column 32 q - 1 of the span
+            if (hf == 1) {
+                uint32_t v0;
+                tmem_ld1(tmem + lane_base + kColW + 32 * wq + 95, v0);
+                tmem_ld_wait();
+                prev = __uint_as_float(v0);
+            }
+            const int q0 = hf ? 3 : 0, nq = hf ? 2 : 3;
+#pragma unroll 1
+            for (int qi = 0; qi < nq; ++qi) {
+                const int q = q0 + qi;
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_base + kColW + 32 * wq + 32 * q, v);
+                tmem_ld_wait();
+                uint32_t w[16];
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const float lo = sh ? (k == 0 ? prev : __uint_as_float(v[2 * k - 1])) : __uint_as_float(v[2 * k]);
+                    const float hi = sh ? __uint_as_float(v[2 * k]) : __uint_as_float(v[2 * k + 1]);
+                    w[k] = pack_bf16x2(lo, hi);
+                }
+                prev = __uint_as_float(v[31]);
+                uint4* dst = reinterpret_cast<uint4*>(srow + 16 * q);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) dst[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+        // ---- dP = dO V^T (into W's lower half, read above)
+        if (tid == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                umma_ss(tmem + kColDP, sdesc_k_sw128(s_go) + 2 * kk, sdesc_k_sw128(s_v) + 2 * kk, id_nn,
+                        kk > 0 ? 1u : 0u);
+            umma_commit(bar);
+        }
+        // ---- P of this thread's 64 keys jl = 64 hf + k: s = S + BD, BD[k] = W[li][li + 127 - jl]
+        //      from stage word (lane + sh)/2 + 63 - 32 hf - m (hi half: k = 2m, lo half: k = 2m + 1)
+        float pv[64];
+        {
+            uint32_t sv[64];
+            tmem_ld64(tmem + lane_base + kColS + 64 * hf, sv);
+            tmem_ld_wait();
+            const int i = i0 + li;
+            const int jb = j0 + 64 * hf;
+            // visible keys: lo <= j <= M + i, j < M + L (none past L)
+            const int klo = max(a.lo - jb, 0);
+            const int khi = i < L ? min(min(M + i, M + L - 1) - jb, 63) : -1;
+            const int wb = ((lane + sh) >> 1) + 63 - 32 * hf;
+#pragma unroll
+            for (int m = 0; m < 32; ++m) {
+                const uint32_t w = srow[wb - m];
+                const float x0 = add_bf16hi_f32(w, __uint_as_float(sv[2 * m]));
+                const float x1 = add_bf16lo_f32(w, __uint_as_float(sv[2 * m + 1]));
+                pv[2 * m] = (2 * m >= klo && 2 * m <= khi) ? ex2_approx(x0 - l2) : 0.f;
+                pv[2 * m + 1] = (2 * m + 1 >= klo && 2 * m + 1 <= khi) ? ex2_approx(x1 - l2) : 0.f;
+            }
+        }
+        ok = mbar_wait(bar, mph & 1, wc, 2) && ok;
+        ++mph;
+        tc_fence_after();
+        // ---- dS = P (dP - D)
+        {
+            uint32_t dpv[64];
+            tmem_ld64(tmem + lane_base + kColDP + 64 * hf, dpv);
+            tmem_ld_wait();
+#pragma unroll
+            for (int k = 0; k < 64; ++k) dpv[k] = __float_as_uint(pv[k] * (__uint_as_float(dpv[k]) - dd));
+            if (!key_cta) {
+                // dS (bf16 pairs) to TMEM, the A operand of dq_ac += dS K
+                uint32_t w[32];
+#pragma unroll
+                for (int m = 0; m < 32; ++m) w[m] = pack_bf16x2(__uint_as_float(dpv[2 * m]), __uint_as_float(dpv[2 * m + 1]));
+                tmem_st32(tmem + lane_base + kColDS + 32 * hf, w);
+                // G[li][c], c = li + 127 - 64 hf - k, for distances 128 t + li - 64 hf - k below
+                // clamp_len; the rest of the row's pairs summed in fp32
+                const int cb = li + 127 - 64 * hf;
+                const int kc = 128 * t + li - 64 * hf - C + 1;     // first k with distance < C
+                const uint32_t gbase = s_x;
+#pragma unroll
+                for (int k = 0; k < 64; ++k) {
+                    const float x = __uint_as_float(dpv[k]);
+                    const bool in = k >= kc;
+                    if (!in) csum += x;
+                    const __nv_bfloat16 gb = __float2bfloat16_rn(in ? x : 0.f);
+                    sts_u16(gbase + g_off(li, cb - k), __bfloat16_as_ushort(gb));
+                }
+                tmem_st_wait();
+            } else {
+                // P and dS as [query][key] rows: atom hf holds keys 64 hf .. 64 hf + 63
+                uint8_t* prow = sm + USmem::X + hf * kTileBytes + li * 128;
+                uint8_t* drow = prow + 2 * kTileBytes;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    uint32_t wp[4], wd[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        wp[e] = pack_bf16x2(pv[8 * j + 2 * e], pv[8 * j + 2 * e + 1]);
+                        wd[e] = pack_bf16x2(__uint_as_float(dpv[8 * j + 2 * e]), __uint_as_float(dpv[8 * j + 2 * e + 1]));
+                    }
+                    const int off = ((j ^ li) & 7) << 4;
+                    *reinterpret_cast<uint4*>(prow + off) = make_uint4(wp[0], wp[1], wp[2], wp[3]);
+                    *reinterpret_cast<uint4*>(drow + off) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+                }
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        // ---- gradient products
+        if (tid == 0) {
+            tc_fence_after();
+            if (!key_cta) {
+                // dq_ac += dS K (A: dS in TMEM, 8 columns per 16 keys; B: K as [key][d], MN-major)
+                const uint64_t kd = sdesc_mn_sw128(s_k, kTileBytes);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    umma_ts(tmem + kColA0, tmem + kColDS + 8 * kk, kd + 128 * kk, id_kn, (t > 0 || kk > 0) ? 1u : 0u);
+                // dq_bd += G R_win (A: G K-major over 256 window columns; B: the two R blocks as
+                // [row][d], MN-major)
+#pragma unroll
+                for (int kk = 0; kk < 16; ++kk) {
+                    const uint64_t ad = sdesc_k_sw128(s_x + (kk >> 2) * kTileBytes) + 2 * (kk & 3);
+                    const uint64_t bd =
+                        sdesc_mn_sw128(s_r + (kk < 8 ? ra : rb) * kTileBytes, kTileBytes) + 128 * (kk & 7);
+                    umma_ss(tmem + kColA1, ad, bd, id_kn, (t > 0 || kk > 0) ? 1u : 0u);
+                }
+                // dr_win = G^T Qc'' (A: G read MN-major, 128 window rows = two atoms; B: Qc''
+                // as [query][d], MN-major), lower block into columns 0..63, upper into 64..127
+                const uint64_t qvd = sdesc_mn_sw128(s_qv, kTileBytes);
+#pragma unroll
+                for (int kq = 0; kq < 8; ++kq) {
+                    umma_ss(tmem + kColS, sdesc_mn_sw128(s_x, kTileBytes) + 128 * kq, qvd + 128 * kq, id_mm,
+                            kq > 0 ? 1u : 0u);
+                    umma_ss(tmem + kColS + 64, sdesc_mn_sw128(s_x + 2 * kTileBytes, kTileBytes) + 128 * kq,
+                            qvd + 128 * kq, id_mm, kq > 0 ? 1u : 0u);
+                }
+            } else {
+                // dv += P^T dO, dk += dS^T Qc' (A: P / dS read MN-major; B: dO / Qc' MN-major)
+                const uint64_t pd = sdesc_mn_sw128(s_x, kTileBytes), dsd = sdesc_mn_sw128(s_x + 2 * kTileBytes, kTileBytes);
+                const uint64_t god = sdesc_mn_sw128(s_go, kTileBytes), qud = sdesc_mn_sw128(s_qu, kTileBytes);
+#pragma unroll
+                for (int kq = 0; kq < 8; ++kq) {
+                    const uint32_t acc = (t > 0 || kq > 0) ? 1u : 0u;
+                    umma_ss(tmem + kColA0, pd + 128 * kq, god + 128 * kq, id_mm, acc);
+                    umma_ss(tmem + kColA1, dsd + 128 * kq, qud + 128 * kq, id_mm, acc);
+                }
+            }
+            umma_commit(bar);
+        }
+        ok = mbar_wait(bar, mph & 1, wc, 3) && ok;
+        ++mph;
+        tc_fence_after();
+        // ---- the next step's operands (every buffer is free once the products above completed)
+        if (t + 1 < n_steps) {
+            if (key_cta) {
+                i0 += 128;
+                load_queries(p, sm, b, h, i0, c, tid);
+            } else {
+                load_keys(a, sm, b, h, j0 - 128, tid);
+            }
+            load_rblock(p, sm, h, t + 2, tid);
+            mma::cp_async_commit();
+            if (key_cta) row_stats(p, b, h, i0 + li, dd, l2);
+        }
+        if (!key_cta) {
+            // dr rows of block t (distances 128 t - 127 + li): this tile's lower block plus the
+            // previous tile's upper block; this thread adds dimensions 32 hf .. 32 hf + 31
+            uint32_t lo[32], hi[32];
+            tmem_ld32(tmem + lane_base + kColS + 32 * hf, lo);
+            tmem_ld32(tmem + lane_base + kColS + 64 + 32 * hf, hi);
+            tmem_ld_wait();
+            const int delta = 128 * t - 127 + li;
+            if (delta >= 0 && delta < C && delta < p.n_rows) {
+                float4* dst = reinterpret_cast<float4*>(p.dr + (static_cast<int64_t>(delta) * a.H + h) * 64 + 32 * hf);
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    atomicAdd(dst + e, make_float4(kLn2u * (__uint_as_float(lo[4 * e]) + carry[4 * e]),
+                                                   kLn2u * (__uint_as_float(lo[4 * e + 1]) + carry[4 * e + 1]),
+                                                   kLn2u * (__uint_as_float(lo[4 * e + 2]) + carry[4 * e + 2]),
+                                                   kLn2u * (__uint_as_float(lo[4 * e + 3]) + carry[4 * e + 3])));
+            }
+#pragma unroll
+            for (int e = 0; e < 32; ++e) carry[e] = __uint_as_float(hi[e]);
+        }
+        tc_fence_before();
+    }
+
+    if (!key_cta) {
+        // the last tile's upper block
+        {
+            const int delta = 128 * n_steps - 127 + li;
+            if (delta >= 0 && delta < C && delta < p.n_rows) {
+                float4* dst = reinterpret_cast<float4*>(p.dr + (static_cast<int64_t>(delta) * a.H + h) * 64 + 32 * hf);
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    atomicAdd(dst + e, make_float4(kLn2u * carry[4 * e], kLn2u * carry[4 * e + 1],
+                                                   kLn2u * carry[4 * e + 2], kLn2u * carry[4 * e + 3]));
+            }
+        }
+        // the clamped pairs: c_i r[C] into dq_bd, ln 2 sum_i c_i Qc''_i into dr[C]
+        csum_s[hf * 128 + li] = csum;
+        __syncthreads();
+        const float crow = csum_s[li] + csum_s[128 + li];
+        uint32_t qa[32], qb[32];
+        tmem_ld32(tmem + lane_base + kColA0 + 32 * hf, qa);
+        tmem_ld32(tmem + lane_base + kColA1 + 32 * hf, qb);
+        tmem_ld_wait();
+        const bool clamped = C < p.n_rows;                // else no distance reaches clamp_len
+        if (clamped) {
+            const __nv_bfloat16* rc =
+                static_cast<const __nv_bfloat16*>(a.r) + static_cast<int64_t>(C) * a.r_row + h * a.r_head + 32 * hf;
+            const uint8_t* qvrow = sm + USmem::QV + li * 128;
+            float* dst = p.dr + (static_cast<int64_t>(C) * a.H + h) * 64 + 32 * hf;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                qb[e] = __float_as_uint(__uint_as_float(qb[e]) + crow * __bfloat162float(rc[e]));
+                const int d = 32 * hf + e;
+                const uint16_t qbits =
+                    *reinterpret_cast<const uint16_t*>(qvrow + ((((d >> 3) ^ li) & 7) << 4) + ((d & 7) << 1));
+                float part = crow * __uint_as_float(static_cast<uint32_t>(qbits) << 16);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+                if (lane == 0) atomicAdd(dst + e, kLn2u * part);
+            }
+        }
+        // dq and the per-query parts of du (dS K) and dv_bias (dS r)
+        const int i = i0 + li;
+        if (i < L) {
+            const int64_t row = ((static_cast<int64_t>(b) * L + i) * a.H + h) * 64 + 32 * hf;
+            const float scale = a.scale;
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) {
+                const float4 xa = make_float4(scale * __uint_as_float(qa[e]), scale * __uint_as_float(qa[e + 1]),
+                                              scale * __uint_as_float(qa[e + 2]), scale * __uint_as_float(qa[e + 3]));
+                const float4 xb = make_float4(scale * __uint_as_float(qb[e]), scale * __uint_as_float(qb[e + 1]),
+                                              scale * __uint_as_float(qb[e + 2]), scale * __uint_as_float(qb[e + 3]));
+                *reinterpret_cast<float4*>(p.dq + row + e) = make_float4(xa.x + xb.x, xa.y + xb.y, xa.z + xb.z, xa.w + xb.w);
+                *reinterpret_cast<float4*>(p.pac + row + e) = xa;
+                *reinterpret_cast<float4*>(p.pbd + row + e) = xb;
+            }
+        }
+    } else {
+        // dv and dk of the owned keys (TMEM lane li = key jk + li)
+        uint32_t va[32], ka[32];
+        tmem_ld32(tmem + lane_base + kColA0 + 32 * hf, va);
+        tmem_ld32(tmem + lane_base + kColA1 + 32 * hf, ka);
+        tmem_ld_wait();
+        const int jt = 128 * own + li;                    // key index inside the current segment
+        if (jt < L) {
+            const int64_t row = ((static_cast<int64_t>(b) * L + jt) * a.H + h) * 64 + 32 * hf;
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) {
+                *reinterpret_cast<float4*>(p.dv + row + e) =
+                    make_float4(__uint_as_float(va[e]), __uint_as_float(va[e + 1]), __uint_as_float(va[e + 2]),
+                                __uint_as_float(va[e + 3]));
+                *reinterpret_cast<float4*>(p.dk + row + e) =
+                    make_float4(kLn2u * __uint_as_float(ka[e]), kLn2u * __uint_as_float(ka[e + 1]),
+                                kLn2u * __uint_as_float(ka[e + 2]), kLn2u * __uint_as_float(ka[e + 3]));
+            }
+        }
+    }
+    (void)ok;
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+inline bool al16u(const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; }
+inline bool st8u(int64_t s) { return (s & 7) == 0; }
+
+}  // namespace
+
+bool bwd_umma_eligible(const BwdParams& p, txl_dtype dtype)
+{
+    const AttnSimtParams& a = p.a;
+    if (!p.lse_given || !bwd_tc_eligible(p, dtype)) return false;
+    if (2 * ((a.L + 127) / 128) > 65535) return false;
+    return al16u(a.out) && st8u(a.o_sb) && st8u(a.o_st) && st8u(a.o_sh) && al16u(p.dq) && al16u(p.dk) &&
+           al16u(p.dv) && al16u(p.dr) && al16u(p.pac) && al16u(p.pbd);
+}
+
+// dq, dk, dv, pac, pbd are written; dr must be zero on entry (atomic accumulation).
+cudaError_t launch_bwd_umma(const BwdParams& p, cudaStream_t s)
+{
+    static bool attr_done = false;
+    if (!attr_done) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(bwd_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, USmem::Size);
+        if (e != cudaSuccess) return e;
+        attr_done = true;
+    }
+    const int n_qt = (p.a.L + 127) / 128;
+    const dim3 grid(p.a.H, p.a.B, 2 * n_qt);
+    bwd_umma_kernel<<<grid, kUThreads, USmem::Size, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace txl

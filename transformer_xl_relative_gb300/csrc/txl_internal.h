@@ -155,6 +155,7 @@ struct BwdParams {
     float* lse; float* dd;                      // workspace [B][L][H]: log-sum-exp, dO . out
     float* pac; float* pbd;                     // workspace [B][L][H][D]: per-query parts of du, dv_bias
     int lse_given;                              // lse already holds every row's log-sum-exp
+    int* err_flag;                              // device status (TXL_ERR_TIMEOUT on a wait abandoned), may be null
 };
 
 struct PosBwdParams {
@@ -168,6 +169,10 @@ cudaError_t launch_rel_attn_bwd(const BwdParams& p, txl_dtype dtype, cudaStream_
 // (dq, pac, pbd written; dk, dv, dr accumulated atomically into zeroed buffers)
 bool bwd_tc_eligible(const BwdParams& p, txl_dtype dtype);
 cudaError_t launch_bwd_tc(const BwdParams& p, cudaStream_t s);
+// tcgen05 gradient kernel (the above, with the forward's log-sum-exp given and out, dq, dk, dv, dr,
+// pac, pbd 16-byte aligned): dq, dk, dv, pac, pbd written; dr accumulated atomically (zeroed first)
+bool bwd_umma_eligible(const BwdParams& p, txl_dtype dtype);
+cudaError_t launch_bwd_umma(const BwdParams& p, cudaStream_t s);
 
 // ---------------------------------------------------------------- learned-table variant (SIMT)
 struct TableParams {
