@@ -595,11 +595,13 @@ def bwd_flops(B, H, D, L, M, n_rows, d_model):
 
 
 def bench_backward(txl, device, stream, rank, args):
-    """Gradients of one fused-attention call on the large workload: txl_rel_attn_bwd (on this
-    workload the fused forward kernel's row log-sum-exp pass on tcgen05, then the gradient kernel:
-    bf16 mma.sync products, fp32 accumulation and gradients) and the position table's
-    txl_rel_pos_bwd, timed together and each alone.  The attention backward is reported against the
-    measured bf16 tensor peak."""
+    """Gradients of one fused-attention call on the large workload.  The forward is run once,
+    untimed, with its softmax statistics saved (txl_rel_attn_fwd_lse, as a training step's forward
+    keeps them); then timed: txl_rel_attn_bwd_lse (the row dot products dO . out, then the tcgen05
+    gradient kernel: bf16 operands, fp32 TMEM accumulators and gradients; the bias reduction) and the
+    position table's txl_rel_pos_bwd, together and each alone; and, for comparison, txl_rel_attn_bwd
+    without the saved statistics (it first retakes them with the fused forward kernel's statistics
+    pass).  The attention backward is reported against the measured bf16 tensor peak."""
     import torch
     B, H, D, L, M, C, dm = 16, 16, 64, 384, 384, 1000, 1024
     dt = torch.bfloat16
@@ -615,13 +617,17 @@ def bench_backward(txl, device, stream, rank, args):
     v = torch.randn(B, M + L, H, D, generator=g, device=device).to(dt)
     dO = torch.randn(B, L, H, D, generator=g, device=device).to(dt)
     out = torch.empty(B, L, H, D, dtype=dt, device=device)
+    lse = torch.empty(B, L, H, dtype=torch.float32, device=device)
     mem = txl.Memory(k[:, :M], v[:, :M], 0, M)
-    txl.rel_attn_fwd(q, mem, k[:, M:], v[:, M:], u, vb, r, n_rows, C, out)
+    txl.rel_attn_fwd(q, mem, k[:, M:], v[:, M:], u, vb, r, n_rows, C, out, lse=lse)
     ws = torch.empty(16 * 1024 * 1024 * 8, dtype=torch.uint8, device=device)
     res = {}
 
     def attn():
-        res["g"] = txl.rel_attn_bwd(q, mem, k[:, M:], v[:, M:], u, vb, r, n_rows, C, out, dO, workspace=ws)
+        res["g"] = txl.rel_attn_bwd(q, mem, k[:, M:], v[:, M:], u, vb, r, n_rows, C, out, dO, workspace=ws, lse=lse)
+
+    def attn_recompute():
+        txl.rel_attn_bwd(q, mem, k[:, M:], v[:, M:], u, vb, r, n_rows, C, out, dO, workspace=ws)
 
     def pos():
         res["dW"] = txl.rel_pos_bwd(res["g"]["dr"], dm)
@@ -646,13 +652,15 @@ def bench_backward(txl, device, stream, rank, args):
     t_us = timed(both)
     t_attn = timed(attn)
     t_pos = timed(pos)
+    t_attn_rec = timed(attn_recompute)
     f_attn, f_pos = bwd_flops(B, H, D, L, M, n_rows, dm)
     bf16_peak, _, _, peak_src = _peaks()
     achieved = f_attn / (t_attn * 1e-6) / 1e12
     return {"workload": "backward: B16 H16 D64 d_model1024 L384 M384 clamp1000, bf16 inputs, fp32 gradients",
             "us_per_call": t_us, "us_attn_bwd": t_attn, "us_pos_bwd": t_pos,
+            "us_attn_bwd_without_saved_lse": t_attn_rec,
             "algorithmic_flops_per_call": f_attn + f_pos, "tflops": (f_attn + f_pos) / (t_us * 1e-6) / 1e12,
-            "roofline": {"kernel": "txl_rel_attn_bwd (attn_persist_kernel log-sum-exp pass + bwd_tc_kernel, bf16 mma.sync, + bias reduction)",
+            "roofline": {"kernel": "txl_rel_attn_bwd_lse (bwd_rowdot_kernel + bwd_umma_kernel, tcgen05 with TMEM accumulators, + bias reduction)",
                          "bound": "tensor", "achieved": achieved, "peak": bf16_peak, "unit": "TFLOP/s",
                          "frac": achieved / bf16_peak, "algorithmic_flops_per_launch": f_attn,
                          "peak_source": peak_src + " bf16 burst"}}

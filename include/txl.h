@@ -321,8 +321,10 @@ size_t txl_rel_attn_layer_fused_workspace_size(int B, int L, int H, int D);
  * strides (q, k, v, the memory, d_out, r): bf16 products on the tensor cores with fp32 accumulation
  * (c(q + u), c(q + v), P and dS rounded to bf16 as product operands, c = scale log2 e; pairs whose
  * distance reaches clamp_len summed in fp32), the row log-sum-exp taken by the fused forward kernel
- * when that kernel takes the inputs (written into the workspace).  Every other case: fp32
- * arithmetic on the CUDA cores.  Enqueues several launches.
+ * when that kernel takes the inputs (written into the workspace).  With out, the gradients and dr
+ * 16-byte aligned as well, the gradient products run as tcgen05 MMAs with TMEM accumulators (a
+ * launch of query CTAs for dq and dr, and key CTAs for dk and dv); otherwise as mma.sync products.
+ * Every other case: fp32 arithmetic on the CUDA cores.  Enqueues several launches.
  */
 txl_status txl_rel_attn_bwd(int B, int L, int H, int D, int clamp_len,
                             const txl_view* q, const txl_mem* mem,
@@ -336,6 +338,45 @@ txl_status txl_rel_attn_bwd(int B, int L, int H, int D, int clamp_len,
 
 /* Bytes of device workspace txl_rel_attn_bwd needs: B*L*H*(2 + 2*D)*4 (0 for an empty shape). */
 size_t txl_rel_attn_bwd_workspace_size(int B, int L, int H, int D);
+
+/*
+ * txl_rel_attn_fwd_lse -- txl_rel_attn_fwd that also saves the statistics of its softmax, as a
+ * forward pass does for its backward:
+ *   lse : device fp32 [B][L][H] (4-byte aligned), lse[(b L + i) H + h] = m_i + log2 l_i, the
+ *         log2-domain log-sum-exp of row i's visible scores in the units c s_ij (c = scale log2 e):
+ *         m_i the row maximum, l_i the sum of the bf16 weights 2^(c s_ij - m_i) that the output's
+ *         P.V multiplied (the output's own normaliser).
+ * out is written exactly as txl_rel_attn_fwd writes it.  Only the fused tcgen05 kernel keeps the
+ * statistics: bf16, D <= 64 and the inputs its path takes (txl_rel_attn_path = 1), else
+ * TXL_ERR_UNSUPPORTED before any launch; lse NULL: TXL_ERR_INVALID_ARG; misaligned:
+ * TXL_ERR_ALIGNMENT.  Other arguments and errors as txl_rel_attn_fwd.
+ */
+txl_status txl_rel_attn_fwd_lse(int B, int L, int H, int D, int clamp_len,
+                                const txl_view* q, const txl_mem* mem,
+                                const txl_view* k_cur, const txl_view* v_cur,
+                                const float* u, const float* v_bias,
+                                const void* r, int64_t ld_r, int n_rows,
+                                float scale, const txl_view* out, float* lse, txl_dtype dtype,
+                                void* workspace, size_t workspace_bytes,
+                                int* err_flag, void* stream);
+
+/*
+ * txl_rel_attn_bwd_lse -- txl_rel_attn_bwd given the statistics txl_rel_attn_fwd_lse saved for
+ * the same call (same inputs and output): on the tensor-core path the gradient kernels read lse
+ * in place of taking the row log-sum-exp again (one pass over the keys fewer).  lse: device fp32
+ * [B][L][H] (4-byte aligned, TXL_ERR_ALIGNMENT otherwise), read only; NULL gives
+ * txl_rel_attn_bwd.  Paths that do not use the statistics ignore it.  Other arguments, results and
+ * errors as txl_rel_attn_bwd.
+ */
+txl_status txl_rel_attn_bwd_lse(int B, int L, int H, int D, int clamp_len,
+                                const txl_view* q, const txl_mem* mem,
+                                const txl_view* k_cur, const txl_view* v_cur,
+                                const float* u, const float* v_bias,
+                                const void* r, int64_t ld_r, int n_rows, float scale,
+                                const txl_view* out, const txl_view* d_out, const float* lse,
+                                float* dq, float* dk_cur, float* dv_cur, float* du, float* dv_bias,
+                                float* dr, txl_dtype dtype, void* workspace, size_t workspace_bytes,
+                                void* stream);
 
 /*
  * txl_rel_pos_bwd -- gradient of W_R from the gradient of the position rows:

@@ -20,5 +20,6 @@ from .oracle import (  # noqa: F401
     stream_layer,
     layer_flops,
     rel_attn_bwd,
+    rel_attn_lse,
     table_attn,
 )

@@ -247,6 +247,36 @@ def rel_attn_bwd(q, k, v, u, vb, W_R, M: int, mem_valid: int, clamp_len: int, dO
     return out
 
 
+def rel_attn_lse(q, k, u, vb, W_R, M: int, mem_valid: int, clamp_len: int, scale=None) -> np.ndarray:
+    """Per query row of one ``rel_attn`` call, the log-sum-exp of its visible scores in log2 units:
+    lse[b, i, h] = log2 sum_j 2^(log2(e) S_ij) = log2(e) ln sum_j exp(S_ij), with the scores S of
+    ``rel_attn_bwd`` (the four-term score of "Transformer-XL 和相对位置编码" §2.3.2, scaled, over the
+    visible keys), i.e. the statistic a forward pass keeps for its backward.  Returns float64
+    [B, L, H]."""
+    q, k, u, vb, W = (_f64(x) for x in (q, k, u, vb, W_R))
+    B, L, H, D = q.shape
+    T = M + L
+    d_model = W.shape[0]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    n_rows = min(T, clamp_len + 1)
+    r = rel_table(n_rows, d_model, H, D, W)
+    i_idx = np.arange(L)[:, None]
+    j_idx = np.arange(T)[None, :]
+    delta = M + i_idx - j_idx
+    vis = (j_idx >= M - mem_valid) & (delta >= 0)
+    dcl = np.clip(np.minimum(delta, clamp_len), 0, n_rows - 1)
+    out = np.empty((B, L, H))
+    for b in range(B):
+        for h in range(H):
+            G = (q[b, :, h] + vb[h]) @ r[:, h].T
+            S = scale * ((q[b, :, h] + u[h]) @ k[b, :, h].T + np.take_along_axis(G, dcl, axis=1))
+            S = np.where(vis, S, -np.inf)
+            m = S.max(axis=1)
+            out[b, :, h] = (m + np.log(np.exp(S - m[:, None]).sum(axis=1))) / math.log(2.0)
+    return out
+
+
 def table_attn(q, k, v, u, vb, r_table, max_len: int, key_mask=None, scale=None) -> np.ndarray:
     """The learned-table variant of "TransformerXL 相对位置编码" §3.1 (bidirectional, no memory):
     the relative index rel(i, j) = clamp(i - j + max_len - 1, 0, 2 max_len - 2) selects a row of the

@@ -136,3 +136,63 @@ def test_backward_large_workload_sampled(txl):
         _close(g["dq"][b, :, h].cpu().numpy(), ref["dq"][b, :, h], RTOL["bf16"], "dq %d %d" % (b, h))
         _close(g["dk_cur"][b, :, h].cpu().numpy(), ref["dk"][b, M:, h], RTOL["bf16"], "dk %d %d" % (b, h))
         _close(g["dv_cur"][b, :, h].cpu().numpy(), ref["dv"][b, M:, h], RTOL["bf16"], "dv %d %d" % (b, h))
+
+
+LSE_CASES = [
+    # B, H, D, d_model, L, M, valid, C
+    (2, 2, 64, 128, 200, 150, 100, 1000),   # partly valid memory, ragged query tiles
+    (1, 2, 64, 128, 130, 0, 0, 60),         # no memory, clamp inside the sequence
+]
+
+
+@pytest.mark.parametrize("shape", LSE_CASES, ids=["B%dH%dL%dM%dv%dC%d" % (s[0], s[1], s[4], s[5], s[6], s[7])
+                                                  for s in LSE_CASES])
+def test_saved_statistics_and_the_backward_given_them(txl, shape):
+    """rel_attn_fwd with lse (txl_rel_attn_fwd_lse): the output is txl_rel_attn_fwd's, bit for bit,
+    and the saved row log-sum-exp is the oracle's (oracle.rel_attn_lse, log2 units) within the bf16
+    rounding of the query forms and of BD (|error| <= 0.05); rel_attn_bwd given it
+    (txl_rel_attn_bwd_lse) matches the oracle's gradients like the call without it."""
+    B, H, D, dm, L, M, valid, C = shape
+    cfg = txl_inputs.custom(B=B, H=H, D=D, d_model=dm, L=L, M=M, clamp_len=C, dtype="bf16", seed=700 + L + M)
+    case = txl_inputs.make_case(cfg)
+    dO = txl_inputs.make_qkv(cfg, seed=701 + L, L=L, T=1)[0]
+    q, k, v = (to_dev(case[n]) for n in ("q", "k", "v"))
+    n_rows = min(M + L, C + 1)
+    r = torch.empty(n_rows, H, D, dtype=torch.bfloat16, device="cuda")
+    txl.rel_pos_gen(case["W_R"].cuda(), r, n_rows, dm, H, D)
+    mem = txl.Memory(k[:, :M].contiguous(), v[:, :M].contiguous(), 0, valid) if M > 0 else None
+    u, vb = case["u"].cuda(), case["vb"].cuda()
+    out0, out1 = torch.empty_like(q), torch.empty_like(q)
+    lse = torch.full((B, L, H), float("nan"), dtype=torch.float32, device="cuda")
+    txl.rel_attn_fwd(q, mem, k[:, M:], v[:, M:], u, vb, r, n_rows, C, out0)
+    txl.rel_attn_fwd(q, mem, k[:, M:], v[:, M:], u, vb, r, n_rows, C, out1, lse=lse)
+    g = txl.rel_attn_bwd(q, mem, k[:, M:], v[:, M:], u, vb, r, n_rows, C, out1, to_dev(dO), lse=lse)
+    torch.cuda.synchronize()
+    assert torch.equal(out0, out1)
+    want = oracle.rel_attn_lse(case["q"], case["k"], case["u"], case["vb"], case["W_R"][:, :H * D], M, valid, C)
+    got = lse.cpu().numpy()
+    assert np.isfinite(got).all()
+    assert np.max(np.abs(got - want)) <= 0.05, np.max(np.abs(got - want))
+    ref = oracle.rel_attn_bwd(case["q"], case["k"], case["v"], case["u"], case["vb"], case["W_R"][:, :H * D], M, valid,
+                              C, dO)
+    tol = RTOL["bf16"]
+    _close(g["dq"].cpu().numpy(), ref["dq"], tol, "dq")
+    _close(g["dk_cur"].cpu().numpy(), ref["dk"][:, M:], tol, "dk")
+    _close(g["dv_cur"].cpu().numpy(), ref["dv"][:, M:], tol, "dv")
+    _close(g["du"].cpu().numpy(), ref["du"], tol, "du")
+    _close(g["dv_bias"].cpu().numpy(), ref["dvb"], tol, "dv_bias")
+    _close(g["dr"].cpu().numpy(), ref["dr"], tol, "dr")
+
+
+def test_saved_statistics_need_the_fused_kernel(txl):
+    """txl_rel_attn_fwd_lse refuses (TXL_ERR_UNSUPPORTED, nothing launched) inputs the fused kernel
+    does not take: fp32 here."""
+    B, L, H, D = 1, 16, 2, 64
+    q = torch.randn(B, L, H, D, device="cuda")
+    k, v = torch.randn_like(q), torch.randn_like(q)
+    u = torch.zeros(H, D, device="cuda")
+    r = torch.zeros(L, H, D, device="cuda")
+    out = torch.empty_like(q)
+    lse = torch.empty(B, L, H, device="cuda")
+    with pytest.raises(RuntimeError, match="txl_rel_attn_fwd_lse"):
+        txl.rel_attn_fwd(q, None, k, v, u, u, r, L, 1000, out, lse=lse)

@@ -67,3 +67,29 @@ def test_clamp_zero_leaves_no_position_bias_gradient():
     g = oracle.rel_attn_bwd(c["q"], c["k"], c["v"], c["u"], c["vb"], c["W_R"], 3, 3, 0, c["dO"])
     assert np.max(np.abs(g["dvb"])) <= 1e-12
     assert np.max(np.abs(g["dr"])) <= 1e-12
+
+
+@pytest.mark.parametrize("M,valid,C", [(2, 2, 10), (2, 1, 3), (0, 0, 1)])
+def test_log_sum_exp_matches_pairwise_scores(M, valid, C):
+    """oracle.rel_attn_lse against a brute-force sum over the visible keys of each row, each score
+    from the C oracle's four-term score (score_terms), in log2 units; and the weights
+    2^(log2(e) s_ij - lse_i) it implies reproduce the forward oracle's output."""
+    import math
+    c = _case(40 + M + valid + C, M=M)
+    B, L, H, D = c["q"].shape
+    scale = 1.0 / math.sqrt(D)
+    lse = oracle.rel_attn_lse(c["q"], c["k"], c["u"], c["vb"], c["W_R"], M, valid, C)
+    out = oracle.rel_attn(c["q"], c["k"], c["v"], c["u"], c["vb"], c["W_R"], M, valid, C, memo=False)
+    n_rows = min(M + L, C + 1)
+    r = oracle.rel_table(n_rows, c["W_R"].shape[0], H, D, c["W_R"])
+    for b in range(B):
+        for h in range(H):
+            for i in range(L):
+                js = [j for j in range(M - valid, M + L) if M + i - j >= 0]
+                s2 = {j: math.log2(math.e) * scale * oracle.score_terms(
+                    c["q"][b, i, h], c["k"][b, j, h], r[min(M + i - j, C), h], c["u"][h], c["vb"][h])[0] for j in js}
+                mx = max(s2.values())
+                want = mx + math.log2(math.fsum(2.0 ** (x - mx) for x in s2.values()))
+                assert abs(lse[b, i, h] - want) <= 1e-12 * max(1.0, abs(want))
+                o = sum(2.0 ** (s2[j] - lse[b, i, h]) * c["v"][b, j, h] for j in js)
+                assert np.max(np.abs(o - out[b, i, h])) <= 1e-12

@@ -118,20 +118,34 @@ def _attn_args(q, mem, k_cur, v_cur, r, out):
 def rel_attn_fwd(q: torch.Tensor, mem: Memory | None, k_cur: torch.Tensor, v_cur: torch.Tensor,
                  u: torch.Tensor, v_bias: torch.Tensor, r: torch.Tensor, n_rows: int,
                  clamp_len: int, out: torch.Tensor, scale: float = 0.0,
-                 err_flag: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """One relative-attention call over [memory ++ current] (txl_rel_attn_fwd)."""
+                 err_flag: torch.Tensor | None = None, stream=None, lse: torch.Tensor | None = None) -> torch.Tensor:
+    """One relative-attention call over [memory ++ current] (txl_rel_attn_fwd).  With `lse` (fp32
+    [B, L, H]) the call also saves every row's log-sum-exp for rel_attn_bwd (txl_rel_attn_fwd_lse)."""
     (B, L, H, D), memc, vq, vk, vv, vo = _attn_args(q, mem, k_cur, v_cur, r, out)
     if u.dtype != torch.float32 or v_bias.dtype != torch.float32:
         raise TypeError("u and v_bias are fp32 [H, D]")
     if not (u.is_contiguous() and v_bias.is_contiguous()):
         raise ValueError("u and v_bias must be contiguous [H, D]")
+    ef = err_flag.data_ptr() if err_flag is not None else None
+    if lse is not None:
+        _check_lse(lse, B, L, H)
+        st = _lib().txl_rel_attn_fwd_lse(
+            B, L, H, D, int(clamp_len), ctypes.byref(vq), memc, ctypes.byref(vk), ctypes.byref(vv),
+            u.data_ptr(), v_bias.data_ptr(), r.data_ptr(), r.stride(1), int(n_rows), float(scale),
+            ctypes.byref(vo), lse.data_ptr(), dtype_code(q), None, 0, ef, _stream(stream))
+        check(st, "txl_rel_attn_fwd_lse")
+        return out
     st = _lib().txl_rel_attn_fwd(
         B, L, H, D, int(clamp_len), ctypes.byref(vq), memc, ctypes.byref(vk), ctypes.byref(vv),
         u.data_ptr(), v_bias.data_ptr(), r.data_ptr(), r.stride(1), int(n_rows), float(scale),
-        ctypes.byref(vo), dtype_code(q), None, 0,
-        err_flag.data_ptr() if err_flag is not None else None, _stream(stream))
+        ctypes.byref(vo), dtype_code(q), None, 0, ef, _stream(stream))
     check(st, "txl_rel_attn_fwd")
     return out
+
+
+def _check_lse(lse: torch.Tensor, B: int, L: int, H: int) -> None:
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, L, H) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 [B, L, H] tensor")
 
 
 def rel_attn_decode_workspace_size(q: torch.Tensor, mem: Memory | None) -> int:
@@ -292,8 +306,9 @@ def rel_attn_layer_fused(h: torch.Tensor, mem: Memory, mem_len: int, W_qkv: torc
 def rel_attn_bwd(q: torch.Tensor, mem: Memory | None, k_cur: torch.Tensor, v_cur: torch.Tensor,
                  u: torch.Tensor, v_bias: torch.Tensor, r: torch.Tensor, n_rows: int, clamp_len: int,
                  out: torch.Tensor, d_out: torch.Tensor, scale: float = 0.0,
-                 workspace: torch.Tensor | None = None, stream=None) -> dict:
-    """Gradients of one rel_attn_fwd call for the upstream gradient d_out (txl_rel_attn_bwd).
+                 workspace: torch.Tensor | None = None, stream=None, lse: torch.Tensor | None = None) -> dict:
+    """Gradients of one rel_attn_fwd call for the upstream gradient d_out (txl_rel_attn_bwd; with
+    `lse`, the statistics rel_attn_fwd saved for this call, txl_rel_attn_bwd_lse).
     Returns fp32 tensors dq, dk_cur, dv_cur [B, L, H, D], du, dv_bias [H, D], dr [n_rows, H, D]."""
     (B, L, H, D), memc, vq, vk, vv, vo = _attn_args(q, mem, k_cur, v_cur, r, out)
     vg = view(d_out)
@@ -306,13 +321,16 @@ def rel_attn_bwd(q: torch.Tensor, mem: Memory | None, k_cur: torch.Tensor, v_cur
     need = int(_lib().txl_rel_attn_bwd_workspace_size(B, L, H, D))
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
-    st = _lib().txl_rel_attn_bwd(
+    if lse is not None:
+        _check_lse(lse, B, L, H)
+    st = _lib().txl_rel_attn_bwd_lse(
         B, L, H, D, int(clamp_len), ctypes.byref(vq), memc, ctypes.byref(vk), ctypes.byref(vv),
         u.data_ptr(), v_bias.data_ptr(), r.data_ptr(), r.stride(1), int(n_rows), float(scale),
-        ctypes.byref(vo), ctypes.byref(vg), g["dq"].data_ptr(), g["dk_cur"].data_ptr(), g["dv_cur"].data_ptr(),
+        ctypes.byref(vo), ctypes.byref(vg), lse.data_ptr() if lse is not None else None,
+        g["dq"].data_ptr(), g["dk_cur"].data_ptr(), g["dv_cur"].data_ptr(),
         g["du"].data_ptr(), g["dv_bias"].data_ptr(), g["dr"].data_ptr(), dtype_code(q), workspace.data_ptr(),
         workspace.numel() * workspace.element_size(), _stream(stream))
-    check(st, "txl_rel_attn_bwd")
+    check(st, "txl_rel_attn_bwd_lse" if lse is not None else "txl_rel_attn_bwd")
     return g
 
 

@@ -243,7 +243,7 @@ namespace {
 txl_status attn_tc_launch(int B, int L, int H, int D, int clamp_len, const txl_view* q, const txl_mem* mem,
                           const txl_view* k_cur, const txl_view* v_cur, const float* u, const float* v_bias,
                           const void* r, int64_t ld_r, int n_rows, float scale, const txl_view* out, int* err_flag,
-                          cudaStream_t s, int ring_slots, float* lse = nullptr)
+                          cudaStream_t s, int ring_slots, float* lse = nullptr, int lse_out = 0)
 {
     const int M = (mem && mem->M > 0) ? mem->M : 0;
     const int valid = M > 0 ? mem->valid : 0;
@@ -293,6 +293,7 @@ txl_status attn_tc_launch(int B, int L, int H, int D, int clamp_len, const txl_v
     p.qscale = scale * 1.4426950408889634f;
     p.err_flag = err_flag;
     p.lse = lse;
+    p.lse_out = lse_out;
     if (lse && p.n_atoms != 1) return TXL_ERR_UNSUPPORTED;
     if (p.n_atoms == 1) {
         if (static_cast<int64_t>(p.n_qt) * H * B > INT32_MAX) return TXL_ERR_UNSUPPORTED;
@@ -400,6 +401,29 @@ bool decode_takes_fused(int B, int L, int H, int D, const txl_view* q, const txl
 }
 
 }  // namespace
+
+txl_status txl_rel_attn_fwd_lse(int B, int L, int H, int D, int clamp_len, const txl_view* q, const txl_mem* mem,
+                                const txl_view* k_cur, const txl_view* v_cur, const float* u, const float* v_bias,
+                                const void* r, int64_t ld_r, int n_rows, float scale, const txl_view* out,
+                                float* lse, txl_dtype dtype, void* workspace, size_t workspace_bytes, int* err_flag,
+                                void* stream)
+{
+    if (!lse) return TXL_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return TXL_ERR_ALIGNMENT;
+    txl_status st = check_attn(B, L, H, D, q, mem, k_cur, v_cur, r, ld_r, out, dtype);
+    if (st != TXL_OK) return st;
+    if (clamp_len < 0 || !u || !v_bias) return TXL_ERR_INVALID_ARG;
+    const int M = (mem && mem->M > 0) ? mem->M : 0;
+    if (n_rows < std::min(M + L, clamp_len + 1)) return TXL_ERR_INVALID_ARG;
+    // the statistics come from the persistent fused kernel (bf16, d_head <= 64) alone
+    if (D > 64 || !attn_tc_eligible(B, L, H, D, q, mem, k_cur, v_cur, r, ld_r, dtype)) return TXL_ERR_UNSUPPORTED;
+    (void)workspace;
+    (void)workspace_bytes;
+    if (B == 0 || L == 0) return TXL_OK;
+    if (scale <= 0.f) scale = 1.0f / std::sqrt(static_cast<float>(D));
+    return attn_tc_launch(B, L, H, D, clamp_len, q, mem, k_cur, v_cur, u, v_bias, r, ld_r, n_rows, scale, out, err_flag,
+                          static_cast<cudaStream_t>(stream), 0, lse, 1);
+}
 
 txl_status txl_rel_attn_fwd(int B, int L, int H, int D, int clamp_len, const txl_view* q, const txl_mem* mem,
                             const txl_view* k_cur, const txl_view* v_cur, const float* u, const float* v_bias,
@@ -809,6 +833,19 @@ txl_status txl_rel_attn_bwd(int B, int L, int H, int D, int clamp_len, const txl
                             float* dv_bias, float* dr, txl_dtype dtype, void* workspace, size_t workspace_bytes,
                             void* stream)
 {
+    return txl_rel_attn_bwd_lse(B, L, H, D, clamp_len, q, mem, k_cur, v_cur, u, v_bias, r, ld_r, n_rows, scale, out,
+                                d_out, nullptr, dq, dk_cur, dv_cur, du, dv_bias, dr, dtype, workspace, workspace_bytes,
+                                stream);
+}
+
+txl_status txl_rel_attn_bwd_lse(int B, int L, int H, int D, int clamp_len, const txl_view* q, const txl_mem* mem,
+                                const txl_view* k_cur, const txl_view* v_cur, const float* u, const float* v_bias,
+                                const void* r, int64_t ld_r, int n_rows, float scale, const txl_view* out,
+                                const txl_view* d_out, const float* lse, float* dq, float* dk_cur, float* dv_cur,
+                                float* du, float* dv_bias, float* dr, txl_dtype dtype, void* workspace,
+                                size_t workspace_bytes, void* stream)
+{
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return TXL_ERR_ALIGNMENT;
     txl_status st = check_attn(B, L, H, D, q, mem, k_cur, v_cur, r, ld_r, out, dtype);
     if (st != TXL_OK) return st;
     if (clamp_len < 0 || !u || !v_bias || !view_ok(d_out)) return TXL_ERR_INVALID_ARG;
@@ -857,9 +894,14 @@ txl_status txl_rel_attn_bwd(int B, int L, int H, int D, int clamp_len, const txl
     // (its statistics alone, nothing else written), in place of the gradient kernel's own first
     // pass over the keys
     if (bwd_tc_eligible(p, dtype) && attn_tc_eligible(B, L, H, D, q, mem, k_cur, v_cur, r, ld_r, dtype)) {
-        const txl_status fs = attn_tc_launch(B, L, H, D, clamp_len, q, mem, k_cur, v_cur, u, v_bias, r, ld_r, n_rows,
-                                             scale, out, nullptr, s, 0, p.lse);
-        if (fs != TXL_OK) return fs;
+        if (lse) {
+            // the forward's own statistics (txl_rel_attn_fwd_lse), read in place
+            p.lse = const_cast<float*>(lse);
+        } else {
+            const txl_status fs = attn_tc_launch(B, L, H, D, clamp_len, q, mem, k_cur, v_cur, u, v_bias, r, ld_r,
+                                                 n_rows, scale, out, nullptr, s, 0, p.lse);
+            if (fs != TXL_OK) return fs;
+        }
         p.lse_given = 1;
     }
     return launch_rel_attn_bwd(p, dtype, s) == cudaSuccess ? TXL_OK : TXL_ERR_CUDA;

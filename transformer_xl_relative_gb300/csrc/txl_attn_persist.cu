@@ -176,8 +176,9 @@ __device__ __forceinline__ void key_tile(const AttnTcParams& p, const Item& it, 
 // get weight 0 beside any unmasked key, and a row whose keys are all masked weighs them equally.
 constexpr uint16_t kMaskedKeyBf16 = 0xF14A;
 
-// kLse: the row statistics alone (log-sum-exp for the gradient kernels): no output is written.
-template <bool kTab, bool kMask = false, bool kLse = false>
+// kLse = 1: the row statistics alone (log-sum-exp for the gradient kernels): no output is written.
+// kLse = 2: the forward output and, besides it, every row's log-sum-exp.
+template <bool kTab, bool kMask = false, int kLse = 0>
 __global__ void __launch_bounds__(kPThreads, 1) attn_persist_kernel(const __grid_constant__ AttnTcParams p)
 {
     constexpr int NPV = 64;
@@ -658,7 +659,7 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_persist_kernel(const __grid
                     const uint64_t negm = f2_pack(-m_run, -m_run);
                     float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
                     uint32_t pw[32];
-                    if constexpr (kLse) {
+                    if constexpr (kLse == 1) {
                         // the row sum alone, from fp32 exponentials of the fp32 logits (P is not
                         // needed: zeros go through P.V)
 #pragma unroll
@@ -725,7 +726,7 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_persist_kernel(const __grid
             xchg[2 * (it.n_t & 1) + hf] = l_half;
             pair_bar(li);
             const bool staged = p.out_a16 != 0;
-            if (ok && kLse) {
+            if (ok && kLse == 1) {
                 // log2-domain log-sum-exp of the row, in the scaled score units of the logits
                 __syncwarp();
                 mbar_arrive_if(bar.o_free, lane == 0);
@@ -742,6 +743,13 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_persist_kernel(const __grid
                 __syncwarp();
                 mbar_arrive_if(bar.o_free, lane == 0);
                 const float inv_l = rcp_approx(l_half + xchg[2 * (it.n_t & 1) + (hf ^ 1)]);
+                if constexpr (kLse == 2) {
+                    // the row sum of the bf16 P that P.V multiplied, the normaliser of out
+                    const int i = it.i0 + pi;
+                    if (hf == 0 && i < p.L)
+                        p.lse[(static_cast<int64_t>(it.b) * p.L + i) * p.H + it.h] =
+                            m_run + __log2f(l_half + xchg[2 * (it.n_t & 1) + 1]);
+                }
                 if (staged) {
                     uint4* st = reinterpret_cast<uint4*>(bdrow + 16 * hf);
 #pragma unroll
@@ -765,7 +773,7 @@ __global__ void __launch_bounds__(kPThreads, 1) attn_persist_kernel(const __grid
                 }
             }
             pair_bar(li);                                   // both halves of every row are staged
-            if (!kLse && ok && staged) {
+            if (kLse != 1 && ok && staged) {
                 // this warp stores rows (li & ~31) + 16 hf + 0..15: lane -> row + lane / 8, chunk
                 // of 8 columns lane mod 8
                 const uint32_t* bd0 = reinterpret_cast<const uint32_t*>(smem + PSmem::BD);
@@ -817,15 +825,21 @@ cudaError_t launch_attn_persist(const AttnTcParams& p, int sm_count, cudaStream_
         e = cudaFuncSetAttribute(attn_persist_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  PSmem::Size);
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(attn_persist_kernel<false, false, true>,
+        e = cudaFuncSetAttribute(attn_persist_kernel<false, false, 1>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, PSmem::Size);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(attn_persist_kernel<false, false, 2>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, PSmem::Size);
         if (e != cudaSuccess) return e;
         attr_done = true;
     }
     const int64_t items = static_cast<int64_t>(p.n_qt) * p.H * p.B;
     const int grid = static_cast<int>(items < sm_count ? items : sm_count);
+    if (p.lse && !p.table && p.lse_out)
+        return launch_dependent(attn_persist_kernel<false, false, 2>, dim3(grid), dim3(kPThreads), PSmem::Size,
+                                s, p);
     if (p.lse && !p.table)
-        return launch_dependent(attn_persist_kernel<false, false, true>, dim3(grid), dim3(kPThreads), PSmem::Size,
+        return launch_dependent(attn_persist_kernel<false, false, 1>, dim3(grid), dim3(kPThreads), PSmem::Size,
                                 s, p);
     if (p.table == 2)
         return launch_dependent(attn_persist_kernel<true, true>, dim3(grid), dim3(kPThreads), PSmem::Size, s, p);

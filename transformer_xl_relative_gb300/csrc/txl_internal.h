@@ -137,8 +137,10 @@ struct AttnTcParams {
     float bscale;
     const uint8_t* key_mask;     // learned-table mode 2: [B][L], keys with 0 score -1e9
     // persistent kernel, log-sum-exp mode (lse != null): every query row's log2-domain
-    // log-sum-exp m + log2(l) is written to lse[(b L + i) H + h]; out is not written
+    // log-sum-exp m + log2(l) is written to lse[(b L + i) H + h]; out is written as well when
+    // lse_out is set, not otherwise
     float* lse;
+    int lse_out;
 };
 
 cudaError_t launch_attn_tc(const AttnTcParams& p, cudaStream_t s);
