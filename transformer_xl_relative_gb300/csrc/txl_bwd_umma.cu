@@ -328,29 +328,34 @@ __global__ void __launch_bounds__(kUThreads, 1) bwd_umma_kernel(const __grid_con
 #pragma unroll
     for (int e = 0; e < 16; ++e) carry[e] = 0.f;
 
+    // operand slots of step t: a query CTA's key and value tiles alternate between two slots, a key
+    // CTA's dO between two; position block beta sits in R slot beta mod 3
+    auto slot_k = [&](int t) { return smem_u32(sm + ((key_cta || (t & 1) == 0) ? USmem::K0 : USmem::K1)); };
+    auto slot_v = [&](int t) { return smem_u32(sm + ((key_cta || (t & 1) == 0) ? USmem::V0 : USmem::V1)); };
+    auto slot_go = [&](int t) { return smem_u32(sm + ((!key_cta || (t & 1) == 0) ? USmem::GO : USmem::V1)); };
+    // ---- S = Qc' K^T, W = Qc'' R_win^T (two halves of 128 window rows) of step t: thread 0, once the
+    //      step's operands are in shared memory and the TMEM columns are free
+    auto issue_scores = [&](int t) {
+        tc_fence_after();
+        const uint32_t sk = slot_k(t), ra = s_r + (t % 3) * kTileBytes, rb = s_r + ((t + 1) % 3) * kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            const uint32_t acc = kk > 0 ? 1u : 0u;
+            umma_ss(tmem + kColS, sdesc_k_sw128(s_qu) + 2 * kk, sdesc_k_sw128(sk) + 2 * kk, id_nn, acc);
+            umma_ss(tmem + kColW, sdesc_k_sw128(s_qv) + 2 * kk, sdesc_k_sw128(ra) + 2 * kk, id_nn, acc);
+            umma_ss(tmem + kColW + 128, sdesc_k_sw128(s_qv) + 2 * kk, sdesc_k_sw128(rb) + 2 * kk, id_nn, acc);
+        }
+        umma_commit(bar);
+    };
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) issue_scores(0);
+
     for (int t = 0; t < n_steps; ++t) {
         const int j0 = key_cta ? jk : M + i0 - 128 * t;
-        // operand slots of this step
-        const uint32_t s_k = smem_u32(sm + ((key_cta || (t & 1) == 0) ? USmem::K0 : USmem::K1));
-        const uint32_t s_v = smem_u32(sm + ((key_cta || (t & 1) == 0) ? USmem::V0 : USmem::V1));
-        const uint32_t s_go = smem_u32(sm + ((!key_cta || (t & 1) == 0) ? USmem::GO : USmem::V1));
+        const uint32_t s_k = slot_k(t), s_v = slot_v(t), s_go = slot_go(t);
         const uint32_t s_ra = s_r + (t % 3) * kTileBytes, s_rb = s_r + ((t + 1) % 3) * kTileBytes;
-        mma::cp_async_wait_all();
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        // ---- S = Qc' K^T, W = Qc'' R_win^T (two halves of 128 window rows)
-        if (tid == 0) {
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                const uint32_t acc = kk > 0 ? 1u : 0u;
-                umma_ss(tmem + kColS, sdesc_k_sw128(s_qu) + 2 * kk, sdesc_k_sw128(s_k) + 2 * kk, id_nn, acc);
-                umma_ss(tmem + kColW, sdesc_k_sw128(s_qv) + 2 * kk, sdesc_k_sw128(s_ra) + 2 * kk, id_nn, acc);
-                umma_ss(tmem + kColW + 128, sdesc_k_sw128(s_qv) + 2 * kk, sdesc_k_sw128(s_rb) + 2 * kk, id_nn, acc);
-            }
-            umma_commit(bar);
-        }
         // ---- the next step's operands, into slots the step before released
         float dd_next = 0.f, l2_next = 0.f;
         if (t + 1 < n_steps) {
@@ -589,7 +594,8 @@ __global__ void __launch_bounds__(kUThreads, 1) bwd_umma_kernel(const __grid_con
         if (!key_cta) {
             // dr rows of block t (distances 128 t - 127 + li): this tile's lower block plus the
             // previous tile's upper block, staged as fp32 rows in X (G is no longer read), then
-            // added to dr a whole row per warp instruction (lane l: dimensions 2l, 2l + 1)
+            // added to dr a whole row per warp instruction (lane l: dimensions 2l, 2l + 1) while the
+            // next step's score products run
             uint32_t lo[16], hi[16];
             tmem_ld16(tmem + lane_base + kColS + 16 * qt4, lo);
             tmem_ld16(tmem + lane_base + kColS + 64 + 16 * qt4, hi);
@@ -603,17 +609,23 @@ __global__ void __launch_bounds__(kUThreads, 1) bwd_umma_kernel(const __grid_con
                                     kLn2u * (__uint_as_float(lo[4 * e + 3]) + carry[4 * e + 3]));
 #pragma unroll
             for (int e = 0; e < 16; ++e) carry[e] = __uint_as_float(hi[e]);
-            __syncthreads();
-            flush_dr_rows(p, sm, h, 128 * t - 127, warp, lane);
-        } else if (t + 1 < n_steps) {
-            // the next query tile: its raw q has landed in the K1 slot (its dO in the other dO slot)
-            mma::cp_async_wait_all();
-            __syncthreads();
-            i0 += 128;
-            convert_queries(a, sm, sm + USmem::K1, i0, tid);
-            dd = dd_next;
-            l2 = l2_next;
         }
+        if (t + 1 < n_steps) {
+            mma::cp_async_wait_all();                     // the next step's operands have landed
+            if (key_cta) {
+                // the next query tile: its raw q in the K1 slot, its dO in the other dO slot
+                __syncthreads();
+                i0 += 128;
+                convert_queries(a, sm, sm + USmem::K1, i0, tid);
+                dd = dd_next;
+                l2 = l2_next;
+            }
+            fence_proxy_async_smem();
+        }
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0 && t + 1 < n_steps) issue_scores(t + 1);
+        if (!key_cta) flush_dr_rows(p, sm, h, 128 * t - 127, warp, lane);
         tc_fence_before();
     }
 
