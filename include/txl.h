@@ -386,7 +386,9 @@ txl_status txl_rel_attn_bwd_lse(int B, int L, int H, int D, int clamp_len,
  * it in fp32; then the fp32 sine or cosine: entries within 6e-7 of the exact sinusoid).  dr: device fp32 [n_rows][H][D] (as txl_rel_attn_bwd writes it);
  * dW_R: device fp32 [d_model][ld_dw], columns 0..H*D-1 written (zeroed, then partial sums over
  * ranges of distances added atomically: the fp32 summation order may differ from call to call).
- * d_model even, ld_dw >= H*D.
+ * d_model even, ld_dw >= H*D.  The products run on the tensor cores as three tf32 products per
+ * step (R and dr each split into a tf32 part and the fp32 remainder; the remainder product dropped):
+ * about 2^-21 relative error per product, fp32 accumulation.
  */
 txl_status txl_rel_pos_bwd(int n_rows, int d_model, int n_head, int d_head, const float* dr,
                            float* dW_R, int64_t ld_dw, void* stream);

@@ -16,7 +16,7 @@ CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libtxl.so")
 CHECKED_LIB = os.path.join(PKG, "libtxl_checked.so")
-SOURCES = ["txl_api.cu", "txl_attn_tc.cu", "txl_attn_persist.cu", "txl_attn_simt.cu", "txl_pos.cu", "txl_mem.cu", "txl_sched.cu", "txl_decode.cu", "txl_linear.cu", "txl_bwd.cu", "txl_table.cu", "txl_bwd_tc.cu", "txl_bwd_umma.cu", "txl_table_tc.cu"]
+SOURCES = ["txl_api.cu", "txl_attn_tc.cu", "txl_attn_persist.cu", "txl_attn_simt.cu", "txl_pos.cu", "txl_mem.cu", "txl_sched.cu", "txl_decode.cu", "txl_linear.cu", "txl_bwd.cu", "txl_table.cu", "txl_bwd_tc.cu", "txl_bwd_umma.cu", "txl_pos_bwd_tc.cu", "txl_table_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CUDA_HOME = os.environ.get("CUDA_HOME", "/usr/local/cuda")
 

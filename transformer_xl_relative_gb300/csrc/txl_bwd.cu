@@ -16,10 +16,9 @@
 //   dist  (h, delta) for distances below the clamp: dr[delta] over every (b, i)
 //   clamp (b, h, i): the pairs whose distance reaches clamp_len, added into dr[C] atomically
 //   bias  (h, d): du and dv_bias from the per-query parts
-// and the position table's backward dW_R = sum_delta R_delta^T dr[delta] with R the sinusoid.
+// and the launch of the position table's backward dW_R = sum_delta R_delta^T dr[delta]
+// (txl_pos_bwd_tc.cu).
 #include <cmath>
-
-#include <algorithm>
 
 #include <cuda_bf16.h>
 
@@ -615,113 +614,6 @@ __global__ void bwd_bias_kernel(const BwdParams p, int64_t chunk)
     atomicAdd(p.dvb + hd, sv);
 }
 
-// ---------------------------------------------------------------------------- dW_R = R^T dr
-// Block: 128 model columns m x 128 columns n = h*D + d over a share of the distances, 256 threads
-// with 8 x 8 outputs each (rows 4 ty .. + 3 and 64 + 4 ty .. + 3, columns 4 tx .. + 3 and
-// 64 + 4 tx .. + 3: float4 fragments), 16 distances per shared-memory chunk.  The block's 128
-// frequencies are computed once in double precision.  For every fourth distance d4 the angle d4 * w
-// of each column is reduced modulo 2 pi in double precision (a multiply, a rounding and an fma; the
-// SMs' fp64 path is slow, so once per four rows); an element d4 + e (e < 4) takes its angle as that
-// base plus e * w in fp32 (|angle| < pi + 3: absolute error below 6e-7) and the fp32 sine or cosine
-// of it.  The shares of the distances (blockIdx.z) add into the zeroed dW.
-constexpr int kPosBwdT = 128, kPosBwdChunk = 16;
-
-__global__ void __launch_bounds__(256) pos_bwd_kernel(PosBwdParams p)
-{
-    __shared__ __align__(16) float Rs[kPosBwdChunk][kPosBwdT];     // R^T chunk: [distance][m]
-    __shared__ __align__(16) float Gs[kPosBwdChunk][kPosBwdT];     // dr chunk: [distance][n]
-    __shared__ double Ws[kPosBwdT];
-    __shared__ float Wf[kPosBwdT];                                 // fp32 frequencies
-    __shared__ float Bs[kPosBwdChunk / 4][kPosBwdT];               // reduced angles of every fourth distance
-    const int tid = threadIdx.x;
-    const int m0 = blockIdx.y * kPosBwdT, n0 = blockIdx.x * kPosBwdT;
-    const int tx = tid & 15, ty = tid >> 4;
-    if (tid < kPosBwdT) {
-        const int k = (m0 + tid) >> 1;
-        Ws[tid] = pow(10000.0, -(2.0 * k) / static_cast<double>(p.d_model));
-        Wf[tid] = static_cast<float>(Ws[tid]);
-    }
-    float acc[8][8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e)
-#pragma unroll
-        for (int f = 0; f < 8; ++f) acc[e][f] = 0.f;
-    const int HD = p.H * p.D;
-    const bool vec = (HD & 3) == 0;
-    constexpr double kTwoPi = 6.283185307179586476925;
-    constexpr double kInvTwoPi = 0.159154943091895335768884;   // the quotient only picks the multiple of 2 pi
-    const int per = (p.n_rows + kPosBwdChunk * gridDim.z - 1) / (kPosBwdChunk * gridDim.z) * kPosBwdChunk;
-    const int d_lo = blockIdx.z * per, d_hi = min(p.n_rows, d_lo + per);
-    __syncthreads();
-    for (int d0 = d_lo; d0 < d_hi; d0 += kPosBwdChunk) {
-        // reduced angles of distances d0, d0 + 4, .. (two per thread)
-        for (int e = tid; e < (kPosBwdChunk / 4) * kPosBwdT; e += 256) {
-            const int q4 = e / kPosBwdT, cc = e % kPosBwdT;
-            const double x = static_cast<double>(d0 + 4 * q4) * Ws[cc];
-            Bs[q4][cc] = static_cast<float>(fma(-rint(x * kInvTwoPi), kTwoPi, x));
-        }
-        // the dr rows of the chunk (zero past the share or past n)
-#pragma unroll
-        for (int x = 0; x < 2; ++x) {
-            const int e = tid + 256 * x;                       // 512 float4 of 16 x 128
-            const int rr = e >> 5, c4 = (e & 31) * 4;
-            const int delta = d0 + rr, n = n0 + c4;
-            float4 g = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (delta < d_hi) {
-                const float* src = p.dr + static_cast<int64_t>(delta) * HD + n;
-                if (vec && n + 3 < HD) {
-                    g = __ldg(reinterpret_cast<const float4*>(src));
-                } else {
-                    if (n < HD) g.x = __ldg(src);
-                    if (n + 1 < HD) g.y = __ldg(src + 1);
-                    if (n + 2 < HD) g.z = __ldg(src + 2);
-                    if (n + 3 < HD) g.w = __ldg(src + 3);
-                }
-            }
-            *reinterpret_cast<float4*>(&Gs[rr][c4]) = g;
-        }
-        __syncthreads();
-#pragma unroll
-        for (int x = 0; x < (kPosBwdChunk * kPosBwdT) / 256; ++x) {
-            const int e = tid + 256 * x;
-            const int rr = e / kPosBwdT, cc = e % kPosBwdT;
-            const int delta = d0 + rr, m = m0 + cc;
-            float rv = 0.f;
-            if (delta < d_hi && m < p.d_model) {
-                const float ang = fmaf(static_cast<float>(rr & 3), Wf[cc], Bs[rr >> 2][cc]);
-                rv = (m & 1) ? cosf(ang) : sinf(ang);
-            }
-            Rs[rr][cc] = rv;
-        }
-        __syncthreads();
-#pragma unroll 4
-        for (int rr = 0; rr < kPosBwdChunk; ++rr) {
-            const float4 a0 = *reinterpret_cast<const float4*>(&Rs[rr][4 * ty]);
-            const float4 a1 = *reinterpret_cast<const float4*>(&Rs[rr][64 + 4 * ty]);
-            const float4 b0 = *reinterpret_cast<const float4*>(&Gs[rr][4 * tx]);
-            const float4 b1 = *reinterpret_cast<const float4*>(&Gs[rr][64 + 4 * tx]);
-            const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-#pragma unroll
-                for (int f = 0; f < 8; ++f) acc[e][f] = fmaf(av[e], bv[f], acc[e][f]);
-        }
-        __syncthreads();
-    }
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        const int m = m0 + (e < 4 ? 4 * ty + e : 64 + 4 * ty + e - 4);
-        if (m >= p.d_model) continue;
-        float* row = p.dW + static_cast<int64_t>(m) * p.ld_dw;
-#pragma unroll
-        for (int f = 0; f < 8; ++f) {
-            const int n = n0 + (f < 4 ? 4 * tx + f : 64 + 4 * tx + f - 4);
-            if (n < HD) atomicAdd(row + n, acc[e][f]);
-        }
-    }
-}
-
 // The bias reduction: du and dv_bias from the per-query parts in the workspace.
 cudaError_t launch_bias(const BwdParams& p, cudaStream_t s)
 {
@@ -791,23 +683,13 @@ cudaError_t launch_rel_attn_bwd(const BwdParams& p, txl_dtype dtype, cudaStream_
 cudaError_t launch_pos_bwd(const PosBwdParams& p, cudaStream_t s)
 {
     if (p.d_model == 0) return cudaSuccess;
-    if (p.n_rows == 0)
-        return cudaMemset2DAsync(p.dW, static_cast<size_t>(p.ld_dw) * sizeof(float), 0,
-                                 sizeof(float) * p.H * p.D, p.d_model, s);
     const cudaError_t e = cudaMemset2DAsync(p.dW, static_cast<size_t>(p.ld_dw) * sizeof(float), 0,
                                             sizeof(float) * p.H * p.D, p.d_model, s);
-    if (e != cudaSuccess) return e;
-    // the distances split over enough blocks per output tile for about two blocks per SM, each
-    // share at least four chunks
-    const int tiles = ((p.H * p.D + kPosBwdT - 1) / kPosBwdT) * ((p.d_model + kPosBwdT - 1) / kPosBwdT);
+    if (e != cudaSuccess || p.n_rows == 0) return e;
     int sms = 0, dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        sms = 148;
-    int splits = (2 * sms + tiles - 1) / tiles;
-    splits = std::max(1, std::min(splits, p.n_rows / (4 * kPosBwdChunk)));
-    dim3 grid((p.H * p.D + kPosBwdT - 1) / kPosBwdT, (p.d_model + kPosBwdT - 1) / kPosBwdT, splits);
-    pos_bwd_kernel<<<grid, 256, 0, s>>>(p);
-    return cudaGetLastError();
+        return cudaErrorUnknown;
+    return launch_pos_bwd_tc(p, sms, s);
 }
 
 }  // namespace txl

@@ -194,6 +194,8 @@ cudaError_t launch_table_tc(const TableParams& p, cudaStream_t s);
 
 cudaError_t launch_table_attn(const TableParams& p, txl_dtype dtype, cudaStream_t s);
 cudaError_t launch_pos_bwd(const PosBwdParams& p, cudaStream_t s);
+// dW_R = R^T dr on the tensor cores (dW zeroed first by the caller)
+cudaError_t launch_pos_bwd_tc(const PosBwdParams& p, int sm_count, cudaStream_t s);
 
 // ---------------------------------------------------------------- projections (tcgen05 GEMM)
 struct LinearParams {
