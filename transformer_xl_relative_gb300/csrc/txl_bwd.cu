@@ -668,12 +668,16 @@ cudaError_t launch_rel_attn_bwd(const BwdParams& p, txl_dtype dtype, cudaStream_
         const size_t cur = static_cast<size_t>(a.B) * a.L * a.H * a.D * sizeof(float);
         cudaError_t e = cudaMemsetAsync(p.dr, 0, static_cast<size_t>(p.n_rows) * a.H * a.D * sizeof(float), s);
         if (bwd_umma_eligible(p, dtype)) {
+            // du and dv_bias come out of the gradient kernel itself
+            const size_t hd = static_cast<size_t>(a.H) * a.D * sizeof(float);
+            if (e == cudaSuccess) e = cudaMemsetAsync(p.du, 0, hd, s);
+            if (e == cudaSuccess) e = cudaMemsetAsync(p.dvb, 0, hd, s);
             if (e == cudaSuccess) e = launch_bwd_umma(p, s);
-        } else {
-            if (e == cudaSuccess) e = cudaMemsetAsync(p.dk, 0, cur, s);
-            if (e == cudaSuccess) e = cudaMemsetAsync(p.dv, 0, cur, s);
-            if (e == cudaSuccess) e = launch_bwd_tc(p, s);
+            return e;
         }
+        if (e == cudaSuccess) e = cudaMemsetAsync(p.dk, 0, cur, s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(p.dv, 0, cur, s);
+        if (e == cudaSuccess) e = launch_bwd_tc(p, s);
         if (e == cudaSuccess) e = launch_bias(p, s);
         return e;
     }

@@ -17,7 +17,8 @@
 //    local, window column c = i - j + 127 in [0, 255) over position rows 128 t - 127 + c).  It
 //    accumulates dq_ac = dS K and dq_bd = G R_win in TMEM over the sweep, where G, dS scattered
 //    by distance (G[i][i - j + 127] = dS_ij), sits in shared memory as the A operand of that
-//    product and, read transposed, of dr_win = G^T Qc''.  The window's lower 128 rows are the
+//    product and, read transposed, of dr_win = G^T Qc''.  Its rows' sums of dq_ac and dq_bd are
+//    added into du and dv_bias.  The window's lower 128 rows are the
 //    upper 128 of the tile before, so every block of 128 distance rows receives the products of
 //    two consecutive tiles and is added to dr (fp32 atomics) once.
 //  * a key CTA owns a key tile of the current segment and sweeps the query tiles that see it,
@@ -667,21 +668,45 @@ __global__ void __launch_bounds__(kUThreads, 1) bwd_umma_kernel(const __grid_con
                 if (lane == 0) atomicAdd(dst + e, kLn2u * part);
             }
         }
-        // dq and the per-query parts of du (dS K) and dv_bias (dS r)
+        // dq; du (sum of the dq_ac rows) and dv_bias (sum of the dq_bd rows) over this tile's queries
         const int i = i0 + li;
+        const float scale = a.scale;
+        float part[32];                                   // scale dq_ac, then scale dq_bd, of this row
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            part[e] = i < L ? scale * __uint_as_float(qa[e]) : 0.f;
+            part[16 + e] = i < L ? scale * __uint_as_float(qb[e]) : 0.f;
+        }
         if (i < L) {
             const int64_t row = ((static_cast<int64_t>(b) * L + i) * a.H + h) * 64 + 16 * qt4;
-            const float scale = a.scale;
 #pragma unroll
-            for (int e = 0; e < 16; e += 4) {
-                const float4 xa = make_float4(scale * __uint_as_float(qa[e]), scale * __uint_as_float(qa[e + 1]),
-                                              scale * __uint_as_float(qa[e + 2]), scale * __uint_as_float(qa[e + 3]));
-                const float4 xb = make_float4(scale * __uint_as_float(qb[e]), scale * __uint_as_float(qb[e + 1]),
-                                              scale * __uint_as_float(qb[e + 2]), scale * __uint_as_float(qb[e + 3]));
-                *reinterpret_cast<float4*>(p.dq + row + e) = make_float4(xa.x + xb.x, xa.y + xb.y, xa.z + xb.z, xa.w + xb.w);
-                *reinterpret_cast<float4*>(p.pac + row + e) = xa;
-                *reinterpret_cast<float4*>(p.pbd + row + e) = xb;
+            for (int e = 0; e < 16; e += 4)
+                *reinterpret_cast<float4*>(p.dq + row + e) =
+                    make_float4(part[e] + part[16 + e], part[e + 1] + part[17 + e], part[e + 2] + part[18 + e],
+                                part[e + 3] + part[19 + e]);
+        }
+        // the warp's 32 rows summed by a transposing butterfly (lane l ends with the sum of value l),
+        // then the four warps of each column quarter through shared memory
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) {
+            const bool up = (lane & o) != 0;
+#pragma unroll
+            for (int k = 0; k < o; ++k) {
+                const float keep = up ? part[k + o] : part[k];
+                const float send = up ? part[k] : part[k + o];
+                part[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
             }
+        }
+        __syncthreads();                                  // X's dr rows have been added
+        float* red = reinterpret_cast<float*>(sm + USmem::X);    // [quarter][lane quarter][32]
+        red[(qt4 * 4 + (warp & 3)) * 32 + lane] = part[0];
+        __syncthreads();
+        if (tid < 128) {
+            const int q = tid >> 5, v = tid & 31;
+            const float sum = red[(q * 4) * 32 + v] + red[(q * 4 + 1) * 32 + v] + red[(q * 4 + 2) * 32 + v] +
+                              red[(q * 4 + 3) * 32 + v];
+            float* dst = v < 16 ? p.du : p.dvb;
+            atomicAdd(dst + h * 64 + 16 * q + (v & 15), sum);
         }
     } else {
         // dv and dk of the owned keys (TMEM lane li = key jk + li)
@@ -724,11 +749,11 @@ bool bwd_umma_eligible(const BwdParams& p, txl_dtype dtype)
     if (!p.lse_given || !bwd_tc_eligible(p, dtype)) return false;
     if (2 * ((a.L + 127) / 128) > 65535) return false;
     return al16u(a.out) && st8u(a.o_sb) && st8u(a.o_st) && st8u(a.o_sh) && al16u(p.dq) && al16u(p.dk) &&
-           al16u(p.dv) && al16u(p.dr) && al16u(p.pac) && al16u(p.pbd);
+           al16u(p.dv) && al16u(p.dr);
 }
 
-// D_i of every row into the workspace (dd), then the gradient kernel: dq, dk, dv, pac, pbd are
-// written; dr must be zero on entry (atomic accumulation).
+// D_i of every row into the workspace (dd), then the gradient kernel: dq, dk, dv are written; dr,
+// du and dv_bias must be zero on entry (atomic accumulation).
 cudaError_t launch_bwd_umma(const BwdParams& p, cudaStream_t s)
 {
     static bool attr_done = false;
