@@ -8,7 +8,8 @@
 //  * its threads generate the chunk of R^T with the arithmetic of the position table (frequencies in
 //    double precision, here as exp(-2k ln(10000) / d_model), the angle of every fourth distance
 //    reduced modulo 2 pi in double precision, the three after it offset in fp32, the fp32 sine or
-//    cosine: entries within 6e-7 of the exact sinusoid), and load the chunk of dr;
+//    cosine, both from one sincosf: entries within 6e-7 of the exact sinusoid), and load the chunk
+//    of dr;
 //  * both are split into tf32 parts, x = hi + lo with hi = x rounded to tf32 and lo = x - hi (exact
 //    in fp32), and R_hi dr_hi + R_hi dr_lo + R_lo dr_hi run as UMMAs (A: R^T and B: dr^T, both
 //    K-major, the distances along the 128-byte swizzled rows, 32 fp32 per row) into one 128 x 256
@@ -85,13 +86,12 @@ __global__ void __launch_bounds__(kPBThreads, 1) pos_bwd_tc_kernel(const __grid_
     constexpr double kInvTwoPi = 0.159154943091895335768884;   // the quotient only picks the multiple of 2 pi
     constexpr uint32_t idesc = idesc_tf32(kPBM, kPBN, 0, 0);
 
-    // generation roles.  A: row ml = 2 (tid mod 64) + (tid / 64 mod 2), so that the lanes of a warp
-    // share the row parity (a warp takes only sines or only cosines), distances 8 (tid / 128) .. + 7 of
-    // the chunk; B: row tid mod 256 (column n0 + tid mod 256 of dr), distances 16 (tid / 256) .. + 15
-    // (each load coalesced across the warp)
-    const int ml = 2 * (tid & 63) + ((tid >> 6) & 1), aq = tid >> 7;
-    const int m = m0 + ml;
-    const bool cosine = (m & 1) != 0;
+    // generation roles.  A: the frequency kl = tid mod 64 of the tile (columns 2 kl, 2 kl + 1: its sine and
+    // cosine from one sincosf), distances 4 (tid / 64) .. + 3 of the chunk; B: row tid mod 256 (column
+    // n0 + tid mod 256 of dr), distances 16 (tid / 256) .. + 15 (each load coalesced across the warp)
+    const int kl = tid & 63, ag = tid >> 6;
+    const int ms = 2 * kl;                                // the sine's row; the cosine's is ms + 1
+    const bool m_in = m0 + ms < p.d_model;
     const int bl = tid & (kPBN - 1), bq = tid >> 8;
     const int nt = n0 + bl;
     for (int c = 0; c < nch; ++c) {
@@ -102,27 +102,28 @@ __global__ void __launch_bounds__(kPBThreads, 1) pos_bwd_tc_kernel(const __grid_
             __syncthreads();
         }
         const int d0 = d_lo + c * kPBChunk;
-        // ---- R^T chunk: A[ml][dl], dl = 8 aq + 4 q + e (an anchor distance every four)
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            const int dl = 8 * aq + 4 * q;
+        // ---- R^T chunk: A[ms][dl] = sin, A[ms + 1][dl] = cos, dl = 4 ag + e (anchor distance 4 ag)
+        {
+            const int dl = 4 * ag;
             const int da = d0 + dl;
-            const double x = static_cast<double>(da) * Ws[ml];
+            const double x = static_cast<double>(da) * Ws[ms];
             const float base = static_cast<float>(fma(-rint(x * kInvTwoPi), kTwoPi, x));
-            float hi[4], lo[4];
+            float sh[4], sl[4], ch[4], cl[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                float rv = 0.f;
-                if (da + e < d_hi && m < p.d_model) {
-                    const float ang = fmaf(static_cast<float>(e), Wf[ml], base);
-                    rv = cosine ? cosf(ang) : sinf(ang);
-                }
-                hi[e] = round_tf32(rv);
-                lo[e] = rv - hi[e];
+                float sv = 0.f, cv = 0.f;
+                if (da + e < d_hi && m_in) sincosf(fmaf(static_cast<float>(e), Wf[ms], base), &sv, &cv);
+                sh[e] = round_tf32(sv);
+                sl[e] = sv - sh[e];
+                ch[e] = round_tf32(cv);
+                cl[e] = cv - ch[e];
             }
-            const uint32_t off = ml * 128 + ((((dl >> 2) ^ ml) & 7) << 4);
-            *reinterpret_cast<float4*>(st + off) = make_float4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<float4*>(st + kATile + off) = make_float4(lo[0], lo[1], lo[2], lo[3]);
+            const uint32_t offs = ms * 128 + ((((dl >> 2) ^ ms) & 7) << 4);
+            const uint32_t offc = (ms + 1) * 128 + ((((dl >> 2) ^ (ms + 1)) & 7) << 4);
+            *reinterpret_cast<float4*>(st + offs) = make_float4(sh[0], sh[1], sh[2], sh[3]);
+            *reinterpret_cast<float4*>(st + kATile + offs) = make_float4(sl[0], sl[1], sl[2], sl[3]);
+            *reinterpret_cast<float4*>(st + offc) = make_float4(ch[0], ch[1], ch[2], ch[3]);
+            *reinterpret_cast<float4*>(st + kATile + offc) = make_float4(cl[0], cl[1], cl[2], cl[3]);
         }
         // ---- dr^T chunk: B[bl][dl] = dr[d0 + dl][n0 + bl], dl = 16 bq + 4 q + e
         {
