@@ -196,3 +196,34 @@ def test_saved_statistics_need_the_fused_kernel(txl):
     lse = torch.empty(B, L, H, device="cuda")
     with pytest.raises(RuntimeError, match="txl_rel_attn_fwd_lse"):
         txl.rel_attn_fwd(q, None, k, v, u, u, r, L, 1000, out, lse=lse)
+
+
+def test_backward_fallback_with_unaligned_output(txl):
+    """An output view 8 bytes past a 16-byte boundary: the tcgen05 gradient kernel declines (it reads out
+    and writes the gradients with 16-byte accesses) and the mma.sync kernel takes the call; its gradients
+    match the oracle like the main path's."""
+    B, H, D, dm, L, M, valid, C = 1, 2, 64, 128, 96, 64, 50, 1000
+    cfg = txl_inputs.custom(B=B, H=H, D=D, d_model=dm, L=L, M=M, clamp_len=C, dtype="bf16", seed=811)
+    case = txl_inputs.make_case(cfg)
+    dO = txl_inputs.make_qkv(cfg, seed=812, L=L, T=1)[0]
+    q, k, v = (to_dev(case[n]) for n in ("q", "k", "v"))
+    n_rows = min(M + L, C + 1)
+    r = torch.empty(n_rows, H, D, dtype=torch.bfloat16, device="cuda")
+    txl.rel_pos_gen(case["W_R"].cuda(), r, n_rows, dm, H, D)
+    mem = txl.Memory(k[:, :M].contiguous(), v[:, :M].contiguous(), 0, valid)
+    u, vb = case["u"].cuda(), case["vb"].cuda()
+    base = torch.zeros(B * L * H * D + 8, dtype=torch.bfloat16, device="cuda")
+    out = base[4:4 + B * L * H * D].view(B, L, H, D)          # 8 bytes off alignment
+    assert out.data_ptr() % 16 == 8
+    txl.rel_attn_fwd(q, mem, k[:, M:], v[:, M:], u, vb, r, n_rows, C, out)
+    g = txl.rel_attn_bwd(q, mem, k[:, M:], v[:, M:], u, vb, r, n_rows, C, out, to_dev(dO))
+    torch.cuda.synchronize()
+    ref = oracle.rel_attn_bwd(case["q"], case["k"], case["v"], case["u"], case["vb"], case["W_R"][:, :H * D], M, valid,
+                              C, dO)
+    tol = RTOL["bf16"]
+    _close(g["dq"].cpu().numpy(), ref["dq"], tol, "dq")
+    _close(g["dk_cur"].cpu().numpy(), ref["dk"][:, M:], tol, "dk")
+    _close(g["dv_cur"].cpu().numpy(), ref["dv"][:, M:], tol, "dv")
+    _close(g["du"].cpu().numpy(), ref["du"], tol, "du")
+    _close(g["dv_bias"].cpu().numpy(), ref["dvb"], tol, "dv_bias")
+    _close(g["dr"].cpu().numpy(), ref["dr"], tol, "dr")
