@@ -336,6 +336,15 @@ txl_status txl_rel_attn_bwd(int B, int L, int H, int D, int clamp_len,
                             float* dr, txl_dtype dtype, void* workspace, size_t workspace_bytes,
                             void* stream);
 
+/* Which gradient kernel txl_rel_attn_bwd and txl_rel_attn_bwd_lse would run for these arguments
+ * (the addresses of out, d_out and the gradient buffers count: their alignment chooses the kernel):
+ * 1 = tcgen05 kernel, 2 = mma.sync kernel, 3 = SIMT kernels, or a negative txl_status if the
+ * arguments are rejected.  No launch. */
+int txl_rel_attn_bwd_path(int B, int L, int H, int D, const txl_view* q, const txl_mem* mem,
+                          const txl_view* k_cur, const txl_view* v_cur, const void* r, int64_t ld_r,
+                          const txl_view* out, const txl_view* d_out, const float* dq, const float* dk_cur,
+                          const float* dv_cur, const float* dr, txl_dtype dtype);
+
 /* Bytes of device workspace txl_rel_attn_bwd needs: B*L*H*(2 + 2*D)*4 (0 for an empty shape). */
 size_t txl_rel_attn_bwd_workspace_size(int B, int L, int H, int D);
 

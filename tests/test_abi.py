@@ -88,6 +88,30 @@ def test_path_selection(native):
     assert _path(native, wp=128, valid=128) == -native.TXL_ERR_INVALID_ARG   # wp >= M
 
 
+def _bwd_path(native, B=2, L=200, H=4, D=64, M=128, wp=0, valid=128, dtype=1, sh=None, out_off=0, grad_off=0,
+              ld_r=64):
+    sh = sh or D
+    V = native.TxlView
+    q = V(FAKE, L * H * sh, H * sh, sh)
+    kc = V(FAKE, (M + L) * H * sh, H * sh, sh)
+    out = V(FAKE + out_off, L * H * sh, H * sh, sh)
+    mem = native.TxlMem(FAKE, FAKE, (M + L) * H * sh, H * sh, sh, B, M, H, D, dtype, wp, valid)
+    return native.load().txl_rel_attn_bwd_path(B, L, H, D, ctypes.byref(q), ctypes.byref(mem), ctypes.byref(kc),
+                                               ctypes.byref(kc), FAKE, ld_r, ctypes.byref(out), ctypes.byref(q),
+                                               FAKE + grad_off, FAKE, FAKE, FAKE, dtype)
+
+
+def test_backward_path_selection(native):
+    assert _bwd_path(native) == 1                             # bf16, D 64, aligned: tcgen05 kernel
+    assert _bwd_path(native, out_off=8) == 2                  # output off 16-byte alignment: mma.sync
+    assert _bwd_path(native, grad_off=4) == 2                 # dq off 16-byte alignment: mma.sync
+    assert _bwd_path(native, M=256, wp=128, valid=200) == 1   # ring aligned to 128
+    assert _bwd_path(native, M=256, wp=64, valid=256) == 2    # ring the fused forward declines
+    assert _bwd_path(native, dtype=0) == 3                    # fp32: SIMT
+    assert _bwd_path(native, D=32, ld_r=32) == 3              # d_head 32: SIMT
+    assert _bwd_path(native, wp=128, valid=128) == -native.TXL_ERR_INVALID_ARG   # wp >= M
+
+
 def _table_path(native, B=2, L=300, H=4, D=64, max_len=512, dtype=1, sh=None, masked=False, ld_r=64):
     sh = sh or D
     V = native.TxlView

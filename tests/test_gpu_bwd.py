@@ -54,6 +54,10 @@ BWD = [
     (1, 2, 64, 128, 384, 384, 384, 0, 1000, "bf16", 0),
     (1, 2, 64, 128, 70, 64, 64, 0, 40, "bf16", 0),
     (1, 2, 64, 128, 40, 30, 30, 0, 1000, "bf16", 68),
+    # the tcgen05 gradient kernel (the fused forward takes the inputs: a ring's write pointer and length
+    # multiples of 128): a wrapped ring with part of the memory valid, ragged query tiles, a clamp
+    # inside the window of the third key tile
+    (2, 2, 64, 128, 200, 256, 200, 128, 300, "bf16", 0),
 ]
 
 
@@ -82,6 +86,13 @@ def test_backward_matches_oracle(txl, shape):
     out = to_dev(torch.zeros_like(case["q"]), cfg.hs)
     txl.rel_attn_fwd(q, mem, k[:, M:], v[:, M:], u, vb, r, n_rows, C, out)
     g = txl.rel_attn_bwd(q, mem, k[:, M:], v[:, M:], u, vb, r, n_rows, C, out, g_dev)
+    path = txl.rel_attn_bwd_path(q, mem, k[:, M:], v[:, M:], r, out, g_dev, g)
+    if dtype == "f32" or D != 64 or hs:
+        assert path == 3
+    elif M > 0 and wp != 0 and (M % 128 or wp % 128):
+        assert path == 2                                   # the fused forward declines the ring
+    else:
+        assert path == 1
     dW = txl.rel_pos_bwd(g["dr"], dm)
     torch.cuda.synchronize()
     ref = oracle.rel_attn_bwd(case["q"], case["k"], case["v"], case["u"], case["vb"], case["W_R"][:, :H * D], M, valid,
@@ -128,6 +139,7 @@ def test_backward_large_workload_sampled(txl):
     out = torch.empty_like(q)
     txl.rel_attn_fwd(q, mem, k[:, M:], v[:, M:], u, vb, r, n_rows, C, out)
     g = txl.rel_attn_bwd(q, mem, k[:, M:], v[:, M:], u, vb, r, n_rows, C, out, to_dev(dO))
+    assert txl.rel_attn_bwd_path(q, mem, k[:, M:], v[:, M:], r, out, to_dev(dO), g) == 1
     torch.cuda.synchronize()
     pairs = [(0, 0), (7, 11), (15, 15)]
     ref = oracle.rel_attn_bwd(case["q"], case["k"], case["v"], case["u"], case["vb"], case["W_R"][:, :H * D], M, M,
@@ -217,6 +229,7 @@ def test_backward_fallback_with_unaligned_output(txl):
     assert out.data_ptr() % 16 == 8
     txl.rel_attn_fwd(q, mem, k[:, M:], v[:, M:], u, vb, r, n_rows, C, out)
     g = txl.rel_attn_bwd(q, mem, k[:, M:], v[:, M:], u, vb, r, n_rows, C, out, to_dev(dO))
+    assert txl.rel_attn_bwd_path(q, mem, k[:, M:], v[:, M:], r, out, to_dev(dO), g) == 2
     torch.cuda.synchronize()
     ref = oracle.rel_attn_bwd(case["q"], case["k"], case["v"], case["u"], case["vb"], case["W_R"][:, :H * D], M, valid,
                               C, dO)

@@ -10,6 +10,7 @@ from .api import (  # noqa: F401
     linear,
     mem_push,
     rel_attn_bwd,
+    rel_attn_bwd_path,
     rel_attn_decode,
     rel_attn_decode_path,
     rel_attn_decode_workspace_size,

@@ -195,6 +195,17 @@ def rel_attn_decode_path(q, mem, k_cur, v_cur, r, out) -> int:
                                            dtype_code(q))
 
 
+def rel_attn_bwd_path(q, mem, k_cur, v_cur, r, out, d_out, g: dict) -> int:
+    """1 = tcgen05 gradient kernel, 2 = mma.sync, 3 = SIMT (txl_rel_attn_bwd_path), for the gradient
+    buffers g (as rel_attn_bwd returns them: dq, dk_cur, dv_cur, dr)."""
+    (B, L, H, D), memc, vq, vk, vv, vo = _attn_args(q, mem, k_cur, v_cur, r, out)
+    vg = view(d_out)
+    return _lib().txl_rel_attn_bwd_path(B, L, H, D, ctypes.byref(vq), memc, ctypes.byref(vk), ctypes.byref(vv),
+                                        r.data_ptr(), r.stride(1), ctypes.byref(vo), ctypes.byref(vg),
+                                        g["dq"].data_ptr(), g["dk_cur"].data_ptr(), g["dv_cur"].data_ptr(),
+                                        g["dr"].data_ptr(), dtype_code(q))
+
+
 def mem_push(mem: Memory, k_new: torch.Tensor, v_new: torch.Tensor, stream=None) -> Memory:
     """Append k_new/v_new [B, L, H, D] to the FIFO memory (txl_mem_push)."""
     vk, vv = view(k_new), view(v_new)

@@ -826,6 +826,56 @@ size_t txl_rel_attn_bwd_workspace_size(int B, int L, int H, int D)
     return rows * 2 * sizeof(float) + rows * D * 2 * sizeof(float);
 }
 
+namespace {
+
+// The gradient kernels' parameters from a backward call's arguments (checked by the caller).
+BwdParams bwd_params(int B, int L, int H, int D, int clamp_len, const txl_view* q, const txl_mem* mem,
+                     const txl_view* k_cur, const txl_view* v_cur, const float* u, const float* v_bias, const void* r,
+                     int64_t ld_r, int n_rows, float scale, const txl_view* out, const txl_view* d_out, float* dq,
+                     float* dk_cur, float* dv_cur, float* du, float* dv_bias, float* dr)
+{
+    const int M = (mem && mem->M > 0) ? mem->M : 0;
+    const int valid = M > 0 ? mem->valid : 0;
+    BwdParams p;
+    std::memset(&p, 0, sizeof(p));
+    AttnSimtParams& a = p.a;
+    a.q = q->ptr; a.q_sb = q->stride_b; a.q_st = q->stride_t; a.q_sh = q->stride_h;
+    if (M > 0) {
+        a.kmem = mem->k; a.vmem = mem->v;
+        a.m_sb = mem->stride_b; a.m_st = mem->stride_t; a.m_sh = mem->stride_h;
+    }
+    a.kcur = k_cur->ptr; a.kc_sb = k_cur->stride_b; a.kc_st = k_cur->stride_t; a.kc_sh = k_cur->stride_h;
+    a.vcur = v_cur->ptr; a.vc_sb = v_cur->stride_b; a.vc_st = v_cur->stride_t; a.vc_sh = v_cur->stride_h;
+    a.out = out->ptr; a.o_sb = out->stride_b; a.o_st = out->stride_t; a.o_sh = out->stride_h;
+    a.u = u; a.vb = v_bias;
+    a.r = r; a.r_row = static_cast<int64_t>(H) * ld_r; a.r_head = ld_r;
+    a.B = B; a.L = L; a.H = H; a.D = D; a.M = M; a.lo = M - valid; a.wp = M > 0 ? mem->wp : 0; a.C = clamp_len;
+    a.scale = scale;
+    p.dout = d_out->ptr; p.g_sb = d_out->stride_b; p.g_st = d_out->stride_t; p.g_sh = d_out->stride_h;
+    p.dq = dq; p.dk = dk_cur; p.dv = dv_cur; p.du = du; p.dvb = dv_bias; p.dr = dr; p.n_rows = n_rows;
+    return p;
+}
+
+}  // namespace
+
+int txl_rel_attn_bwd_path(int B, int L, int H, int D, const txl_view* q, const txl_mem* mem, const txl_view* k_cur,
+                          const txl_view* v_cur, const void* r, int64_t ld_r, const txl_view* out,
+                          const txl_view* d_out, const float* dq, const float* dk_cur, const float* dv_cur,
+                          const float* dr, txl_dtype dtype)
+{
+    const txl_status st = check_attn(B, L, H, D, q, mem, k_cur, v_cur, r, ld_r, out, dtype);
+    if (st != TXL_OK) return -static_cast<int>(st);
+    if (!view_ok(d_out) || !dq || !dk_cur || !dv_cur || !dr) return -static_cast<int>(TXL_ERR_INVALID_ARG);
+    static const float bias[1] = {0.f};
+    BwdParams p = bwd_params(B, L, H, D, 0, q, mem, k_cur, v_cur, bias, bias, r, ld_r, 1, 1.f, out, d_out,
+                             const_cast<float*>(dq), const_cast<float*>(dk_cur), const_cast<float*>(dv_cur), nullptr,
+                             nullptr, const_cast<float*>(dr));
+    if (!bwd_tc_eligible(p, dtype)) return 3;
+    if (!attn_tc_eligible(B, L, H, D, q, mem, k_cur, v_cur, r, ld_r, dtype)) return 2;
+    p.lse_given = 1;
+    return bwd_umma_eligible(p, dtype) ? 1 : 2;
+}
+
 txl_status txl_rel_attn_bwd(int B, int L, int H, int D, int clamp_len, const txl_view* q, const txl_mem* mem,
                             const txl_view* k_cur, const txl_view* v_cur, const float* u, const float* v_bias,
                             const void* r, int64_t ld_r, int n_rows, float scale, const txl_view* out,
@@ -867,23 +917,9 @@ txl_status txl_rel_attn_bwd_lse(int B, int L, int H, int D, int clamp_len, const
     if (!workspace || workspace_bytes < need) return TXL_ERR_WORKSPACE;
     if (!a16(workspace)) return TXL_ERR_ALIGNMENT;
     if (scale <= 0.f) scale = 1.0f / std::sqrt(static_cast<float>(D));
-    BwdParams p;
-    std::memset(&p, 0, sizeof(p));
-    AttnSimtParams& a = p.a;
-    a.q = q->ptr; a.q_sb = q->stride_b; a.q_st = q->stride_t; a.q_sh = q->stride_h;
-    if (M > 0) {
-        a.kmem = mem->k; a.vmem = mem->v;
-        a.m_sb = mem->stride_b; a.m_st = mem->stride_t; a.m_sh = mem->stride_h;
-    }
-    a.kcur = k_cur->ptr; a.kc_sb = k_cur->stride_b; a.kc_st = k_cur->stride_t; a.kc_sh = k_cur->stride_h;
-    a.vcur = v_cur->ptr; a.vc_sb = v_cur->stride_b; a.vc_st = v_cur->stride_t; a.vc_sh = v_cur->stride_h;
-    a.out = out->ptr; a.o_sb = out->stride_b; a.o_st = out->stride_t; a.o_sh = out->stride_h;
-    a.u = u; a.vb = v_bias;
-    a.r = r; a.r_row = static_cast<int64_t>(H) * ld_r; a.r_head = ld_r;
-    a.B = B; a.L = L; a.H = H; a.D = D; a.M = M; a.lo = M - valid; a.wp = M > 0 ? mem->wp : 0; a.C = clamp_len;
-    a.scale = scale;
-    p.dout = d_out->ptr; p.g_sb = d_out->stride_b; p.g_st = d_out->stride_t; p.g_sh = d_out->stride_h;
-    p.dq = dq; p.dk = dk_cur; p.dv = dv_cur; p.du = du; p.dvb = dv_bias; p.dr = dr; p.n_rows = n_rows;
+    BwdParams p = bwd_params(B, L, H, D, clamp_len, q, mem, k_cur, v_cur, u, v_bias, r, ld_r, n_rows, scale, out,
+                             d_out, dq, dk_cur, dv_cur, du, dv_bias, dr);
+    (void)valid;
     const size_t rows = static_cast<size_t>(B) * L * H;
     float* ws = static_cast<float*>(workspace);
     p.lse = ws;

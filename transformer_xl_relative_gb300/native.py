@@ -27,6 +27,7 @@ EXPORTS = (
     "txl_checked_build", "txl_range_errors", "txl_range_errors_clear", "txl_selftest_range_check",
     "txl_rel_attn_bwd", "txl_rel_attn_bwd_workspace_size", "txl_rel_pos_bwd", "txl_rel_attn_table_fwd",
     "txl_rel_attn_table_path", "txl_rel_attn_decode_path", "txl_rel_attn_fwd_lse", "txl_rel_attn_bwd_lse",
+    "txl_rel_attn_bwd_path",
 )
 
 
@@ -118,6 +119,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.txl_rel_attn_bwd_lse.argtypes = [i, i, i, i, i, V, Mp, V, V, vp, vp, vp, i64, i, fp, V, V, vp,
                                          vp, vp, vp, vp, vp, vp, i, vp, ctypes.c_size_t, vp]
     lib.txl_rel_attn_bwd_lse.restype = i
+    lib.txl_rel_attn_bwd_path.argtypes = [i, i, i, i, V, Mp, V, V, vp, i64, V, V, vp, vp, vp, vp, i]
+    lib.txl_rel_attn_bwd_path.restype = i
     lib.txl_rel_attn_bwd_workspace_size.argtypes = [i, i, i, i]
     lib.txl_rel_attn_bwd_workspace_size.restype = ctypes.c_size_t
     lib.txl_rel_pos_bwd.argtypes = [i, i, i, i, vp, vp, i64, vp]
