@@ -141,10 +141,10 @@ def _barrier(world: int):
         dist.barrier()
 
 
-def _profile_traffic(kernel_src: str):
-    """DRAM bytes per launch of the fused kernel from the committed ncu summary, if it was taken
-    on the current kernel source (sha256 recorded next to it); else None."""
-    path = os.path.join(ROOT, "profiles", "rel_attn_fwd_large.json")
+def _profile_traffic(kernel_src: str, summary: str = "rel_attn_fwd_large.json"):
+    """DRAM bytes per launch of a kernel from its committed ncu summary, if it was taken on the
+    current kernel source (sha256 recorded next to it); else None."""
+    path = os.path.join(ROOT, "profiles", summary)
     try:
         with open(path) as f:
             d = json.load(f)
@@ -660,7 +660,10 @@ def bench_backward(txl, device, stream, rank, args):
             "us_per_call": t_us, "us_attn_bwd": t_attn, "us_pos_bwd": t_pos,
             "us_attn_bwd_without_saved_lse": t_attn_rec,
             "algorithmic_flops_per_call": f_attn + f_pos, "tflops": (f_attn + f_pos) / (t_us * 1e-6) / 1e12,
-            "roofline": {"kernel": "txl_rel_attn_bwd_lse (bwd_rowdot_kernel + bwd_umma_kernel, tcgen05 with TMEM accumulators, + bias reduction)",
+            "roofline": {"kernel": "txl_rel_attn_bwd_lse (bwd_rowdot_kernel + bwd_umma_kernel, tcgen05 with TMEM accumulators)",
+                         "traffic": _profile_traffic(os.path.join(ROOT, "transformer_xl_relative_gb300", "csrc",
+                                                                  "txl_bwd_umma.cu"), "bwd_umma_kernel_large.json"),
+                         "traffic_kernel": "bwd_umma_kernel (ncu, bytes per launch)",
                          "bound": "tensor", "achieved": achieved, "peak": bf16_peak, "unit": "TFLOP/s",
                          "frac": achieved / bf16_peak, "algorithmic_flops_per_launch": f_attn,
                          "peak_source": peak_src + " bf16 burst"}}
