@@ -17,10 +17,11 @@
 //    local, window column c = i - j + 127 in [0, 255) over position rows 128 t - 127 + c).  It
 //    accumulates dq_ac = dS K and dq_bd = G R_win in TMEM over the sweep, where G, dS scattered
 //    by distance (G[i][i - j + 127] = dS_ij), sits in shared memory as the A operand of that
-//    product and, read transposed, of dr_win = G^T Qc''.  Its rows' sums of dq_ac and dq_bd are
-//    added into du and dv_bias.  The window's lower 128 rows are the
+//    product and, read transposed, of dr_win = G^T Qc''.  The window's lower 128 rows are the
 //    upper 128 of the tile before, so every block of 128 distance rows receives the products of
-//    two consecutive tiles and is added to dr (fp32 atomics) once.
+//    two consecutive tiles and is added to dr (fp32 atomics) once, while the next tile's score
+//    products run.  The sums of dq_ac and dq_bd over the CTA's queries are added into du and
+//    dv_bias.
 //  * a key CTA owns a key tile of the current segment and sweeps the query tiles that see it,
 //    with dv += P^T dO and dk += dS^T Qc' accumulated in TMEM (P and dS in shared memory, read
 //    transposed): every key has one owner, so dk and dv are written once, without atomics.
@@ -69,8 +70,8 @@ struct USmem {
     static constexpr int X = R + 3 * kTileBytes;           // query CTA: G, 4 atoms [128][64];
                                                            // key CTA: P, 2 atoms, then dS, 2 atoms;
                                                            // first the W stage [128][kStagePitch] words
-    static constexpr int Bar = X + 4 * kTileBytes;
-    static constexpr int Misc = Bar + 8;                   // TMEM base, abort flag
+    static constexpr int Bar = X + 4 * kTileBytes;         // MMA completion, drain
+    static constexpr int Misc = Bar + 16;                  // TMEM base, abort flag
     static constexpr int Csum = Misc + 16;                 // float [4][128]
     static constexpr int Bias = Csum + 4 * 128 * 4;        // float [2][64]: c u, c v_bias
     static constexpr int Size = Bias + 2 * 64 * 4;
@@ -280,10 +281,15 @@ __global__ void __launch_bounds__(kUThreads, 1) bwd_umma_kernel(const __grid_con
     uint32_t* srow = reinterpret_cast<uint32_t*>(sm + USmem::X) + li * kStagePitch;
     if (tid == 0) {
         mbar_init(bar, 1);
+        mbar_init(bar + 1, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(tmem_holder, 512);
+    // set (by thread 0, only inside its bounded waits, read by all after the CTA barrier that
+    // follows them) once a wait gave up: every later wait returns at once, so the sweep runs out
+    // without waiting, and no result is written
+    auto aborted = [&]() { return *reinterpret_cast<volatile int*>(abort_flag) != 0; };
 
     // sweep geometry: step t pairs query tile i0 with the key tile starting at j0 = M + i0 - 128 t
     const int n_steps = key_cta ? n_qt - own : (M + 128 * own + 127 - a.lo) / 128 + 1;
@@ -630,7 +636,10 @@ __global__ void __launch_bounds__(kUThreads, 1) bwd_umma_kernel(const __grid_con
         tc_fence_before();
     }
 
-    if (!key_cta) {
+    const bool failed = aborted();
+    if (failed) {
+        // a wait gave up: no result is written; every copy and product in flight lands first
+    } else if (!key_cta) {
         // the last tile's upper block
         {
             __syncthreads();                              // the last step's staged rows are added
@@ -729,6 +738,13 @@ __global__ void __launch_bounds__(kUThreads, 1) bwd_umma_kernel(const __grid_con
         }
     }
     (void)ok;
+    mma::cp_async_wait_all();
+    if (failed && tid == 0) {
+        int never = 0;
+        const WaitCtl dw{&never, nullptr, 100000000ull};
+        umma_commit(bar + 1);                             // arrives once every issued MMA is complete
+        (void)mbar_wait(bar + 1, 0, dw, 9);
+    }
 
     tc_fence_before();
     __syncthreads();

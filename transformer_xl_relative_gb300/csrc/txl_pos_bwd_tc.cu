@@ -39,8 +39,8 @@ struct PBSmem {
     static constexpr int Stages = 0;                 // two stages: A_hi, A_lo, B_hi, B_lo
     static constexpr int Ws = Stages + 2 * kPBStage; // double [128]
     static constexpr int Wf = Ws + kPBM * 8;         // float [128]
-    static constexpr int Bars = Wf + kPBM * 4;       // two mbarriers
-    static constexpr int Misc = Bars + 16;           // TMEM base, abort flag
+    static constexpr int Bars = Wf + kPBM * 4;       // two stage mbarriers, drain
+    static constexpr int Misc = Bars + 24;           // TMEM base, abort flag
     static constexpr int Size = Misc + 16;
 };
 static_assert(kPBM * kOutPitch * 4 <= 2 * kPBStage, "output staging inside the stages");
@@ -68,6 +68,7 @@ __global__ void __launch_bounds__(kPBThreads, 1) pos_bwd_tc_kernel(const __grid_
     if (tid == 0) {
         mbar_init(&bar[0], 1);
         mbar_init(&bar[1], 1);
+        mbar_init(&bar[2], 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -100,6 +101,7 @@ __global__ void __launch_bounds__(kPBThreads, 1) pos_bwd_tc_kernel(const __grid_
         if (c >= 2) {                                     // the products that read this stage are done
             if (tid == 0) (void)mbar_spin(&bar[s], ((c - 2) >> 1) & 1, wc, 1);
             __syncthreads();
+            if (*reinterpret_cast<volatile int*>(abort_flag)) break;
         }
         const int d0 = d_lo + c * kPBChunk;
         // ---- R^T chunk: A[ms][dl] = sin, A[ms + 1][dl] = cos, dl = 4 ag + e (anchor distance 4 ag)
@@ -164,9 +166,13 @@ __global__ void __launch_bounds__(kPBThreads, 1) pos_bwd_tc_kernel(const __grid_
             umma_commit(&bar[s]);
         }
     }
-    if (nch > 0) {
+    if (nch > 0 && !*reinterpret_cast<volatile int*>(abort_flag)) {
         if (tid == 0) (void)mbar_spin(&bar[(nch - 1) & 1], ((nch - 1) >> 1) & 1, wc, 2);
         __syncthreads();
+    }
+    // set only inside thread 0's bounded waits, read by all after the CTA barrier that follows them
+    const bool failed = *reinterpret_cast<volatile int*>(abort_flag) != 0;
+    if (nch > 0 && !failed) {
         tc_fence_after();
         // ---- the tile through shared memory: warp w reads lane quarter w mod 4, columns 64 (w / 4) ..
         float* out = reinterpret_cast<float*>(sm + PBSmem::Stages);
@@ -209,6 +215,13 @@ __global__ void __launch_bounds__(kPBThreads, 1) pos_bwd_tc_kernel(const __grid_
                 }
             }
         }
+    }
+    if (failed && tid == 0) {
+        // a wait gave up: every issued product completes before the TMEM is released
+        int never = 0;
+        const WaitCtl dw{&never, nullptr, 100000000ull};
+        umma_commit(&bar[2]);
+        (void)mbar_wait(&bar[2], 0, dw, 3);
     }
     tc_fence_before();
     __syncthreads();
