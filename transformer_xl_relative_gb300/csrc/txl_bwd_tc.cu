@@ -8,6 +8,9 @@
 //   dr[delta] = scale sum_{delta_ij = delta} dS_ij q''_i,   q' = q + u,  q'' = q + v_bias,
 // with delta_ij = min(M + i - j, clamp_len).
 //
+// This is the mma.sync path: txl_bwd_umma.cu's tcgen05 kernel takes the bf16 d_head 64 calls whose
+// row log-sum-exp is given and whose gradient buffers are 16-byte aligned; the rest come here.
+//
 // One CTA of four warps per (query tile of 64, head, batch entry); warp w owns query rows
 // 16w .. 16w + 15.  Key tiles of 64 are aligned to the query tile (tile t covers keys
 // j0 = M + i0 - 64 t ...), so the distances of tile t fill a window of 127 position rows starting
