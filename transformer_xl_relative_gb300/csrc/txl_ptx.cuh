@@ -239,14 +239,6 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, int c0, int
     asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];"
                  ::"l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(src)) : "memory");
 }
-// Element-wise fp32 add of `bytes` bytes of shared memory into global memory (TMA bulk
-// reduction; both addresses 16-byte aligned, bytes a multiple of 16).
-__device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, uint32_t ssrc, uint32_t bytes)
-{
-    asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;"
-                 ::"l"(gdst), "r"(ssrc), "r"(bytes) : "memory");
-}
-
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until at most N committed groups of this thread still read their shared-memory source.
 template <int N>
