@@ -901,7 +901,6 @@ txl_status txl_rel_attn_bwd_lse(int B, int L, int H, int D, int clamp_len, const
     if (clamp_len < 0 || !u || !v_bias || !view_ok(d_out)) return TXL_ERR_INVALID_ARG;
     if (!dq || !dk_cur || !dv_cur || !du || !dv_bias || !dr) return TXL_ERR_INVALID_ARG;
     const int M = (mem && mem->M > 0) ? mem->M : 0;
-    const int valid = M > 0 ? mem->valid : 0;
     const int need_rows = std::min(M + L, clamp_len + 1);
     if (n_rows < need_rows) return TXL_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -919,7 +918,6 @@ txl_status txl_rel_attn_bwd_lse(int B, int L, int H, int D, int clamp_len, const
     if (scale <= 0.f) scale = 1.0f / std::sqrt(static_cast<float>(D));
     BwdParams p = bwd_params(B, L, H, D, clamp_len, q, mem, k_cur, v_cur, u, v_bias, r, ld_r, n_rows, scale, out,
                              d_out, dq, dk_cur, dv_cur, du, dv_bias, dr);
-    (void)valid;
     const size_t rows = static_cast<size_t>(B) * L * H;
     float* ws = static_cast<float*>(workspace);
     p.lse = ws;
