@@ -234,6 +234,56 @@ def test_rejections_before_any_launch(native):
     assert lib.txl_selftest_wait_timeout(None, 10, None) == native.TXL_ERR_INVALID_ARG
 
 
+def test_gradient_entry_points_reject_before_any_launch(native):
+    """The saved-statistics forward, the two backward entry points and dW_R validate on the host:
+    every call below returns its status before any CUDA work."""
+    lib = native.load()
+    V = native.TxlView
+    B, L, H, D = 2, 8, 1, 64
+    q = V(FAKE, L * H * D, H * D, D)
+    nullv = V(None, 1, 1, 1)
+    bq = ctypes.byref(q)
+
+    def fwd_lse(lse, dtype=1, D=D, n_rows=16):
+        return lib.txl_rel_attn_fwd_lse(B, L, H, D, 16, bq, None, bq, bq, FAKE, FAKE, FAKE, D, n_rows, 0.0, bq,
+                                        lse, dtype, None, 0, None, None)
+
+    assert fwd_lse(None) == native.TXL_ERR_INVALID_ARG               # no statistics buffer
+    assert fwd_lse(FAKE + 2) == native.TXL_ERR_ALIGNMENT             # statistics not 4-byte aligned
+    assert fwd_lse(FAKE, n_rows=4) == native.TXL_ERR_INVALID_ARG     # min(M + L, clamp + 1) = 8 rows of r
+    assert fwd_lse(FAKE, dtype=0) == native.TXL_ERR_UNSUPPORTED      # fp32: only the fused bf16 kernel saves them
+    assert fwd_lse(FAKE, D=128) == native.TXL_ERR_UNSUPPORTED        # d_head above 64
+
+    need = lib.txl_rel_attn_bwd_workspace_size(B, L, H, D)
+    rows = B * L * H
+    assert need == rows * 2 * 4 + rows * D * 2 * 4                   # lse, D_i, and two fp32 [rows][D] parts
+    assert lib.txl_rel_attn_bwd_workspace_size(0, L, H, D) == 0
+
+    def bwd_lse(lse=None, dq=FAKE, d_out=q, ws=FAKE, ws_bytes=need, n_rows=16):
+        return lib.txl_rel_attn_bwd_lse(B, L, H, D, 16, bq, None, bq, bq, FAKE, FAKE, FAKE, D, n_rows, 0.0, bq,
+                                        ctypes.byref(d_out), lse, dq, FAKE, FAKE, FAKE, FAKE, FAKE, 1, ws,
+                                        ws_bytes, None)
+
+    assert bwd_lse(lse=FAKE + 2) == native.TXL_ERR_ALIGNMENT
+    assert bwd_lse(dq=None) == native.TXL_ERR_INVALID_ARG
+    assert bwd_lse(d_out=nullv) == native.TXL_ERR_INVALID_ARG
+    assert bwd_lse(n_rows=4) == native.TXL_ERR_INVALID_ARG
+    assert bwd_lse(ws=None, ws_bytes=0) == native.TXL_ERR_WORKSPACE
+    assert bwd_lse(ws_bytes=need - 16) == native.TXL_ERR_WORKSPACE
+    assert bwd_lse(ws=FAKE + 4) == native.TXL_ERR_ALIGNMENT          # workspace not 16-byte aligned
+    # the entry point without statistics applies the same checks
+    assert lib.txl_rel_attn_bwd(B, L, H, D, 16, bq, None, bq, bq, FAKE, FAKE, FAKE, D, 16, 0.0, bq, bq,
+                                FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, None, 0, None) == native.TXL_ERR_WORKSPACE
+
+    # dW_R: d_model even and at least 2, a destination, a row stride holding H * D columns, dr when
+    # there are rows
+    assert lib.txl_rel_pos_bwd(16, 15, 2, 8, FAKE, FAKE, 16, None) == native.TXL_ERR_INVALID_ARG
+    assert lib.txl_rel_pos_bwd(16, 0, 2, 8, FAKE, FAKE, 16, None) == native.TXL_ERR_INVALID_ARG
+    assert lib.txl_rel_pos_bwd(16, 16, 2, 8, FAKE, FAKE, 15, None) == native.TXL_ERR_INVALID_ARG
+    assert lib.txl_rel_pos_bwd(16, 16, 2, 8, FAKE, None, 16, None) == native.TXL_ERR_INVALID_ARG
+    assert lib.txl_rel_pos_bwd(16, 16, 2, 8, None, FAKE, 16, None) == native.TXL_ERR_INVALID_ARG
+
+
 def test_empty_batch_is_a_no_op(native):
     lib = native.load()
     q = native.TxlView(FAKE, 1, 1, 1)
